@@ -1,0 +1,297 @@
+"""Pins for the fp64 oracle: checks against facts that do not come from the
+oracle itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with what the pages or the mathematics fix:
+
+* values the pages print for worked examples (``tests/golden``);
+* closed forms derived by hand from the definitions (identities that hold for
+  any input, special inputs with a known answer);
+* central finite differences of the forward, which pin the backward to the
+  forward without restating the backward formula;
+* an independent library implementation (PyTorch's ``rms_norm`` with autograd
+  in float64 on the CPU).
+
+The same functions run against deliberately broken copies of the oracle in
+``test_oracle_mutants.py``; every plausible mistake must trip at least one.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_examples.json")
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return {c["name"]: c for c in json.load(f)["cases"]}
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _rows(M, N, seed, scale=1.0):
+    return _rng(seed).standard_normal((M, N)) * scale
+
+
+# ---------------------------------------------------------------- printed values
+
+def pin_printed_two_columns(o):
+    """hello-gpu ch. 13 section 13.1: x=[3,4], w=[1,1], eps=1e-5 -> r~0.2828,
+    y~[0.8485, 1.1314]; the sum of squares is 25 and its mean 12.5."""
+    c = _golden()["two_columns"]
+    p = c["printed"]
+    y, r = o.fwd(np.array([c["x"]]), np.array(c["w"]), c["eps"])
+    d = c["decimals"]
+    assert np.allclose(np.round(y[0], d), p["y"], atol=0, rtol=0), y
+    assert round(float(r[0]), d) == p["r"], r
+    mean_square = 1.0 / float(r[0]) ** 2 - c["eps"]
+    assert abs(mean_square - p["mean_square"]) < 1e-9, mean_square
+    assert abs(mean_square * len(c["x"]) - p["sum_of_squares"]) < 1e-9
+
+
+def pin_printed_four_columns(o):
+    """hello-gpu ch. 13 Figure 13.1: x=[3,4,-3,-4], w=[1,.5,2,1], eps=1e-5 ->
+    sum of squares 50, mean over the 4 valid columns 12.5, r~0.2828,
+    second output 4 * 0.2828 * 0.5 ~ 0.5657; every output shares r and keeps
+    its input's sign."""
+    c = _golden()["four_columns_with_weights"]
+    p = c["printed"]
+    x, w = np.array([c["x"]]), np.array(c["w"])
+    y, r = o.fwd(x, w, c["eps"])
+    d = c["decimals"]
+    assert round(float(y[0, p["y_index"]]), d) == p["y_at_index"], y
+    assert round(float(r[0]), d) == p["r"], r
+    mean_square = 1.0 / float(r[0]) ** 2 - c["eps"]
+    assert abs(mean_square - p["mean_square"]) < 1e-9, mean_square
+    assert abs(mean_square * 4 - p["sum_of_squares"]) < 1e-9
+    assert np.all(np.sign(y[0]) == np.sign(x[0])), y
+    # one shared scale: y_j / (x_j w_j) is the same r for every column
+    assert np.allclose(y[0] / (x[0] * w), r[0], rtol=1e-14, atol=0)
+
+
+# ---------------------------------------------------------------- closed forms
+
+def pin_zero_input(o):
+    """All-zero rows give all-zero outputs and r = eps^(-1/2) (hello-gpu 13.4)."""
+    eps = 1e-5
+    x = np.zeros((3, 7))
+    w = _rng(1).standard_normal(7)
+    y, r = o.fwd(x, w, eps)
+    assert np.all(y == 0.0)
+    assert np.allclose(r, 1.0 / math.sqrt(eps), rtol=1e-15, atol=0), r
+
+
+def pin_zero_weight(o):
+    """All-zero weights give y = 0 (hello-gpu 13.4) and, since g = dy*w = 0,
+    dx = 0."""
+    x = _rows(4, 9, 2)
+    w = np.zeros(9)
+    dy = _rows(4, 9, 3)
+    y, _ = o.fwd(x, w, 1e-5)
+    dx = o.bwd_dx(x, w, dy, 1e-5)
+    assert np.all(y == 0.0)
+    assert np.all(dx == 0.0)
+
+
+def pin_constant_row(o):
+    """x = a*1 gives r = 1/sqrt(a^2 + eps), so y = a*w/sqrt(a^2 + eps)."""
+    for a, eps in ((2.5, 1e-5), (-0.75, 1e-2), (1e-3, 1e-6)):
+        N = 11
+        x = np.full((1, N), a)
+        w = _rng(4).standard_normal(N)
+        y, r = o.fwd(x, w, eps)
+        assert math.isclose(r[0], 1.0 / math.sqrt(a * a + eps), rel_tol=1e-14)
+        assert np.allclose(y[0], a * w / math.sqrt(a * a + eps), rtol=1e-13, atol=0)
+
+
+def pin_scale_invariance(o):
+    """With eps = 0, y(alpha*x) = y(x) for alpha > 0; with eps != 0 it is not
+    exactly invariant (hello-gpu 13.4)."""
+    x = _rows(3, 17, 5)
+    w = _rng(6).standard_normal(17)
+    y1, _ = o.fwd(x, w, 0.0)
+    y2, _ = o.fwd(3.7 * x, w, 0.0)
+    assert np.allclose(y1, y2, rtol=1e-13, atol=1e-15)
+    small = x * 1e-3  # mean square ~1e-6, comparable with eps
+    y3, _ = o.fwd(small, w, 1e-6)
+    y4, _ = o.fwd(2.0 * small, w, 1e-6)
+    assert not np.allclose(y3, y4, rtol=1e-3, atol=0)
+
+
+def pin_backward_two_columns(o):
+    """Derived by hand from the definitions: x=[3,4], w=[1,1], dy=[1,0], eps=0.
+    r = 1/sqrt(12.5), xhat = [0.8485281, 1.1313708], mean(g*xhat) = 0.4242641,
+    dx = r*([1,0] - xhat*0.4242641) = r*[0.64, -0.48], dw = [0.8485281, 0]."""
+    x = np.array([[3.0, 4.0]])
+    w = np.array([1.0, 1.0])
+    dy = np.array([[1.0, 0.0]])
+    r = 1.0 / math.sqrt(12.5)
+    dx = o.bwd_dx(x, w, dy, 0.0)
+    dw = o.bwd_dw(x, dy, 0.0)
+    assert np.allclose(dx[0], [0.64 * r, -0.48 * r], rtol=1e-13, atol=1e-16), dx
+    assert np.allclose(dw, [3.0 * r, 0.0], rtol=1e-13, atol=1e-16), dw
+
+
+def pin_dx_orthogonal_to_x(o):
+    """sum_j dx_ij x_ij = eps * r_i^3 * sum_j g_ij x_ij (derived from the
+    definitions); exactly zero when eps = 0."""
+    M, N = 5, 23
+    x = _rows(M, N, 7)
+    w = 1.0 + 0.1 * _rng(8).standard_normal(N)
+    dy = _rows(M, N, 9)
+    for eps in (0.0, 1e-6, 0.25):
+        dx = o.bwd_dx(x, w, dy, eps)
+        _, r = o.fwd(x, w, eps)
+        lhs = np.sum(dx * x, axis=1)
+        rhs = eps * r ** 3 * np.sum(dy * w * x, axis=1)
+        scale = np.sum(np.abs(dy * w * x), axis=1) * r
+        assert np.all(np.abs(lhs - rhs) <= 1e-12 * scale), (eps, lhs, rhs)
+
+
+def pin_dy_equal_y(o):
+    """dy = y, w = 1, eps = 0 gives dx = 0 (g = xhat and mean(xhat^2) = 1)."""
+    M, N = 3, 19
+    x = _rows(M, N, 10)
+    w = np.ones(N)
+    y, _ = o.fwd(x, w, 0.0)
+    dx = o.bwd_dx(x, w, y, 0.0)
+    assert np.max(np.abs(dx)) < 1e-14, np.max(np.abs(dx))
+
+
+def pin_single_row_dw(o):
+    """One row: dw_j = dy_j * xhat_j = dy_j * y_j / w_j, tying dw to the
+    forward output."""
+    N = 13
+    x = _rows(1, N, 11)
+    w = 1.0 + 0.1 * _rng(12).standard_normal(N)
+    dy = _rows(1, N, 13)
+    y, _ = o.fwd(x, w, 1e-5)
+    dw = o.bwd_dw(x, dy, 1e-5)
+    assert np.allclose(dw, dy[0] * y[0] / w, rtol=1e-13, atol=0)
+
+
+def pin_dw_sums_rows(o):
+    """dw over M rows is the sum of the single-row weight gradients."""
+    M, N = 6, 10
+    x = _rows(M, N, 14)
+    dy = _rows(M, N, 15)
+    total = o.bwd_dw(x, dy, 1e-5)
+    parts = sum(o.bwd_dw(x[i:i + 1], dy[i:i + 1], 1e-5) for i in range(M))
+    assert np.allclose(total, parts, rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------- finite differences
+
+def pin_finite_differences(o):
+    """dx and dw equal the central differences of L = sum(dy * y) (forward
+    only), h = 1e-6, in float64."""
+    h = 1e-6
+    for (M, N, eps, seed) in ((1, 3, 1e-5, 20), (3, 8, 1e-6, 21), (4, 16, 0.5, 22), (2, 5, 0.0, 23)):
+        x = _rows(M, N, seed)
+        w = 1.0 + 0.3 * _rng(seed + 100).standard_normal(N)
+        dy = _rows(M, N, seed + 200)
+
+        def loss(xx, ww):
+            y, _ = o.fwd(xx, ww, eps)
+            return float(np.sum(dy * y))
+
+        fd_x = np.zeros_like(x)
+        for i in range(M):
+            for j in range(N):
+                xp, xm = x.copy(), x.copy()
+                xp[i, j] += h
+                xm[i, j] -= h
+                fd_x[i, j] = (loss(xp, w) - loss(xm, w)) / (2 * h)
+        fd_w = np.zeros(N)
+        for j in range(N):
+            wp, wm = w.copy(), w.copy()
+            wp[j] += h
+            wm[j] -= h
+            fd_w[j] = (loss(x, wp) - loss(x, wm)) / (2 * h)
+        dx = o.bwd_dx(x, w, dy, eps)
+        dw = o.bwd_dw(x, dy, eps)
+        tol_x = 1e-7 * max(1.0, np.max(np.abs(fd_x)))
+        tol_w = 1e-7 * max(1.0, np.max(np.abs(fd_w)))
+        assert np.max(np.abs(dx - fd_x)) < tol_x, (M, N, np.max(np.abs(dx - fd_x)))
+        assert np.max(np.abs(dw - fd_w)) < tol_w, (M, N, np.max(np.abs(dw - fd_w)))
+
+
+# ------------------------------------------------ independent library routine
+
+def pin_torch_rms_norm(o):
+    """PyTorch's CPU float64 rms_norm with autograd agrees to ~1e-12."""
+    import torch
+    import torch.nn.functional as F
+
+    for (M, N, eps, seed) in ((7, 33, 1e-6, 30), (2, 128, 1e-5, 31), (5, 4, 1e-2, 32)):
+        g = torch.Generator().manual_seed(seed)
+        x = torch.randn(M, N, dtype=torch.float64, generator=g)
+        w = 1.0 + 0.1 * torch.randn(N, dtype=torch.float64, generator=g)
+        dy = torch.randn(M, N, dtype=torch.float64, generator=g)
+        xt, wt = x.clone().requires_grad_(True), w.clone().requires_grad_(True)
+        yt = F.rms_norm(xt, (N,), wt, eps)
+        yt.backward(dy)
+        y, _ = o.fwd(x, w, eps)
+        dx = o.bwd_dx(x, w, dy, eps)
+        dw = o.bwd_dw(x, dy, eps)
+        assert np.allclose(y, yt.detach().numpy(), rtol=1e-12, atol=1e-14)
+        assert np.allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-13)
+        assert np.allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+# ------------------------------------------------------ input decoding, rows
+
+def pin_bf16_decoding(o):
+    """bf16 bit patterns decode exactly: 0x3F80 = 1, 0xC040 = -3,
+    0x4049 = 3.140625, 0x0001 = 2^-133 (a subnormal); the oracle sees the same
+    values whether they arrive as bf16 bits, fp32 or fp64."""
+    bits = np.array([[0x3F80, 0xC040, 0x4049, 0x0001]], dtype=np.uint16)
+    vals = np.array([[1.0, -3.0, 3.140625, 2.0 ** -133]])
+    wb = np.array([0x3F80, 0x3F80, 0x3F80, 0x3F80], dtype=np.uint16)
+    y_b, r_b = o.fwd(bits, wb, 1e-5, dtype="bf16")
+    y_d, r_d = o.fwd(vals, np.ones(4), 1e-5)
+    y_f, r_f = o.fwd(vals.astype(np.float32), np.ones(4, dtype=np.float32), 1e-5)
+    assert np.array_equal(y_b, y_d) and np.array_equal(r_b, r_d), (y_b, y_d)
+    assert np.array_equal(y_f, y_d) and np.array_equal(r_f, r_d)
+
+
+def pin_row_selection(o):
+    """A requested row list returns exactly those rows, in the order given."""
+    x = _rows(6, 5, 40)
+    w = _rng(41).standard_normal(5)
+    dy = _rows(6, 5, 42)
+    y_all, r_all = o.fwd(x, w, 1e-5)
+    dx_all = o.bwd_dx(x, w, dy, 1e-5)
+    rows = [5, 0, 3]
+    y, r = o.fwd(x, w, 1e-5, rows=rows)
+    dx = o.bwd_dx(x, w, dy, 1e-5, rows=rows)
+    assert np.array_equal(y, y_all[rows]) and np.array_equal(r, r_all[rows])
+    assert np.array_equal(dx, dx_all[rows])
+    # each row is computed from itself only
+    y_last, _ = o.fwd(x[5:6], w, 1e-5)
+    assert np.array_equal(y_last[0], y_all[5])
+
+
+ALL_PINS = [
+    pin_printed_two_columns,
+    pin_printed_four_columns,
+    pin_zero_input,
+    pin_zero_weight,
+    pin_constant_row,
+    pin_scale_invariance,
+    pin_backward_two_columns,
+    pin_dx_orthogonal_to_x,
+    pin_dy_equal_y,
+    pin_single_row_dw,
+    pin_dw_sums_rows,
+    pin_finite_differences,
+    pin_torch_rms_norm,
+    pin_bf16_decoding,
+    pin_row_selection,
+]

@@ -1,0 +1,77 @@
+"""Every plausible mistake planted in a copy of the oracle trips a pin.
+
+Each mutant is a textual edit of the oracle's C source, compiled into a
+temporary library on the CPU; the real source is never modified. A mutant
+that passes every pin would mean the pins cannot tell that mistake apart from
+a correct oracle.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "rmsnorm_oracle.c")
+
+# (name, text to replace, replacement, which occurrence (0-based) or None = all)
+MUTANTS = [
+    ("eps_dropped", "sum_sq / (double)N + eps", "sum_sq / (double)N", None),
+    ("eps_outside_sqrt", "1.0 / sqrt(sum_sq / (double)N + eps)",
+     "1.0 / sqrt(sum_sq / (double)N) + eps", None),
+    ("mean_over_padded_width", "sum_sq / (double)N", "sum_sq / (double)(N + 1)", None),
+    ("no_square_root", "1.0 / sqrt(", "1.0 / (", None),
+    ("sum_not_squared", "sum_sq += v * v;", "sum_sq += v;", None),
+    ("fwd_weight_by_row", "load_as_double(w, dtype, j);\n    }\n    return ORACLE_OK;",
+     "load_as_double(w, dtype, i);\n    }\n    return ORACLE_OK;", None),
+    ("fwd_weight_dropped", "* r *\n                                   load_as_double(w, dtype, j);",
+     "* r;", None),
+    ("dx_sign_flipped", "r * (g - xhat * c)", "r * (g + xhat * c)", None),
+    ("dx_correction_dropped", "r * (g - xhat * c)", "r * g", None),
+    ("dx_outer_r_dropped", "r * (g - xhat * c)", "(g - xhat * c)", None),
+    ("dx_mean_not_divided", "c /= (double)N;", "", None),
+    ("dx_gain_dropped", "double g = load_as_double(dy, dtype, i * N + j) *\n"
+                        "                       load_as_double(w, dtype, j);\n"
+                        "            dx_out", "double g = load_as_double(dy, dtype, i * N + j);\n"
+                                            "            dx_out", None),
+    ("dx_x_for_dy", "double g = load_as_double(dy, dtype, i * N + j) *\n"
+                    "                       load_as_double(w, dtype, j);\n            c +=",
+     "double g = load_as_double(x, dtype, i * N + j) *\n"
+     "                       load_as_double(w, dtype, j);\n            c +=", None),
+    ("dw_extra_r", "dw_out[j] += load_as_double(dy, dtype, i * N + j) * xhat;",
+     "dw_out[j] += load_as_double(dy, dtype, i * N + j) * xhat * r;", None),
+    ("dw_x_for_dy", "dw_out[j] += load_as_double(dy,", "dw_out[j] += load_as_double(x,", None),
+    ("dw_last_row_skipped", "for (i = 0; i < M; ++i) {", "for (i = 0; i + 1 < M; ++i) {", None),
+    ("dw_transposed_index", "dw_out[j] += load_as_double(dy, dtype, i * N + j)",
+     "dw_out[j] += load_as_double(dy, dtype, j * M + i)", None),
+    ("bf16_wrong_shift", "<< 16;", "<< 15;", None),
+    ("row_selection_ignored", "return rows ? rows[k] : k;", "return k;", None),
+]
+
+
+def _mutant_source(old, new, which):
+    src = open(SRC).read()
+    count = src.count(old)
+    assert count >= 1, f"mutation anchor not found: {old!r}"
+    if which is None:
+        return src.replace(old, new)
+    parts = src.split(old)
+    return old.join(parts[:which + 1]) + new + old.join(parts[which + 1:])
+
+
+@pytest.mark.parametrize("name,old,new,which", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, which):
+    src = tmp_path / f"{name}.c"
+    src.write_text(_mutant_source(old, new, which))
+    lib_path = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", str(lib_path),
+                    str(src), "-lm"], check=True)
+    mutant = oracle.Oracle(oracle.load(str(lib_path)))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError) as e:
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"mutant {name} passed every pin"
