@@ -1,0 +1,582 @@
+#!/usr/bin/env python3
+"""RMSNorm forward + backward throughput on GB300: GB/s of logical bytes and
+the fraction of the HBM roofline.
+
+One step = one forward (x, w -> y, rstd) and one backward (x, w, dy, rstd ->
+dx, dw) over the whole workload, both through the C ABI of librmsnorm.so.
+Timing rules:
+  * every call is validated (against a float32 PyTorch reference on the GPU)
+    before anything is timed;
+  * inputs rotate through clone sets whose total size is >= 3x L2, and a
+    buffer of 2x L2 is overwritten before every timed call (outside the
+    events), so no call is served from L2;
+  * each call is bracketed by CUDA events on the stream it is launched on;
+  * the HBM roofline is measured in the same run (best of copy, pure write
+    and 2-read-1-write probes) before and after the timed region, to catch
+    drift; the measured copy bandwidth (MEASURED_PEAKS.json) is the
+    reported `roofline.peak`;
+  * SM clocks and throttle reasons are sampled with nvidia-smi during the
+    timed region.
+
+`--impl reference` times the fp64 CPU oracle (the slow, obviously correct
+restatement of the method) on the host cores, on a bounded sample of rows of
+the same workload.
+
+Multi-GPU (torchrun): RMSNorm rows are independent and every rank runs its
+own replica of the workload (weak scaling, no collective on the data path);
+the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm fwd+bwd GB/s and % of measured HBM roofline, bf16 M×N sweep"
+DEFAULT_WORKLOAD = "hidden4096_16384x4096"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------- setup
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU oracle budget for the cpu_baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--json-out", default=None, help="also write the JSON line to this file")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_profiled_traffic(kernel_tag: str, workload: str, source_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    h = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not h or not t or h.group(1) != source_hash:
+        return None
+    return int(t.group(1))
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampler around the timed region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 10:
+                continue
+            rec = [r.strip() for r in rec]
+            try:
+                ts = time.mktime(time.strptime(rec[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + rec[0].split(".")[1]) if "." in rec[0] else 0.0
+                rows.append({"t": ts + frac, "sm": float(rec[2]), "max": float(rec[3]),
+                             "power": float(rec[4]) if rec[4] not in ("[N/A]", "N/A") else None,
+                             "active": rec[5], "hw": rec[6], "hw_thermal": rec[7],
+                             "sw_thermal": rec[8], "sw_power": rec[9]})
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 - 0.15 <= r["t"] <= self.t1 + 0.15]
+        window = "timed_region"
+        if len(inside) < 2:
+            inside, window = rows, "whole_run"
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in inside):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["max"] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max((r["power"] for r in inside if r["power"] is not None),
+                                   default=None)}
+
+
+# ------------------------------------------------------------ GPU helpers
+
+def event_ms(a, b) -> float:
+    return a.elapsed_time(b)
+
+
+def run_probes(pkg, torch, nbytes: int, samples: int = 10):
+    """Best-of GB/s for copy, pure write and 2R1W over nbytes-sized buffers."""
+    dev = torch.cuda.current_device()
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    c = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    a.fill_(1)
+    b.fill_(2)
+    res = {}
+    moved = {pkg.PROBE_COPY: 2 * nbytes, pkg.PROBE_WRITE: nbytes, pkg.PROBE_2R1W: 3 * nbytes}
+    names = {pkg.PROBE_COPY: "copy", pkg.PROBE_WRITE: "write", pkg.PROBE_2R1W: "2r1w"}
+    for kind in (pkg.PROBE_COPY, pkg.PROBE_WRITE, pkg.PROBE_2R1W):
+        best = 0.0
+        for bps in (2, 4):
+            for _ in range(2):
+                pkg.check(pkg.rmsnorm_probe(kind, c, a, b, nbytes, bps), "probe")
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(samples):
+                e0.record()
+                pkg.check(pkg.rmsnorm_probe(kind, c, a, b, nbytes, bps), "probe")
+                e1.record()
+                e1.synchronize()
+                best = max(best, moved[kind] / (event_ms(e0, e1) * 1e-3) / 1e9)
+        res[names[kind]] = round(best, 1)
+    del a, b, c
+    torch.cuda.empty_cache()
+    res["best"] = max(res.values())
+    return res
+
+
+def validate(torch, x, w, dy, eps, y, rstd, dx, dw):
+    """Compare against a float32 PyTorch reference on the GPU (the check
+    happens before timing; tolerances as in the tests, bf16 rule for 16-bit
+    data)."""
+    import torch.nn.functional as F
+
+    N = x.shape[-1]
+    x32 = x.float().requires_grad_(True)
+    w32 = w.float().requires_grad_(True)
+    y32 = F.rms_norm(x32, (N,), w32, eps)
+    y32.backward(dy.float())
+    errs = {}
+    for name, got, ref in (("y", y, y32.detach()), ("dx", dx, x32.grad)):
+        err = (got.float() - ref).abs()
+        if x.dtype == torch.bfloat16:
+            bad = (err > 1e-2 * ref.abs() + 1e-3).sum().item()
+        else:
+            rms = ref.pow(2).mean(-1, keepdim=True).sqrt()
+            bad = (err > 1e-4 * ref.abs() + 1e-4 * rms).sum().item()
+        errs[name] = {"max_abs_err": float(err.max().item()), "bad": int(bad)}
+    r_ref = torch.rsqrt(x.float().pow(2).mean(-1) + eps)
+    errs["rstd"] = {"max_rel_err": float(((rstd - r_ref).abs() / r_ref).max().item())}
+    dwr = w32.grad
+    errs["dw"] = {"rel_l2": float(((dw - dwr).norm() / dwr.norm()).item())}
+    ok = errs["y"]["bad"] == 0 and errs["dx"]["bad"] == 0 and errs["rstd"]["max_rel_err"] < 1e-4 \
+        and errs["dw"]["rel_l2"] < 1e-3
+    return ok, errs
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def cpu_baseline(wl, budget_s: float, x_host=None, w_host=None, dy_host=None):
+    """Times the fp64 CPU oracle, as it stands, on the first rows of the
+    workload (single thread). Returns GB/s of logical bytes over the rows it
+    covered."""
+    import numpy as np
+    import torch
+
+    import oracle  # the one place bench.py uses the oracle
+    from memory_bound_normalization_gb300 import synth
+
+    oracle.build()
+    elem = 2 if wl.dtype == torch.bfloat16 else 4
+    if x_host is None:
+        inp = synth.make_inputs(wl, device="cpu", M=min(wl.M, 4096))
+        x_host, w_host, dy_host = inp["x"], inp["w"], inp["dy"]
+    avail = x_host.shape[0]
+
+    def one(rows):
+        t0 = time.perf_counter()
+        oracle.fwd(x_host[:rows], w_host, wl.eps)
+        oracle.bwd_dx(x_host[:rows], w_host, dy_host[:rows], wl.eps)
+        oracle.bwd_dw(x_host[:rows], dy_host[:rows], wl.eps)
+        return time.perf_counter() - t0
+
+    probe_rows = max(1, min(avail, 16))
+    t = one(probe_rows)
+    per_row = t / probe_rows
+    rows = int(max(1, min(avail, budget_s / max(per_row, 1e-9))))
+    t = one(rows)
+    fb, bb = synth.logical_bytes(rows, wl.N, elem)
+    del np
+    return {"value": round((fb + bb) / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {wl.M} rows x {wl.N} ({wl.dtype_name}); fwd + dx + dw "
+                      f"in fp64, single thread, {t:.1f} s"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+
+    import memory_bound_normalization_gb300 as pkg
+    from memory_bound_normalization_gb300 import build as libbuild
+    from memory_bound_normalization_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    pkg.load_library()  # raises if librmsnorm.so is missing
+    wl = synth.WORKLOADS[args.workload]
+    M, N, eps = wl.M, wl.N, wl.eps
+    code = pkg.dtype_code(wl.dtype)
+    elem = 2 if wl.dtype == torch.bfloat16 else 4
+    fwd_bytes, bwd_bytes = synth.logical_bytes(M, N, elem)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+
+    peak, peak_src = read_peaks()
+    probes_open = run_probes(pkg, torch, 1 << 30)
+
+    # inputs, rotated over clone sets covering >= 3x L2
+    base = synth.make_inputs(wl, device=f"cuda:{local}")
+    set_bytes = (base["x"].numel() + base["dy"].numel()) * elem
+    nsets = max(2, -(-3 * l2 // set_bytes))
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+    outs = []
+    for _ in range(nsets):
+        outs.append({"y": torch.empty_like(base["x"]), "dx": torch.empty_like(base["x"]),
+                     "rstd": torch.empty(M, dtype=torch.float32, device=base["x"].device),
+                     "dw": torch.empty(N, dtype=torch.float32, device=base["x"].device)})
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=base["x"].device)
+    stream = torch.cuda.current_stream()
+
+    def fwd(i):
+        s, o = sets[i], outs[i]
+        return pkg.rmsnorm_fwd(s["x"], s["w"], o["y"], o["rstd"], M, N, eps, code, stream)
+
+    def bwd(i):
+        s, o = sets[i], outs[i]
+        return pkg.rmsnorm_bwd(s["x"], s["w"], s["dy"], o["rstd"], o["dx"], o["dw"], M, N, code,
+                               stream)
+
+    # validate every clone set before timing
+    for i in range(nsets):
+        pkg.check(fwd(i), "rmsnorm_fwd")
+        pkg.check(bwd(i), "rmsnorm_bwd")
+    st = pkg.rmsnorm_get_last_device_error(stream)
+    pkg.check(st, "device status")
+    ok, errs = validate(torch, sets[0]["x"], sets[0]["w"], sets[0]["dy"], eps, outs[0]["y"],
+                        outs[0]["rstd"], outs[0]["dx"], outs[0]["dw"])
+    if not ok:
+        raise SystemExit(f"validation failed before timing: {json.dumps(errs)}")
+    dw0 = outs[0]["dw"].clone()
+
+    for k in range(args.warmup):
+        i = k % nsets
+        flush.zero_()
+        pkg.check(fwd(i))
+        flush.zero_()
+        pkg.check(bwd(i))
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    region0.record(stream)
+    for k in range(K):
+        i = k % nsets
+        e = ev[k]
+        flush.zero_()
+        e[0].record(stream)
+        fwd(i)
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        bwd(i)
+        e[3].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    if dist is not None:
+        dist.barrier()
+    clock_info = clocks.stop()
+    st = pkg.rmsnorm_get_last_device_error(stream)
+    pkg.check(st, "device status after timing")
+    if not torch.equal(outs[0]["dw"], dw0):
+        raise SystemExit("dw changed between identical backward calls")
+
+    fwd_ms = [event_ms(e[0], e[1]) for e in ev]
+    bwd_ms = [event_ms(e[2], e[3]) for e in ev]
+    fwd_mean = sum(fwd_ms) / K
+    bwd_mean = sum(bwd_ms) / K
+    step_ms = fwd_mean + bwd_mean
+    region_ms = event_ms(region0, region1)
+    if dist is not None:
+        t = torch.tensor([step_ms, fwd_mean, bwd_mean], device=base["x"].device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, fwd_mean, bwd_mean = (float(v) for v in t.tolist())
+
+    probes_close = run_probes(pkg, torch, 1 << 30)
+
+    # end to end through pinned host buffers
+    e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes)
+    if dist is not None:
+        t = torch.tensor([e2e["step_ms"]], device=base["x"].device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["step_ms"] = float(t.item())
+        e2e["value"] = round(world * (fwd_bytes + bwd_bytes) / (e2e["step_ms"] * 1e-3) / 1e9, 2)
+
+    plan_f = pkg.rmsnorm_plan(M, N, code, pkg.PASS_FWD, local).as_dict()
+    plan_b = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD, local).as_dict()
+    value = world * (fwd_bytes + bwd_bytes) / (step_ms * 1e-3) / 1e9
+    bwd_gbs = bwd_bytes / (bwd_mean * 1e-3) / 1e9
+    fwd_gbs = fwd_bytes / (fwd_mean * 1e-3) / 1e9
+    traffic = read_profiled_traffic("rmsnorm_bwd", wl.name, libbuild.source_hash())
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype_name,
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name, "M": M, "N": N, "eps": eps, "io_dtype": wl.dtype_name,
+            "accumulate": "f32", "rstd_dw_dtype": "f32", "about": wl.about,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"inputs rotated over {nsets} clone sets ({nsets * set_bytes >> 20} MiB, "
+                  f">= 3x L2 of {l2 >> 20} MiB) and a {2 * l2 >> 20} MiB write before every "
+                  "timed call, outside the events",
+            "logical_bytes": {"fwd": fwd_bytes, "bwd": bwd_bytes},
+        },
+        "fwd": {"ms": round(fwd_mean, 5), "gbs": round(fwd_gbs, 1),
+                "frac_of_peak": round(fwd_gbs / peak, 4),
+                "frac_of_probe": round(fwd_gbs / probes_open["best"], 4), "plan": plan_f},
+        "bwd": {"ms": round(bwd_mean, 5), "gbs": round(bwd_gbs, 1),
+                "frac_of_peak": round(bwd_gbs / peak, 4),
+                "frac_of_probe": round(bwd_gbs / probes_open["best"], 4), "plan": plan_b,
+                "workspace_bytes_overhead": 2 * plan_b["workspace_bytes"]},
+        "frac_of_peak": round(value / world / peak, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "rmsnorm_bwd (persistent kernel + fixed-order column sum, one call)",
+            "achieved": round(bwd_gbs, 1),
+            "peak": peak,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6800 GB/s",
+            "unit": "GB/s",
+            "frac": round(bwd_gbs / peak, 4),
+            "traffic": traffic,
+        },
+        "probes": {"open": probes_open, "close": probes_close,
+                   "close_over_open": round(probes_close["best"] / probes_open["best"], 4)},
+        "timed_region_ms": round(region_ms, 3),
+        "clocks": clock_info,
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "validation": errs,
+        "library": {"path": pkg.library_path(), "source_hash": libbuild.source_hash(),
+                    "version": pkg.rmsnorm_version()},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def run_e2e(pkg, torch, wl, base, code, stream, steps, logical):
+    """Same work through the C ABI with the inputs in pinned host memory: each
+    step copies x, w, dy to the device, runs forward and backward, and copies
+    y, rstd, dx, dw back."""
+    M, N, eps = wl.M, wl.N, wl.eps
+    hx = base["x"].cpu().pin_memory()
+    hw = base["w"].cpu().pin_memory()
+    hdy = base["dy"].cpu().pin_memory()
+    dx_in, dw_in, ddy_in = torch.empty_like(base["x"]), torch.empty_like(base["w"]), \
+        torch.empty_like(base["dy"])
+    y, dx = torch.empty_like(base["x"]), torch.empty_like(base["x"])
+    rstd = torch.empty(M, dtype=torch.float32, device=base["x"].device)
+    dw = torch.empty(N, dtype=torch.float32, device=base["x"].device)
+    hy, hdx = torch.empty_like(hx).pin_memory(), torch.empty_like(hx).pin_memory()
+    hr = torch.empty(M, dtype=torch.float32).pin_memory()
+    hdw = torch.empty(N, dtype=torch.float32).pin_memory()
+
+    def step():
+        dx_in.copy_(hx, non_blocking=True)
+        dw_in.copy_(hw, non_blocking=True)
+        ddy_in.copy_(hdy, non_blocking=True)
+        pkg.check(pkg.rmsnorm_fwd(dx_in, dw_in, y, rstd, M, N, eps, code, stream))
+        pkg.check(pkg.rmsnorm_bwd(dx_in, dw_in, ddy_in, rstd, dx, dw, M, N, code, stream))
+        hy.copy_(y, non_blocking=True)
+        hr.copy_(rstd, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hdw.copy_(dw, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = event_ms(e0, e1) / steps
+    elem = hx.element_size()
+    h2d = (hx.numel() + hw.numel() + hdy.numel()) * elem
+    d2h = (hy.numel() + hdx.numel()) * elem + hr.numel() * 4 + hdw.numel() * 4
+    return {"value": round(logical / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "step_ms": round(ms, 4), "steps": steps}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The fp64 CPU oracle timed on the host cores, one bounded sample of rows
+    per step, sized so that warm-up plus timed steps end within minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import torch
+
+    import oracle
+    from memory_bound_normalization_gb300 import synth
+
+    oracle.build()
+    wl = synth.WORKLOADS[args.workload]
+    elem = 2 if wl.dtype == torch.bfloat16 else 4
+    rows_avail = min(wl.M, 2048)
+    inp = synth.make_inputs(wl, device="cpu", M=rows_avail)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+
+    def one(rows):
+        t0 = time.perf_counter()
+        oracle.fwd(x[:rows], w, wl.eps)
+        oracle.bwd_dx(x[:rows], w, dy[:rows], wl.eps)
+        oracle.bwd_dw(x[:rows], dy[:rows], wl.eps)
+        return time.perf_counter() - t0
+
+    t = one(4)
+    per_row = t / 4
+    total_budget = 120.0
+    rows = int(max(1, min(rows_avail, total_budget / max(1, args.steps + args.warmup) / per_row)))
+    for _ in range(args.warmup):
+        one(rows)
+    times = [one(rows) for _ in range(args.steps)]
+    med = statistics.median(times)
+    fb, bb = synth.logical_bytes(rows, wl.N, elem)
+    value = (fb + bb) / med / 1e9
+    sample = (f"first {rows} of {wl.M} rows x {wl.N} ({wl.dtype_name}) per step; fp64 oracle "
+              "fwd + dx + dw, single thread")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(med * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.dtype_name,
+        "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "eps": wl.eps,
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        s = json.dumps(line)
+        print(s, flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                f.write(s + "\n")
+
+
+if __name__ == "__main__":
+    main()

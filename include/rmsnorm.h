@@ -1,0 +1,209 @@
+/*
+ * rmsnorm.h -- C ABI of librmsnorm.so: fused RMSNorm forward and a
+ * deterministic backward for NVIDIA GB300 (sm_103a).
+ *
+ * Operation (row i of an M x N matrix, column j):
+ *   forward   rstd_i = 1 / sqrt((1/N) * sum_j x_ij^2 + eps)
+ *             y_ij   = x_ij * rstd_i * w_j
+ *   backward  xhat_ij = x_ij * rstd_i,  g_ij = dy_ij * w_j
+ *             dx_ij   = rstd_i * (g_ij - xhat_ij * (1/N) * sum_j g_ij * xhat_ij)
+ *             dw_j    = sum_i dy_ij * xhat_ij
+ * Sources: "Chapter 13: Fused RMSNorm" (hello-gpu), section 13.1 equation
+ * (eps inside the square root, mean over the true column count); "RMSNorm
+ * backward (almost) without the column reduction", sections "The backward
+ * pass", "The problem: summing across rows" and "The persistent kernel"
+ * (weight gradient from per-block partial rows and a column sum, no float
+ * atomics); "What a tuned RMSNorm kernel actually costs on Hopper", section
+ * 05 (the backward reads the forward's fp32 reciprocal standard deviation).
+ *
+ * Conventions for every entry point below:
+ *   - Tensors are caller-owned DEVICE memory on the current CUDA device,
+ *     contiguous and row-major: x, y, dy, dx are M x N (row stride N), w is
+ *     N, rstd is M, dw is N. The library keeps no pointer after a call.
+ *   - `dtype` is the element type of x, w, y, dy and dx (one type for all
+ *     five): RMSNORM_F32 or RMSNORM_BF16. rstd and dw are always fp32.
+ *     Arithmetic is fp32; each 16-bit output is rounded once, to nearest.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream);
+ *     results are valid once the stream has reached the call.
+ *   - Return value is an rmsnorm_status_t. Arguments are checked before any
+ *     CUDA call; nothing aborts or throws across this boundary.
+ *     M == 0 is a no-op returning RMSNORM_OK. M < 0, N <= 0, N > 2^31-1, an
+ *     unknown dtype, a negative or NaN eps, or a NULL tensor pointer when
+ *     M > 0 return RMSNORM_ERR_INVALID_ARG. rstd or dw not 4-byte aligned,
+ *     or an element pointer not aligned to its element size, return
+ *     RMSNORM_ERR_MISALIGNED. Pointers that are 16-byte aligned with
+ *     N * element size a multiple of 16 take the vectorised kernels; any
+ *     other aligned input takes a scalar kernel that gives the same results
+ *     within rounding. A failed launch returns RMSNORM_ERR_CUDA.
+ *   - No output may alias an input.
+ *   - Results are deterministic: the same inputs, shapes, dtype, device
+ *     model and pointer-alignment class give bitwise-identical outputs,
+ *     dw included (fixed reduction trees, no floating-point atomics).
+ */
+#ifndef RMSNORM_H_
+#define RMSNORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RMSNORM_F32 = 0,
+    RMSNORM_BF16 = 1
+} rmsnorm_dtype_t;
+
+typedef enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_INVALID_ARG = 1,
+    RMSNORM_ERR_UNSUPPORTED = 2,
+    RMSNORM_ERR_MISALIGNED = 3,
+    RMSNORM_ERR_CUDA = 4,
+    RMSNORM_ERR_NOMEM = 5,
+    RMSNORM_ERR_DEVICE_TIMEOUT = 6
+} rmsnorm_status_t;
+
+/*
+ * Forward. Reads x [M,N] and w [N]; writes y [M,N] and rstd [M] (fp32, the
+ * per-row 1/sqrt(mean(x^2)+eps) that rmsnorm_bwd consumes).
+ * One kernel launch. Source: hello-gpu chapter 13, section 13.1.
+ */
+int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
+                int64_t M, int64_t N, float eps, int dtype,
+                cudaStream_t stream);
+
+/*
+ * Backward. Reads x [M,N], w [N], dy [M,N] and rstd [M] (as written by
+ * rmsnorm_fwd for the same x and eps; the backward takes no eps of its
+ * own); writes dx [M,N] and dw [N] (fp32, overwritten, not accumulated).
+ * A persistent kernel keeps each block's dw partial on chip across the rows
+ * it owns and writes one partial row; a second kernel sums the partial rows
+ * in a fixed order. Source: "RMSNorm backward (almost) without the column
+ * reduction", section "The persistent kernel".
+ * The partial rows live in a workspace that this call takes from the
+ * stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `stream`);
+ * RMSNORM_ERR_NOMEM if that fails. Use rmsnorm_bwd_ws to pass your own.
+ */
+int rmsnorm_bwd(const void *x, const void *w, const void *dy,
+                const float *rstd, void *dx, float *dw,
+                int64_t M, int64_t N, int dtype, cudaStream_t stream);
+
+/*
+ * Bytes of workspace rmsnorm_bwd_ws needs for this shape on `device`
+ * (a CUDA ordinal). Returns 0 when M == 0 or the arguments are invalid.
+ */
+size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype,
+                                  int device);
+
+/*
+ * rmsnorm_bwd with a caller-provided workspace: device memory of at least
+ * rmsnorm_bwd_workspace_size(M, N, dtype, current device) bytes, 16-byte
+ * aligned, not read by the caller until the stream reaches the end of the
+ * call, and not shared with another call in flight. A smaller or NULL
+ * workspace (with M > 0) returns RMSNORM_ERR_INVALID_ARG; misaligned returns
+ * RMSNORM_ERR_MISALIGNED. Allocates nothing.
+ */
+int rmsnorm_bwd_ws(const void *x, const void *w, const void *dy,
+                   const float *rstd, void *dx, float *dw,
+                   int64_t M, int64_t N, int dtype,
+                   void *workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/*
+ * Device-side status. Every wait inside the kernels (on a bulk copy landing
+ * in shared memory) is bounded in time; a wait that runs out records
+ * RMSNORM_ERR_DEVICE_TIMEOUT in a status word on the device and the kernel
+ * returns early instead of hanging. This call synchronises `stream`, returns
+ * the status recorded on the current device since the last call (RMSNORM_OK
+ * if none), and clears it. RMSNORM_ERR_CUDA if the synchronisation fails.
+ */
+int rmsnorm_get_last_device_error(cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *rmsnorm_status_string(int status);
+
+/*
+ * Time limit of each bounded wait, in nanoseconds, for kernels launched
+ * after the call (process-wide; 0 restores the default of one second).
+ */
+void rmsnorm_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Failure-injection hook for testing the bounded waits: the next backward
+ * launch that stages rows through bulk copies will not issue the copy of
+ * unit `unit` (a row, or a tile of rows for short rows), so the wait for it
+ * runs out and the status word reads RMSNORM_ERR_DEVICE_TIMEOUT. Outputs of
+ * that call are unspecified. One-shot; -1 cancels.
+ */
+void rmsnorm_test_drop_copy(int64_t unit);
+
+/*
+ * HBM roofline probes (the measured denominator of the throughput ratio;
+ * "What a tuned RMSNorm kernel actually costs on Hopper", section 02: best
+ * of a copy, a pure write and a two-read-one-write pattern). 16-byte vector
+ * accesses in a grid-stride loop over `bytes` bytes (a multiple of 16; all
+ * pointers 16-byte aligned):
+ *   RMSNORM_PROBE_COPY   dst[k] = a[k]                      (moves 2*bytes)
+ *   RMSNORM_PROBE_WRITE  dst[k] = a bit pattern of zeros     (moves bytes)
+ *   RMSNORM_PROBE_2R1W   dst[k] = a[k] + b[k] as fp32       (moves 3*bytes)
+ * `blocks_per_sm` (>= 1) sets the grid. Unused pointers may be NULL.
+ */
+typedef enum {
+    RMSNORM_PROBE_COPY = 0,
+    RMSNORM_PROBE_WRITE = 1,
+    RMSNORM_PROBE_2R1W = 2
+} rmsnorm_probe_t;
+
+int rmsnorm_probe(int kind, void *dst, const void *a, const void *b,
+                  size_t bytes, int blocks_per_sm, cudaStream_t stream);
+
+/* Kernel family a call dispatches to. */
+typedef enum {
+    RMSNORM_VARIANT_NONE = 0,      /* M == 0: nothing launched */
+    RMSNORM_VARIANT_ROWGROUP = 1,  /* short rows: a sub-warp or warp per row */
+    RMSNORM_VARIANT_CTA_ROW = 2,   /* one thread block per row */
+    RMSNORM_VARIANT_CLUSTER_ROW = 3, /* a thread-block cluster per row */
+    RMSNORM_VARIANT_SCALAR = 4     /* unaligned or ragged rows */
+} rmsnorm_variant_t;
+
+typedef enum {
+    RMSNORM_PASS_FWD = 0,
+    RMSNORM_PASS_BWD = 1
+} rmsnorm_pass_t;
+
+typedef struct {
+    int variant;            /* rmsnorm_variant_t */
+    int threads;            /* threads per block */
+    int vectors_per_thread; /* 16-byte vectors of a row each thread owns */
+    int threads_per_row;    /* lanes sharing one row (ROWGROUP), else threads */
+    int rows_per_unit;      /* rows moved per bulk copy / per block pass */
+    int cluster;            /* blocks per row (1 unless CLUSTER_ROW) */
+    int stages;             /* shared-memory pipeline depth (backward) */
+    int smem_bytes;         /* dynamic shared memory per block */
+    int grid;               /* blocks launched; 0 when device < 0 */
+    int partial_rows;       /* dw partial rows written (backward), else 0 */
+    int64_t workspace_bytes;/* backward workspace, 0 for the forward */
+} rmsnorm_plan_t;
+
+/*
+ * Describe, without launching anything, what rmsnorm_fwd (pass 0) or
+ * rmsnorm_bwd (pass 1) would run for this shape with 16-byte aligned
+ * pointers. With device >= 0 the grid and workspace are filled in from
+ * that device's properties (needs a GPU); with device < 0 only the
+ * width-dependent choices are made (host only). Returns a status code.
+ */
+int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device,
+                 rmsnorm_plan_t *out);
+
+/* Library version as "major.minor.patch" (static storage). */
+const char *rmsnorm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_H_ */

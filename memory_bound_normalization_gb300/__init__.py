@@ -1,0 +1,81 @@
+"""Fused RMSNorm forward and deterministic backward for NVIDIA GB300.
+
+The computation lives in the CUDA library ``librmsnorm.so`` (C ABI in
+``include/rmsnorm.h``); this package is its Python binding. The ``rmsnorm_*``
+functions mirror the C entry points one for one. ``forward`` and ``backward``
+are conveniences that allocate outputs with PyTorch (device memory only) and
+raise ``RMSNormError`` on a non-OK status.
+"""
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401
+    BF16,
+    ERR_CUDA,
+    ERR_DEVICE_TIMEOUT,
+    ERR_INVALID_ARG,
+    ERR_MISALIGNED,
+    ERR_NOMEM,
+    ERR_UNSUPPORTED,
+    EXPORTS,
+    F32,
+    OK,
+    PASS_BWD,
+    PASS_FWD,
+    PROBE_2R1W,
+    PROBE_COPY,
+    PROBE_WRITE,
+    VARIANTS,
+    Plan,
+    RMSNormError,
+    check,
+    library_path,
+    load_library,
+    rmsnorm_bwd,
+    rmsnorm_bwd_workspace_size,
+    rmsnorm_bwd_ws,
+    rmsnorm_fwd,
+    rmsnorm_get_last_device_error,
+    rmsnorm_plan,
+    rmsnorm_probe,
+    rmsnorm_set_wait_limit_ns,
+    rmsnorm_status_string,
+    rmsnorm_test_drop_copy,
+    rmsnorm_version,
+)
+
+__version__ = "0.1.0"
+
+
+def dtype_code(torch_dtype) -> int:
+    """C-ABI dtype code of a torch dtype (float32 or bfloat16)."""
+    import torch
+
+    if torch_dtype == torch.bfloat16:
+        return BF16
+    if torch_dtype == torch.float32:
+        return F32
+    raise RMSNormError(ERR_INVALID_ARG, f"unsupported dtype {torch_dtype}")
+
+
+def forward(x, w, eps: float = 1e-6, stream=None):
+    """y, rstd = RMSNorm(x) over the last dimension (x contiguous, on a GPU)."""
+    import torch
+
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    y = torch.empty_like(x)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    check(rmsnorm_fwd(x, w, y, rstd, M, N, eps, dtype_code(x.dtype), stream), "rmsnorm_fwd")
+    return y, rstd
+
+
+def backward(x, w, dy, rstd, stream=None):
+    """dx, dw = RMSNorm backward from the forward's rstd."""
+    import torch
+
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    dx = torch.empty_like(x)
+    dw = torch.empty((N,), dtype=torch.float32, device=x.device)
+    check(rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, dtype_code(x.dtype), stream), "rmsnorm_bwd")
+    return dx, dw

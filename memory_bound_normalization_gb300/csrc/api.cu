@@ -1,0 +1,274 @@
+// C ABI of librmsnorm.so (declared in include/rmsnorm.h): argument checks,
+// per-device properties, the device status word, workspace handling and
+// dispatch to the kernel translation units.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace rmsn {
+
+// One status word per device (a module-scope variable lives once in every
+// device context that loads the library). Kernels receive its address.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // one second
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int64_t> g_drop_unit{-1};
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int shape_status(int64_t M, int64_t N, int dtype) {
+    if (M < 0 || N <= 0 || N > INT32_MAX) return RMSNORM_ERR_INVALID_ARG;
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    return RMSNORM_OK;
+}
+
+int current_device(const DeviceInfo** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    *out = device_info(dev);
+    return *out ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+// Backward checks shared by rmsnorm_bwd and rmsnorm_bwd_ws. On success fills
+// the plan (with M > 0) or reports that there is nothing to do besides
+// clearing dw (M == 0).
+int bwd_prepare(const void* x, const void* w, const void* dy, const float* rstd, void* dx,
+                float* dw, int64_t M, int64_t N, int dtype, const DeviceInfo** dev,
+                rmsnorm_plan_t* plan) {
+    int st = shape_status(M, N, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (M == 0) {
+        if (dw != nullptr && !aligned(dw, 4)) return RMSNORM_ERR_MISALIGNED;
+        *plan = rmsnorm_plan_t{};
+        return RMSNORM_OK;
+    }
+    if (!x || !w || !dy || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
+    const int sz = dtype_size(dtype);
+    if (!aligned(x, sz) || !aligned(w, sz) || !aligned(dy, sz) || !aligned(dx, sz) ||
+        !aligned(rstd, 4) || !aligned(dw, 4))
+        return RMSNORM_ERR_MISALIGNED;
+    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(dy, 16) && aligned(dx, 16) &&
+                     (N * sz) % 16 == 0;
+    bwd_choose(N, dtype, vec, plan);
+    st = current_device(dev);
+    if (st != RMSNORM_OK) return st;
+    if (bwd_finish_plan(**dev, dtype, M, N, plan) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+int bwd_run(const void* x, const void* w, const void* dy, const float* rstd, void* dx, float* dw,
+            int64_t M, int64_t N, int dtype, const DeviceInfo& dev, const rmsnorm_plan_t& plan,
+            void* workspace, cudaStream_t stream) {
+    BwdArgs a{};
+    a.x = x;
+    a.w = w;
+    a.dy = dy;
+    a.rstd = rstd;
+    a.dx = dx;
+    a.partial = static_cast<float*>(workspace);
+    a.dw = dw;
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.status = dev.status_word;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.drop_unit = plan.variant != RMSNORM_VARIANT_SCALAR ? g_drop_unit.exchange(-1) : -1;
+    return bwd_launch(plan, dtype, a, stream) == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+}  // namespace
+
+const DeviceInfo* device_info(int device) {
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev_ready[device]) return &g_dev[device];
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return nullptr;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return nullptr;
+    DeviceInfo d;
+    d.device = device;
+    bool ok = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) == cudaSuccess &&
+              cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) == cudaSuccess &&
+              cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, device) == cudaSuccess &&
+              cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_word), g_status_word) == cudaSuccess;
+    if (prev != device) cudaSetDevice(prev);
+    if (!ok || d.sm_count <= 0) return nullptr;
+    g_dev[device] = d;
+    g_dev_ready[device] = true;
+    return &g_dev[device];
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+extern "C" {
+
+int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                float eps, int dtype, cudaStream_t stream) {
+    int st = shape_status(M, N, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (!(eps >= 0.f)) return RMSNORM_ERR_INVALID_ARG;  // negative or NaN
+    if (M == 0) return RMSNORM_OK;
+    if (!x || !w || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;
+    const int sz = dtype_size(dtype);
+    if (!aligned(x, sz) || !aligned(w, sz) || !aligned(y, sz) || !aligned(rstd, 4))
+        return RMSNORM_ERR_MISALIGNED;
+    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(y, 16) && (N * sz) % 16 == 0;
+    rmsnorm_plan_t plan;
+    fwd_choose(N, dtype, vec, &plan);
+    const DeviceInfo* dev = nullptr;
+    st = current_device(&dev);
+    if (st != RMSNORM_OK) return st;
+    if (fwd_finish_plan(*dev, dtype, M, &plan) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (static_cast<int64_t>(plan.grid) <= 0 ||
+        (plan.variant != RMSNORM_VARIANT_SCALAR &&
+         cdiv(M, plan.variant == RMSNORM_VARIANT_ROWGROUP ? plan.rows_per_unit : 1) * plan.cluster >
+             INT32_MAX))
+        return RMSNORM_ERR_UNSUPPORTED;
+    FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps};
+    return fwd_launch(plan, dtype, a, stream) == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype, int device) {
+    if (shape_status(M, N, dtype) != RMSNORM_OK || M == 0) return 0;
+    const DeviceInfo* dev = device_info(device);
+    if (!dev) return 0;
+    rmsnorm_plan_t plan;
+    // the workspace only depends on the partial-row count; take the largest
+    // of the vector and scalar plans so either alignment class fits
+    size_t need = 0;
+    for (int vec = 0; vec < 2; ++vec) {
+        if (vec && (N * dtype_size(dtype)) % 16 != 0) continue;
+        bwd_choose(N, dtype, vec != 0, &plan);
+        if (bwd_finish_plan(*dev, dtype, M, N, &plan) != cudaSuccess) return 0;
+        if (static_cast<size_t>(plan.workspace_bytes) > need) need = static_cast<size_t>(plan.workspace_bytes);
+    }
+    return need;
+}
+
+int rmsnorm_bwd_ws(const void* x, const void* w, const void* dy, const float* rstd, void* dx,
+                   float* dw, int64_t M, int64_t N, int dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+    const DeviceInfo* dev = nullptr;
+    rmsnorm_plan_t plan;
+    int st = bwd_prepare(x, w, dy, rstd, dx, dw, M, N, dtype, &dev, &plan);
+    if (st != RMSNORM_OK) return st;
+    if (M == 0) {
+        if (dw == nullptr) return RMSNORM_OK;
+        return cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream) == cudaSuccess
+                   ? RMSNORM_OK
+                   : RMSNORM_ERR_CUDA;
+    }
+    if (workspace == nullptr || workspace_bytes < static_cast<size_t>(plan.workspace_bytes))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return RMSNORM_ERR_MISALIGNED;
+    return bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, workspace, stream);
+}
+
+int rmsnorm_bwd(const void* x, const void* w, const void* dy, const float* rstd, void* dx,
+                float* dw, int64_t M, int64_t N, int dtype, cudaStream_t stream) {
+    const DeviceInfo* dev = nullptr;
+    rmsnorm_plan_t plan;
+    int st = bwd_prepare(x, w, dy, rstd, dx, dw, M, N, dtype, &dev, &plan);
+    if (st != RMSNORM_OK) return st;
+    if (M == 0) {
+        if (dw == nullptr) return RMSNORM_OK;
+        return cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream) == cudaSuccess
+                   ? RMSNORM_OK
+                   : RMSNORM_ERR_CUDA;
+    }
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, static_cast<size_t>(plan.workspace_bytes), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return RMSNORM_ERR_NOMEM;
+    }
+    st = bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, ws, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && st == RMSNORM_OK) st = RMSNORM_ERR_CUDA;
+    return st;
+}
+
+int rmsnorm_get_last_device_error(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    const DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != RMSNORM_OK) return RMSNORM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, dev->status_word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (v != 0 && cudaMemset(dev->status_word, 0, sizeof v) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    return v;
+}
+
+const char* rmsnorm_status_string(int status) {
+    switch (status) {
+        case RMSNORM_OK: return "RMSNORM_OK";
+        case RMSNORM_ERR_INVALID_ARG: return "RMSNORM_ERR_INVALID_ARG";
+        case RMSNORM_ERR_UNSUPPORTED: return "RMSNORM_ERR_UNSUPPORTED";
+        case RMSNORM_ERR_MISALIGNED: return "RMSNORM_ERR_MISALIGNED";
+        case RMSNORM_ERR_CUDA: return "RMSNORM_ERR_CUDA";
+        case RMSNORM_ERR_NOMEM: return "RMSNORM_ERR_NOMEM";
+        case RMSNORM_ERR_DEVICE_TIMEOUT: return "RMSNORM_ERR_DEVICE_TIMEOUT";
+        default: return "RMSNORM_STATUS_UNKNOWN";
+    }
+}
+
+void rmsnorm_set_wait_limit_ns(uint64_t ns) {
+    g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns);
+}
+
+void rmsnorm_test_drop_copy(int64_t unit) { g_drop_unit.store(unit < 0 ? -1 : unit); }
+
+int rmsnorm_probe(int kind, void* dst, const void* a, const void* b, size_t bytes,
+                  int blocks_per_sm, cudaStream_t stream) {
+    if (kind < RMSNORM_PROBE_COPY || kind > RMSNORM_PROBE_2R1W) return RMSNORM_ERR_INVALID_ARG;
+    if (bytes % 16 != 0 || blocks_per_sm < 1) return RMSNORM_ERR_INVALID_ARG;
+    if (bytes == 0) return RMSNORM_OK;
+    if (dst == nullptr) return RMSNORM_ERR_INVALID_ARG;
+    if (kind != RMSNORM_PROBE_WRITE && a == nullptr) return RMSNORM_ERR_INVALID_ARG;
+    if (kind == RMSNORM_PROBE_2R1W && b == nullptr) return RMSNORM_ERR_INVALID_ARG;
+    if (!aligned(dst, 16) || (a && !aligned(a, 16)) || (b && !aligned(b, 16)))
+        return RMSNORM_ERR_MISALIGNED;
+    const DeviceInfo* dev = nullptr;
+    int st = current_device(&dev);
+    if (st != RMSNORM_OK) return st;
+    const int grid = dev->sm_count * blocks_per_sm;
+    return probe_launch(kind, dst, a, b, bytes, grid, stream) == cudaSuccess ? RMSNORM_OK
+                                                                              : RMSNORM_ERR_CUDA;
+}
+
+int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_plan_t* out) {
+    if (out == nullptr) return RMSNORM_ERR_INVALID_ARG;
+    int st = shape_status(M, N, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (pass != RMSNORM_PASS_FWD && pass != RMSNORM_PASS_BWD) return RMSNORM_ERR_INVALID_ARG;
+    if (M == 0) {
+        *out = rmsnorm_plan_t{};
+        return RMSNORM_OK;
+    }
+    const bool vec = (N * dtype_size(dtype)) % 16 == 0;
+    if (pass == RMSNORM_PASS_FWD)
+        fwd_choose(N, dtype, vec, out);
+    else
+        bwd_choose(N, dtype, vec, out);
+    if (device < 0) return RMSNORM_OK;
+    const DeviceInfo* dev = device_info(device);
+    if (!dev) return RMSNORM_ERR_CUDA;
+    cudaError_t e = pass == RMSNORM_PASS_FWD ? fwd_finish_plan(*dev, dtype, M, out)
+                                             : bwd_finish_plan(*dev, dtype, M, N, out);
+    return e == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+const char* rmsnorm_version(void) { return "0.1.0"; }
+
+}  // extern "C"

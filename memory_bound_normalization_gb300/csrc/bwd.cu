@@ -1,0 +1,653 @@
+// RMSNorm backward kernels.
+//
+//   xhat = x * rstd, g = dy * w
+//   dx   = rstd * (g - xhat * mean_j(g * xhat))
+//   dw   = sum over rows of dy * xhat
+//
+// Definitions: "RMSNorm backward (almost) without the column reduction",
+// sections "The backward pass" (the gradients) and "The problem: summing
+// across rows" (no float atomics: their order changes the bits run to run).
+// Structure follows that page's section "The persistent kernel": the grid is
+// sized by the machine (resident blocks per SM times SMs, at most one block
+// per row), block b walks rows b, b+P, b+2P, ..., keeps its dw contribution
+// in registers across those rows and writes one partial row at the end; a
+// second kernel sums the P partial rows in a fixed order. The next rows are
+// prefetched into a shared-memory ring while the current row is computed.
+//
+// What differs from that page's kernel: rows land through 1-D bulk copies
+// (cp.async.bulk, completion counted on an mbarrier) instead of per-thread
+// cp.async; the ring depth is a parameter (2-4 stages) rather than 2; rstd is
+// read from the forward (as the Quack backward does, "What a tuned RMSNorm
+// kernel actually costs on Hopper", section 05) rather than recomputed, so a
+// row needs one reduction, not two; rows may be split over a thread-block
+// cluster with the row sum exchanged through distributed shared memory; and
+// short rows move as tiles of whole rows. Every wait on a copy is bounded in
+// time and reports a status instead of hanging.
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmsn {
+namespace {
+
+constexpr int kStageBudget = 96 * 1024;   // shared memory aimed at per block
+constexpr int kSliceBudget = 48 * 1024;   // x+dy bytes of one row slice per stage
+constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory a block may opt into
+
+// Dynamic shared memory: [S][unit] x | [S][unit] dy | mbarrier[S] |
+// reduction slots [2][32] | cluster slots [2] | failure flag.
+__host__ __device__ inline int bwd_smem_bytes(int stages, int unit) {
+    return 2 * stages * unit + stages * 8 + 64 * 4 + 2 * 4 + 16;
+}
+
+// ------------------------------------------------ block or cluster per row
+template <typename T, int V>
+__global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages) {
+    using P = Pack<T>;
+    constexpr int VEC = P::VEC;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int nthr = blockDim.x, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    const uint32_t csize = cluster_size();
+    const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
+    const int64_t cid = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
+    const int64_t ncl = csize > 1 ? static_cast<int64_t>(cluster_count()) : gridDim.x;
+    const int N = a.N;
+    const int nvec = N / VEC;
+    const int slots = V * nthr;
+    const int vbeg = static_cast<int>(crank) * slots;
+    const int vcnt = max(0, min(slots, nvec - vbeg));
+    const uint32_t bytes = static_cast<uint32_t>(vcnt) * 16u;
+    const int S = stages;
+    const int unit = slots * 16;
+
+    unsigned char* sx = smem;
+    unsigned char* sdy = smem + S * unit;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * S * unit);
+    float* red = reinterpret_cast<float*>(bar + S);
+    float* cpart = red + 64;
+    volatile int* fail = reinterpret_cast<volatile int*>(cpart + 2);
+
+    const T* X = static_cast<const T*>(a.x);
+    const T* DY = static_cast<const T*>(a.dy);
+    const T* W = static_cast<const T*>(a.w);
+    T* DX = static_cast<T*>(a.dx);
+
+    // rows of this cluster: cid, cid+ncl, ...
+    const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        *fail = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    // Producer state, meaningful in thread 0 only: stages with a copy in
+    // flight and the parity of the phase that copy completes.
+    uint32_t pending = 0, pending_parity = 0;
+    auto issue = [&](int64_t t) {
+        const int s = static_cast<int>(t % S);
+        const int64_t row = cid + t * ncl;
+        if (bytes == 0) {
+            mbar_arrive(&bar[s]);
+            return;
+        }
+        mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+        if (row == a.drop_unit) return;  // failure injection: this wait runs out
+        const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
+        bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
+        bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
+        pending |= 1u << s;
+        pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
+    };
+    if (tid == 0)
+        for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
+
+    uint4 wv[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * nthr + tid;
+        wv[j] = k < vcnt ? ld_global_16(W + static_cast<int64_t>(vbeg + k) * VEC)
+                         : make_uint4(0, 0, 0, 0);
+    }
+    float acc[V][VEC];
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[j][e] = 0.f;
+
+    // rstd is read two rows ahead so its latency hides behind the rows before
+    float r1 = nrows > 0 ? __ldg(a.rstd + cid) : 0.f;
+    float r2 = nrows > 1 ? __ldg(a.rstd + cid + ncl) : 0.f;
+    bool failed = false;
+
+    for (int64_t t = 0; t < nrows; ++t) {
+        const int64_t row = cid + t * ncl;
+        const int s = static_cast<int>(t % S);
+        const uint32_t parity = static_cast<uint32_t>((t / S) & 1);
+        const float r = r1;
+        r1 = r2;
+        if (t + 2 < nrows) r2 = __ldg(a.rstd + row + 2 * ncl);
+
+        if (!failed) {
+            if (mbar_wait_bounded(&bar[s], parity, a.wait_limit_ns)) {
+                if (tid == 0) pending &= ~(1u << s);
+            } else {
+                *fail = 1;
+                report_status(a.status, kStatusTimeout);
+            }
+        }
+        // pass 1: dot = sum_j (dy*w)*x over this thread's slots
+        float dot = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * nthr + tid;
+            if (k >= vcnt) continue;
+            float fx[VEC], fd[VEC], fw[VEC];
+            P::unpack(ld_shared_16(sx + s * unit + k * 16), fx);
+            P::unpack(ld_shared_16(sdy + s * unit + k * 16), fd);
+            P::unpack(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) dot = fmaf(fd[e] * fw[e], fx[e], dot);
+        }
+        dot = group_allreduce<32>(dot);
+        float* rslot = red + (t & 1) * 32;
+        if (lane == 0) rslot[warp] = dot;
+        __syncthreads();  // partial sums published; every thread is done with row t-1
+        failed = *fail != 0;
+        float tot = lane < nw ? rslot[lane] : 0.f;
+        tot = group_allreduce<32>(tot);
+        // the stage of row t-1 is free now: refill it with row t-1+S
+        if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+            fence_proxy_async_shared();
+            issue(t - 1 + S);
+        }
+        if (csize > 1) {
+            if (tid == 0) cpart[t & 1] = tot;
+            cluster_sync_all();
+            tot = 0.f;
+            for (uint32_t q = 0; q < csize; ++q) tot += ld_cluster_f32(&cpart[t & 1], q);
+        }
+        // mean_j(g * xhat) = rstd * mean_j(g * x)
+        const float c = r * (tot / static_cast<float>(N));
+        T* dxr = DX + row * N;
+        // pass 2: dx and the dw contribution, reading the row from shared memory again
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * nthr + tid;
+            if (k >= vcnt) continue;
+            float fx[VEC], fd[VEC], fw[VEC], o[VEC];
+            P::unpack(ld_shared_16(sx + s * unit + k * 16), fx);
+            P::unpack(ld_shared_16(sdy + s * unit + k * 16), fd);
+            P::unpack(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float xh = fx[e] * r;
+                const float g = fd[e] * fw[e];
+                o[e] = r * (g - xh * c);
+                acc[j][e] = fmaf(fd[e], xh, acc[j][e]);
+            }
+            st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack(o));
+        }
+    }
+
+    // one partial row per cluster; each block writes its column slice
+    float* prow = a.partial + cid * N + static_cast<int64_t>(vbeg) * VEC;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * nthr + tid;
+        if (k >= vcnt) continue;
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+            *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
+                make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2], acc[j][4 * q + 3]);
+    }
+    // after a failure, let copies already in flight land before exiting
+    if (tid == 0 && failed)
+        for (int s = 0; s < S; ++s)
+            if ((pending >> s) & 1u) mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
+    if (csize > 1) cluster_sync_all();
+}
+
+// ---------------------------------------------------------- short rows
+// A unit is a tile of RT = (threads/G)*R consecutive rows, moved by one bulk
+// copy per tensor. Group g (G lanes) handles tile rows r*groups + g.
+template <typename T, int G, int V, int R>
+__global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages) {
+    using P = Pack<T>;
+    constexpr int VEC = P::VEC;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int tid = threadIdx.x;
+    const int lane = tid % G, group = tid / G, groups = blockDim.x / G;
+    const int RT = groups * R;
+    const int N = a.N;
+    const int nvec = N / VEC;
+    const int64_t ntiles = (a.M + RT - 1) / RT;
+    const int64_t b = blockIdx.x, nb = gridDim.x;
+    const int64_t count = b < ntiles ? (ntiles - 1 - b) / nb + 1 : 0;
+    const int S = stages;
+    const int unit = RT * N * static_cast<int>(sizeof(T));
+
+    unsigned char* sx = smem;
+    unsigned char* sdy = smem + S * unit;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * S * unit);
+    volatile int* fail = reinterpret_cast<volatile int*>(reinterpret_cast<float*>(bar + S) + 66);
+
+    const T* X = static_cast<const T*>(a.x);
+    const T* DY = static_cast<const T*>(a.dy);
+    const T* W = static_cast<const T*>(a.w);
+    T* DX = static_cast<T*>(a.dx);
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        *fail = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    uint32_t pending = 0, pending_parity = 0;
+    auto issue = [&](int64_t t) {
+        const int s = static_cast<int>(t % S);
+        const int64_t tile = b + t * nb;
+        const int64_t rows = min(static_cast<int64_t>(RT), a.M - tile * RT);
+        const uint32_t bytes = static_cast<uint32_t>(rows * N * static_cast<int64_t>(sizeof(T)));
+        mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+        if (tile == a.drop_unit) return;  // failure injection
+        const int64_t off = tile * RT * N;
+        bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
+        bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
+        pending |= 1u << s;
+        pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
+    };
+    if (tid == 0)
+        for (int64_t t = 0; t < S && t < count; ++t) issue(t);
+
+    uint4 wv[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * G + lane;
+        wv[j] = k < nvec ? ld_global_16(W + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+    }
+    float acc[V][VEC];
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[j][e] = 0.f;
+
+    float rnext[R];
+    auto load_rstd = [&](int64_t t, float (&dst)[R]) {
+        const int64_t tile = b + t * nb;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = tile * RT + r * groups + group;
+            dst[r] = (t < count && row < a.M) ? __ldg(a.rstd + row) : 0.f;
+        }
+    };
+    load_rstd(0, rnext);
+    bool failed = false;
+
+    for (int64_t t = 0; t < count; ++t) {
+        const int64_t tile = b + t * nb;
+        const int s = static_cast<int>(t % S);
+        const uint32_t parity = static_cast<uint32_t>((t / S) & 1);
+        float rcur[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) rcur[r] = rnext[r];
+        load_rstd(t + 1, rnext);
+
+        if (!failed) {
+            if (mbar_wait_bounded(&bar[s], parity, a.wait_limit_ns)) {
+                if (tid == 0) pending &= ~(1u << s);
+            } else {
+                *fail = 1;
+                report_status(a.status, kStatusTimeout);
+            }
+        }
+        // pass 1: per-row dot = sum_j (dy*w)*x over this lane's slots
+        float dot[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int lr = r * groups + group;
+            const bool row_ok = tile * RT + lr < a.M;
+            dot[r] = 0.f;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int k = j * G + lane;
+                if (!row_ok || k >= nvec) continue;
+                const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
+                float fx[VEC], fd[VEC], fw[VEC];
+                P::unpack(ld_shared_16(sx + s * unit + off), fx);
+                P::unpack(ld_shared_16(sdy + s * unit + off), fd);
+                P::unpack(wv[j], fw);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) dot[r] = fmaf(fd[e] * fw[e], fx[e], dot[r]);
+            }
+        }
+        __syncthreads();  // every thread is done with tile t-1
+        failed = *fail != 0;
+        if (tid == 0 && !failed && t >= 1 && t - 1 + S < count) {
+            fence_proxy_async_shared();
+            issue(t - 1 + S);
+        }
+#pragma unroll
+        for (int off = G / 2; off >= 1; off /= 2)
+#pragma unroll
+            for (int r = 0; r < R; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], off);
+
+        // pass 2: dx and the dw contribution, re-reading the tile from shared memory
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int lr = r * groups + group;
+            const int64_t row = tile * RT + lr;
+            if (row >= a.M) continue;
+            const float rs = rcur[r];
+            const float c = rs * (dot[r] / static_cast<float>(N));
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int k = j * G + lane;
+                if (k >= nvec) continue;
+                const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
+                float fx[VEC], fd[VEC], fw[VEC], o[VEC];
+                P::unpack(ld_shared_16(sx + s * unit + off), fx);
+                P::unpack(ld_shared_16(sdy + s * unit + off), fd);
+                P::unpack(wv[j], fw);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float xh = fx[e] * rs;
+                    const float g = fd[e] * fw[e];
+                    o[e] = rs * (g - xh * c);
+                    acc[j][e] = fmaf(fd[e], xh, acc[j][e]);
+                }
+                st_global_16(DX + row * N + static_cast<int64_t>(k) * VEC, P::pack(o));
+            }
+        }
+    }
+
+    if (tid == 0 && failed)
+        for (int s = 0; s < S; ++s)
+            if ((pending >> s) & 1u) mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
+    __syncthreads();  // all lanes done with the last tile; the ring is idle
+    // combine the groups' dw in group order through shared memory
+    // (groups*N*4 bytes always fit in the 2*S*unit bytes of the ring)
+    float* comb = reinterpret_cast<float*>(smem);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * G + lane;
+        if (k >= nvec) continue;
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q)
+            *reinterpret_cast<float4*>(comb + group * N + k * VEC + 4 * q) =
+                make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2], acc[j][4 * q + 3]);
+    }
+    __syncthreads();
+    float* prow = a.partial + b * N;
+    for (int col = tid; col < N; col += blockDim.x) {
+        float sum = 0.f;
+        for (int gi = 0; gi < groups; ++gi) sum += comb[gi * N + col];
+        prow[col] = sum;
+    }
+}
+
+// ------------------------------------------------------------------ scalar
+// Any alignment, any N. Persistent: block b owns rows b, b+P, ... and its
+// partial row, which thread t updates at columns t, t+blockDim, ... only.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages*/) {
+    using P = Pack<T>;
+    __shared__ float red[2][32];
+    const int N = a.N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const T* X = static_cast<const T*>(a.x);
+    const T* DY = static_cast<const T*>(a.dy);
+    const T* W = static_cast<const T*>(a.w);
+    T* DX = static_cast<T*>(a.dx);
+    float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
+    for (int col = threadIdx.x; col < N; col += blockDim.x) prow[col] = 0.f;
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, ++it) {
+        const T* xr = X + row * N;
+        const T* dyr = DY + row * N;
+        const float r = a.rstd[row];
+        float dot = 0.f;
+        for (int col = threadIdx.x; col < N; col += blockDim.x)
+            dot = fmaf(P::to_float(dyr[col]) * P::to_float(W[col]), P::to_float(xr[col]), dot);
+        dot = group_allreduce<32>(dot);
+        if (lane == 0) red[it & 1][warp] = dot;
+        __syncthreads();
+        float tot = lane < nw ? red[it & 1][lane] : 0.f;
+        tot = group_allreduce<32>(tot);
+        const float c = r * (tot / static_cast<float>(N));
+        T* dxr = DX + row * N;
+        for (int col = threadIdx.x; col < N; col += blockDim.x) {
+            const float d = P::to_float(dyr[col]);
+            const float xh = P::to_float(xr[col]) * r;
+            const float g = d * P::to_float(W[col]);
+            dxr[col] = P::from_float(r * (g - xh * c));
+            prow[col] = fmaf(d, xh, prow[col]);
+        }
+    }
+}
+
+// ---------------------------------------------------------- column sum
+// dw[j] = sum over p of partial[p][j] in a fixed tree: thread row q of the
+// block sums p = q, q+32, q+64, ... in ascending order, then the 32 sums are
+// added in q order. Same bits on every run for a given P.
+__global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ partial,
+                                                      float* __restrict__ dw, int P, int N) {
+    __shared__ float part[32][33];
+    const int cx = threadIdx.x, q = threadIdx.y;
+    const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + cx;
+    float s = 0.f;
+    if (col < N) {
+#pragma unroll 4
+        for (int p = q; p < P; p += 32) s += partial[static_cast<int64_t>(p) * N + col];
+    }
+    part[q][cx] = s;
+    __syncthreads();
+    if (q == 0 && col < N) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) t += part[i][cx];
+        dw[col] = t;
+    }
+}
+
+// ------------------------------------------------------------ host side
+template <typename T>
+const void* row_kernel(int V) {
+    switch (V) {
+        case 1: return reinterpret_cast<const void*>(&bwd_row_kernel<T, 1>);
+        case 2: return reinterpret_cast<const void*>(&bwd_row_kernel<T, 2>);
+        case 4: return reinterpret_cast<const void*>(&bwd_row_kernel<T, 4>);
+        case 8: return reinterpret_cast<const void*>(&bwd_row_kernel<T, 8>);
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+const void* rowgroup_kernel(int G, int V) {
+    if (G == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 4, 1, 4>);
+    if (G == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 8, 1, 4>);
+    if (G == 16) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 16, 1, 4>);
+    if (V == 1) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 1, 2>);
+    if (V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 2, 2>);
+    if (V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 4, 1>);
+    if (V == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 8, 1>);
+    return nullptr;
+}
+
+template <typename T>
+const void* main_kernel(const rmsnorm_plan_t& p) {
+    switch (p.variant) {
+        case RMSNORM_VARIANT_ROWGROUP: return rowgroup_kernel<T>(p.threads_per_row, p.vectors_per_thread);
+        case RMSNORM_VARIANT_CTA_ROW:
+        case RMSNORM_VARIANT_CLUSTER_ROW: return row_kernel<T>(p.vectors_per_thread);
+        case RMSNORM_VARIANT_SCALAR: return reinterpret_cast<const void*>(&bwd_scalar_kernel<T>);
+        default: return nullptr;
+    }
+}
+
+const void* main_kernel_for(int dtype, const rmsnorm_plan_t& p) {
+    return dtype == RMSNORM_BF16 ? main_kernel<__nv_bfloat16>(p) : main_kernel<float>(p);
+}
+
+// Resident blocks (or clusters) per GPU for one kernel configuration, cached
+// so that every call on a device sees the same persistent grid.
+struct OccKey {
+    int device;
+    const void* fn;
+    int threads, smem, cluster;
+    bool operator<(const OccKey& o) const {
+        return std::tie(device, fn, threads, smem, cluster) <
+               std::tie(o.device, o.fn, o.threads, o.smem, o.cluster);
+    }
+};
+std::mutex g_occ_mu;
+std::map<OccKey, int> g_occ;
+
+cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, int smem,
+                           int cluster, int* out) {
+    const OccKey key{dev.device, fn, threads, smem, cluster};
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) {
+            *out = it->second;
+            return cudaSuccess;
+        }
+    }
+    cudaError_t err = cudaSuccess;
+    if (smem > 48 * 1024) {
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (err != cudaSuccess) return err;
+    }
+    int units = 0;
+    if (cluster <= 1) {
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+        if (err != cudaSuccess) return err;
+        units = per_sm * dev.sm_count;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(cluster * dev.sm_count));
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaOccupancyMaxActiveClusters(&units, fn, &cfg);
+        if (err != cudaSuccess) return err;
+    }
+    if (units < 1) return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    g_occ[key] = units;
+    *out = units;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
+    *p = rmsnorm_plan_t{};
+    p->cluster = 1;
+    p->rows_per_unit = 1;
+    const int sz = dtype_size(dtype);
+    const int64_t nvec = N / dtype_vec(dtype);
+    GroupShape g;
+    if (vector_ok && group_shape(nvec, &g)) {
+        p->variant = RMSNORM_VARIANT_ROWGROUP;
+        p->threads = g.threads;
+        p->threads_per_row = g.G;
+        p->vectors_per_thread = g.V;
+        p->rows_per_unit = (g.threads / g.G) * g.R;
+        const int unit = static_cast<int>(p->rows_per_unit * N * sz);
+        p->stages = std::max(3, std::min(6, kStageBudget / (2 * unit)));
+        p->smem_bytes = bwd_smem_bytes(p->stages, unit);
+        return;
+    }
+    if (vector_ok) {
+        int c = 1;
+        while (2 * cdiv(nvec, c) * 16 > kSliceBudget && c < kMaxCluster) c *= 2;
+        const int64_t slots = cdiv(nvec, c);
+        int v = 1;
+        while (v * 512 < slots && v < 8) v *= 2;
+        // at least three stages of the slice must fit in shared memory
+        const int threads = round_up(static_cast<int>(cdiv(slots, v)), 32);
+        if (v * 512 >= slots && bwd_smem_bytes(3, v * threads * 16) <= kSmemMax) {
+            p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
+            p->cluster = c;
+            p->vectors_per_thread = v;
+            p->threads = threads;
+            p->threads_per_row = p->threads * c;
+            const int unit = v * p->threads * 16;
+            p->stages = std::max(3, std::min(6, kStageBudget / (2 * unit)));
+            p->smem_bytes = bwd_smem_bytes(p->stages, unit);
+            return;
+        }
+    }
+    p->variant = RMSNORM_VARIANT_SCALAR;
+    p->threads = 256;
+    p->threads_per_row = 256;
+    p->vectors_per_thread = 0;
+    p->stages = 0;
+    p->smem_bytes = 0;
+}
+
+cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
+                            rmsnorm_plan_t* p) {
+    if (p->smem_bytes > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+    const void* fn = main_kernel_for(dtype, *p);
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    int units = 0;
+    cudaError_t err = resident_units(dev, fn, p->threads, p->smem_bytes, p->cluster, &units);
+    if (err != cudaSuccess) return err;
+    int64_t work = M;  // rows, or tiles of rows for the short-row kernel
+    if (p->variant == RMSNORM_VARIANT_ROWGROUP) work = cdiv(M, p->rows_per_unit);
+    const int64_t n = std::min<int64_t>(units, work);
+    p->partial_rows = static_cast<int>(n);
+    p->grid = static_cast<int>(n * p->cluster);
+    p->workspace_bytes = (n * N * 4 + 255) / 256 * 256;
+    return cudaSuccess;
+}
+
+cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cudaStream_t s) {
+    if (p.grid <= 0) return cudaSuccess;
+    const void* fn = main_kernel_for(dtype, p);
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (p.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    BwdArgs args = a;
+    int stages = p.stages;
+    void* kargs[2] = {&args, &stages};
+    cudaError_t err = cudaLaunchKernelExC(&cfg, fn, kargs);
+    if (err != cudaSuccess) return err;
+    const dim3 cs_block(32, 32);
+    const dim3 cs_grid(static_cast<unsigned>(cdiv(a.N, 32)));
+    colsum_kernel<<<cs_grid, cs_block, 0, s>>>(a.partial, a.dw, p.partial_rows, a.N);
+    return cudaGetLastError();
+}
+
+}  // namespace rmsn

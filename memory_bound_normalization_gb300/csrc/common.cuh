@@ -1,0 +1,212 @@
+// Device helpers shared by the RMSNorm kernels: 16-byte packing of bf16/fp32
+// rows, warp reductions, and inline-PTX wrappers for mbarriers, 1-D bulk
+// copies (cp.async.bulk, no tensor map), thread-block clusters and the
+// global timer used by the bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+// Status codes written to the device status word (match rmsnorm_status_t).
+constexpr int kStatusTimeout = 6;
+
+// ---------------------------------------------------------------- packing
+// A 16-byte vector holds VEC elements; arithmetic is always fp32.
+template <typename T>
+struct Pack;
+
+template <>
+struct Pack<float> {
+    static constexpr int VEC = 4;
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[VEC]) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[VEC]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                          __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+    __device__ __forceinline__ static float to_float(float v) { return v; }
+    __device__ __forceinline__ static float from_float(float v) { return v; }
+};
+
+template <>
+struct Pack<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    // bf16 is the high half of an fp32 bit pattern, so widening is a shift.
+    __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[VEC]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            f[2 * k] = __uint_as_float(w[k] << 16);
+            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[VEC]) {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                          pack2(f[6], f[7]));
+    }
+    __device__ __forceinline__ static float to_float(__nv_bfloat16 v) {
+        return __bfloat162float(v);
+    }
+    __device__ __forceinline__ static __nv_bfloat16 from_float(float v) {
+        return __float2bfloat16_rn(v);
+    }
+};
+
+// ------------------------------------------------------------ global memory
+__device__ __forceinline__ uint4 ld_global_16(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+// Streaming read: the row is used once, do not keep it in L1.
+__device__ __forceinline__ uint4 ld_global_16_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_global_16(void* p, const uint4& v) {
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+// ------------------------------------------------------------ reductions
+// xor butterfly: every lane ends with the same bits (each step adds the
+// same two operands in both partner lanes, and fp32 addition commutes).
+template <int WIDTH>
+__device__ __forceinline__ float group_allreduce(float v) {
+#pragma unroll
+    for (int off = WIDTH / 2; off >= 1; off /= 2) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// -------------------------------------------------------------- shared memory
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint4 ld_shared_16(const void* p) {
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+// Makes the initialised barriers visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with the given parity to complete, for at most
+// limit_ns nanoseconds. Returns false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ------------------------------------------------------------ bulk copies
+// 1-D global -> shared copy completed on an mbarrier (complete_tx). Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gmem,
+                                              uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses to the same buffers.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ clusters
+// Without a cluster launch every block is its own cluster of one.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Full cluster barrier: release this thread's prior shared-memory writes,
+// acquire the other blocks' ones. Every thread of every block calls it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::
+            : "memory");
+}
+// Reads a float from the same shared-memory variable in block `rank` of
+// this cluster (distributed shared memory).
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Records the first failure on the device status word.
+__device__ __forceinline__ void report_status(int* status, int code) {
+    if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+}  // namespace rmsn

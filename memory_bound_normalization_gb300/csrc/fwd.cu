@@ -1,0 +1,336 @@
+// RMSNorm forward kernels: y = x * rstd * w, rstd = 1/sqrt(mean(x^2) + eps).
+//
+// Definition: "Chapter 13: Fused RMSNorm" (hello-gpu), section 13.1 (eps
+// inside the square root; the mean divides by the true column count N, not a
+// padded width -- same chapter, the masking note under the Triton route).
+// Layout of the work follows the width of a row:
+//   * short rows (at most 256 16-byte vectors): a group of G <= 32 lanes per
+//     row, several rows per lane in flight, shuffle-only reduction;
+//   * mid rows: one thread block per row, row held in registers (x is read
+//     once from HBM), warp shuffles then one shared-memory hop -- the block
+//     per row shape of "RMSNorm backward (almost) without the column
+//     reduction", section "The forward pass", and the block kernel of the
+//     hello-gpu chapter;
+//   * wide rows: a thread-block cluster per row, each block holding a slice
+//     of the row, the row sum exchanged through distributed shared memory.
+// Any input that is not 16-byte aligned, or whose row is not a whole number
+// of 16-byte vectors, takes the scalar kernel.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmsn {
+namespace {
+
+// ---------------------------------------------------------------- short rows
+// Block = threads/G groups; group g handles rows tile + r*groups + g for
+// r < R, so at each r the block touches consecutive rows.
+template <typename T, int G, int V, int R>
+__global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__ x,
+                                                           const T* __restrict__ w,
+                                                           T* __restrict__ y,
+                                                           float* __restrict__ rstd, int64_t M,
+                                                           int N, float eps) {
+    using P = Pack<T>;
+    constexpr int VEC = P::VEC;
+    const int nvec = N / VEC;
+    const int lane = threadIdx.x % G;
+    const int group = threadIdx.x / G;
+    const int groups = blockDim.x / G;
+    const int64_t tile = static_cast<int64_t>(blockIdx.x) * groups * R;
+
+    uint4 xv[R][V];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = tile + static_cast<int64_t>(r) * groups + group;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * G + lane;
+            xv[r][j] = (row < M && k < nvec)
+                           ? ld_global_16_stream(x + row * N + static_cast<int64_t>(k) * VEC)
+                           : make_uint4(0, 0, 0, 0);
+        }
+    }
+    uint4 wv[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * G + lane;
+        wv[j] = k < nvec ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+    }
+
+    float ss[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            float f[VEC];
+            P::unpack(xv[r][j], f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc = fmaf(f[e], f[e], acc);
+        }
+        ss[r] = acc;
+    }
+#pragma unroll
+    for (int off = G / 2; off >= 1; off /= 2)
+#pragma unroll
+        for (int r = 0; r < R; ++r) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], off);
+
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t row = tile + static_cast<int64_t>(r) * groups + group;
+        if (row >= M) continue;
+        const float rs = rsqrtf(ss[r] / static_cast<float>(N) + eps);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * G + lane;
+            if (k >= nvec) continue;
+            float fx[VEC], fw[VEC], fy[VEC];
+            P::unpack(xv[r][j], fx);
+            P::unpack(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) fy[e] = fx[e] * rs * fw[e];
+            st_global_16(y + row * N + static_cast<int64_t>(k) * VEC, P::pack(fy));
+        }
+        if (lane == 0) rstd[row] = rs;
+    }
+}
+
+// ------------------------------------------------------- block/cluster per row
+// Cluster c (a single block when launched without clusters) owns row c; block
+// rank q of the cluster owns vector slots [q*S, (q+1)*S), S = V*blockDim.x,
+// thread t holding slots q*S + j*blockDim.x + t.
+template <typename T, int V>
+__global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
+                                                       const T* __restrict__ w,
+                                                       T* __restrict__ y, float* __restrict__ rstd,
+                                                       int64_t M, int N, float eps) {
+    using P = Pack<T>;
+    constexpr int VEC = P::VEC;
+    __shared__ float red[32];
+    __shared__ float cluster_part;
+
+    const uint32_t csize = cluster_size();
+    const uint32_t crank = cluster_rank();
+    const int64_t row = cluster_index();
+    const int nthr = blockDim.x;
+    const int nvec = N / VEC;
+    const int base = static_cast<int>(crank) * V * nthr;
+    const T* xr = x + row * N;
+
+    uint4 xv[V], wv[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = base + j * nthr + threadIdx.x;
+        const bool ok = k < nvec;
+        xv[j] = ok ? ld_global_16_stream(xr + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+        wv[j] = ok ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        float f[VEC];
+        P::unpack(xv[j], f);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+    // block: butterfly per warp, then one shared-memory hop
+    ss = group_allreduce<32>(ss);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float total = lane < (nthr >> 5) ? red[lane] : 0.f;
+    total = group_allreduce<32>(total);
+    if (csize > 1) {
+        // cluster: each block publishes its sum, then every thread adds the
+        // blocks' sums in rank order (same bits in every block)
+        if (threadIdx.x == 0) cluster_part = total;
+        cluster_sync_all();
+        total = 0.f;
+        for (uint32_t q = 0; q < csize; ++q) total += ld_cluster_f32(&cluster_part, q);
+    }
+    const float rs = rsqrtf(total / static_cast<float>(N) + eps);
+    T* yr = y + row * N;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = base + j * nthr + threadIdx.x;
+        if (k >= nvec) continue;
+        float fx[VEC], fw[VEC], fy[VEC];
+        P::unpack(xv[j], fx);
+        P::unpack(wv[j], fw);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) fy[e] = fx[e] * rs * fw[e];
+        st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack(fy));
+    }
+    if (crank == 0 && threadIdx.x == 0) rstd[row] = rs;
+    // a block's shared memory must outlive the other blocks' reads of it
+    if (csize > 1) cluster_sync_all();
+}
+
+// -------------------------------------------------------------------- scalar
+// Any alignment, any N: one block per row (grid-strided over rows), two
+// passes over the row with scalar loads.
+template <typename T>
+__global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x,
+                                                         const T* __restrict__ w,
+                                                         T* __restrict__ y,
+                                                         float* __restrict__ rstd, int64_t M,
+                                                         int N, float eps) {
+    using P = Pack<T>;
+    __shared__ float red[2][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
+        const T* xr = x + row * N;
+        float ss = 0.f;
+        for (int j = threadIdx.x; j < N; j += blockDim.x) {
+            const float v = P::to_float(xr[j]);
+            ss = fmaf(v, v, ss);
+        }
+        ss = group_allreduce<32>(ss);
+        if (lane == 0) red[it & 1][warp] = ss;
+        __syncthreads();
+        float total = lane < nw ? red[it & 1][lane] : 0.f;
+        total = group_allreduce<32>(total);
+        const float rs = rsqrtf(total / static_cast<float>(N) + eps);
+        T* yr = y + row * N;
+        for (int j = threadIdx.x; j < N; j += blockDim.x)
+            yr[j] = P::from_float(P::to_float(xr[j]) * rs * P::to_float(w[j]));
+        if (threadIdx.x == 0) rstd[row] = rs;
+    }
+}
+
+template <typename T, int G, int V, int R>
+cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    fwd_rowgroup_kernel<T, G, V, R><<<p.grid, p.threads, 0, s>>>(
+        static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd, a.M,
+        a.N, a.eps);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    const int G = p.threads_per_row, V = p.vectors_per_thread;
+    if (G == 4) return launch_rowgroup<T, 4, 1, 4>(p, a, s);
+    if (G == 8) return launch_rowgroup<T, 8, 1, 4>(p, a, s);
+    if (G == 16) return launch_rowgroup<T, 16, 1, 4>(p, a, s);
+    if (V == 1) return launch_rowgroup<T, 32, 1, 2>(p, a, s);
+    if (V == 2) return launch_rowgroup<T, 32, 2, 2>(p, a, s);
+    if (V == 4) return launch_rowgroup<T, 32, 4, 1>(p, a, s);
+    if (V == 8) return launch_rowgroup<T, 32, 8, 1>(p, a, s);
+    return cudaErrorInvalidValue;
+}
+
+template <typename T, int V>
+cudaError_t launch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (p.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, fwd_row_kernel<T, V>, static_cast<const T*>(a.x),
+                              static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
+                              a.eps);
+}
+
+template <typename T>
+cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    switch (p.vectors_per_thread) {
+        case 1: return launch_row<T, 1>(p, a, s);
+        case 2: return launch_row<T, 2>(p, a, s);
+        case 4: return launch_row<T, 4>(p, a, s);
+        case 8: return launch_row<T, 8>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    switch (p.variant) {
+        case RMSNORM_VARIANT_ROWGROUP: return dispatch_rowgroup<T>(p, a, s);
+        case RMSNORM_VARIANT_CTA_ROW:
+        case RMSNORM_VARIANT_CLUSTER_ROW: return dispatch_row<T>(p, a, s);
+        case RMSNORM_VARIANT_SCALAR:
+            fwd_scalar_kernel<T><<<p.grid, p.threads, 0, s>>>(
+                static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y),
+                a.rstd, a.M, a.N, a.eps);
+            return cudaGetLastError();
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+// Largest row (in 16-byte vectors) one block holds in registers: 1024
+// threads x 4 vectors. Wider rows are split over a cluster, then the vector
+// count per thread doubles; beyond that the scalar kernel runs.
+void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
+    *p = rmsnorm_plan_t{};
+    p->stages = 0;
+    p->cluster = 1;
+    p->rows_per_unit = 1;
+    const int64_t nvec = N / dtype_vec(dtype);
+    GroupShape g;
+    if (vector_ok && group_shape(nvec, &g)) {
+        p->variant = RMSNORM_VARIANT_ROWGROUP;
+        p->threads = g.threads;
+        p->threads_per_row = g.G;
+        p->vectors_per_thread = g.V;
+        p->rows_per_unit = (g.threads / g.G) * g.R;
+        return;
+    }
+    if (vector_ok) {
+        int c = 1, v = 4;
+        while (cdiv(nvec, c) > 1024 * v && c < kMaxCluster) c *= 2;
+        if (cdiv(nvec, c) > 1024 * v) v = 8;
+        if (cdiv(nvec, c) <= 1024 * v) {
+            const int64_t slots = cdiv(nvec, c);
+            p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
+            p->cluster = c;
+            p->vectors_per_thread = v;
+            p->threads = round_up(static_cast<int>(cdiv(slots, v)), 32);
+            p->threads_per_row = p->threads * c;
+            return;
+        }
+    }
+    p->variant = RMSNORM_VARIANT_SCALAR;
+    p->threads = 256;
+    p->threads_per_row = 256;
+    p->vectors_per_thread = 0;
+}
+
+cudaError_t fwd_finish_plan(const DeviceInfo& dev, int, int64_t M, rmsnorm_plan_t* p) {
+    switch (p->variant) {
+        case RMSNORM_VARIANT_ROWGROUP:
+            p->grid = static_cast<int>(cdiv(M, p->rows_per_unit));
+            break;
+        case RMSNORM_VARIANT_CTA_ROW:
+        case RMSNORM_VARIANT_CLUSTER_ROW:
+            p->grid = static_cast<int>(M * p->cluster);
+            break;
+        case RMSNORM_VARIANT_SCALAR:
+            p->grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(dev.sm_count) * 64));
+            break;
+        default:
+            p->grid = 0;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t fwd_launch(const rmsnorm_plan_t& p, int dtype, const FwdArgs& a, cudaStream_t s) {
+    if (p.grid <= 0) return cudaSuccess;
+    if (dtype == RMSNORM_BF16) return dispatch<__nv_bfloat16>(p, a, s);
+    return dispatch<float>(p, a, s);
+}
+
+}  // namespace rmsn

@@ -1,0 +1,88 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units (fwd.cu, bwd.cu, probe.cu). Host code only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rmsnorm.h"
+
+namespace rmsn {
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+    int l2_bytes = 0;
+    int* status_word = nullptr;  // device address of this device's status word
+};
+
+// Cached properties of `device` (nullptr if the query fails).
+const DeviceInfo* device_info(int device);
+
+struct FwdArgs {
+    const void* x;
+    const void* w;
+    void* y;
+    float* rstd;
+    int64_t M;
+    int N;
+    float eps;
+};
+
+struct BwdArgs {
+    const void* x;
+    const void* w;
+    const void* dy;
+    const float* rstd;
+    void* dx;
+    float* partial;  // [partial_rows, N] fp32 workspace
+    float* dw;
+    int64_t M;
+    int N;
+    int* status;
+    uint64_t wait_limit_ns;
+    int64_t drop_unit;  // failure-injection hook, -1 = off
+};
+
+constexpr int kMaxCluster = 8;
+
+// Width-dependent choices (host only, no device queries). `vector_ok` says
+// whether the pointers and N allow 16-byte vector access.
+void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);
+void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);
+
+// Device-dependent completion of a plan (grid size, shared-memory opt-in).
+cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p);
+cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
+                            rmsnorm_plan_t* p);
+
+cudaError_t fwd_launch(const rmsnorm_plan_t& p, int dtype, const FwdArgs& a, cudaStream_t s);
+cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cudaStream_t s);
+
+cudaError_t probe_launch(int kind, void* dst, const void* a, const void* b, size_t bytes,
+                         int grid, cudaStream_t s);
+
+// Row-group geometry shared by the forward and backward short-row kernels:
+// G lanes per row, V 16-byte vectors per lane, R rows per group per pass.
+struct GroupShape {
+    int G, V, R, threads;
+};
+inline bool group_shape(int64_t nvec, GroupShape* g) {
+    if (nvec <= 4) *g = {4, 1, 4, 256};
+    else if (nvec <= 8) *g = {8, 1, 4, 256};
+    else if (nvec <= 16) *g = {16, 1, 4, 256};
+    else if (nvec <= 32) *g = {32, 1, 2, 256};
+    else if (nvec <= 64) *g = {32, 2, 2, 256};
+    else if (nvec <= 128) *g = {32, 4, 1, 256};
+    else if (nvec <= 256) *g = {32, 8, 1, 128};
+    else return false;
+    return true;
+}
+
+inline int dtype_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
+inline int dtype_vec(int dtype) { return 16 / dtype_size(dtype); }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+}  // namespace rmsn

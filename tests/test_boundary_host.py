@@ -1,0 +1,152 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, rejects bad arguments before touching CUDA, and its width ladder
+makes consistent choices. No kernel is launched here."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import memory_bound_normalization_gb300 as pkg
+from memory_bound_normalization_gb300 import build as libbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "rmsnorm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return pkg.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"\b(rmsnorm_[a-z0-9_]+)\s*\(", text)
+
+
+def test_header_and_exports_agree(lib):
+    names = header_functions()
+    assert names == list(pkg.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in rmsnorm.h but not exported"
+
+
+def test_exports_are_c_symbols(lib):
+    # extern "C": plain names, callable through ctypes without mangling
+    for n in pkg.EXPORTS:
+        ctypes.cast(getattr(lib, n), ctypes.c_void_p)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = pkg.rmsnorm_status_string(code)
+        assert s.startswith("RMSNORM_") and "UNKNOWN" not in s
+    assert "UNKNOWN" in pkg.rmsnorm_status_string(99)
+    assert pkg.rmsnorm_version().count(".") == 2
+
+
+FAKE = 1 << 20  # aligned non-null addresses; never dereferenced by these calls
+
+
+def test_argument_checks_need_no_device(lib):
+    B, F = pkg.BF16, pkg.F32
+    fwd = pkg.rmsnorm_fwd
+    # M == 0: nothing to do
+    assert fwd(FAKE, FAKE, FAKE, FAKE, 0, 64, 1e-6, B, 0) == pkg.OK
+    # shape, dtype and eps
+    assert fwd(FAKE, FAKE, FAKE, FAKE, 4, 0, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert fwd(FAKE, FAKE, FAKE, FAKE, -1, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert fwd(FAKE, FAKE, FAKE, FAKE, 4, 1 << 31, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert fwd(FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, 5, 0) == pkg.ERR_INVALID_ARG
+    assert fwd(FAKE, FAKE, FAKE, FAKE, 4, 64, -1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert fwd(FAKE, FAKE, FAKE, FAKE, 4, 64, math.nan, B, 0) == pkg.ERR_INVALID_ARG
+    # null tensors
+    assert fwd(None, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert fwd(FAKE, FAKE, FAKE, None, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    # misaligned element or fp32 pointers
+    assert fwd(FAKE + 1, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_MISALIGNED
+    assert fwd(FAKE + 2, FAKE, FAKE, FAKE, 4, 64, 1e-6, F, 0) == pkg.ERR_MISALIGNED
+    assert fwd(FAKE, FAKE, FAKE, FAKE + 2, 4, 64, 1e-6, B, 0) == pkg.ERR_MISALIGNED
+
+    bwd = pkg.rmsnorm_bwd
+    assert bwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 64, B, 0) == pkg.OK
+    assert bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 0, B, 0) == pkg.ERR_INVALID_ARG
+    assert bwd(FAKE, FAKE, None, FAKE, FAKE, FAKE, 4, 64, B, 0) == pkg.ERR_INVALID_ARG
+    assert bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, 4, 64, B, 0) == pkg.ERR_MISALIGNED
+    assert bwd(FAKE, FAKE, FAKE, FAKE + 1, FAKE, FAKE, 4, 64, B, 0) == pkg.ERR_MISALIGNED
+    ws = pkg.rmsnorm_bwd_ws
+    assert ws(FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 64, B, None, 0, 0) == pkg.OK
+    assert ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 3, FAKE, 1 << 20, 0) == \
+        pkg.ERR_INVALID_ARG
+    assert pkg.rmsnorm_bwd_workspace_size(0, 64, B, 0) == 0
+    assert pkg.rmsnorm_bwd_workspace_size(4, 0, B, 0) == 0
+
+    probe = pkg.rmsnorm_probe
+    assert probe(7, FAKE, FAKE, FAKE, 1024, 1, 0) == pkg.ERR_INVALID_ARG
+    assert probe(pkg.PROBE_COPY, FAKE, FAKE, None, 1000, 1, 0) == pkg.ERR_INVALID_ARG
+    assert probe(pkg.PROBE_COPY, FAKE, None, None, 1024, 1, 0) == pkg.ERR_INVALID_ARG
+    assert probe(pkg.PROBE_2R1W, FAKE, FAKE, None, 1024, 1, 0) == pkg.ERR_INVALID_ARG
+    assert probe(pkg.PROBE_WRITE, FAKE, None, None, 1024, 0, 0) == pkg.ERR_INVALID_ARG
+    assert probe(pkg.PROBE_WRITE, FAKE + 8, None, None, 1024, 1, 0) == pkg.ERR_MISALIGNED
+    assert probe(pkg.PROBE_WRITE, FAKE, None, None, 0, 1, 0) == pkg.OK
+
+    # test hooks are plain setters
+    pkg.rmsnorm_set_wait_limit_ns(0)
+    pkg.rmsnorm_test_drop_copy(-1)
+
+
+WIDTHS = sorted({1, 2, 3, 4, 7, 8, 13, 16, 24, 32, 40, 64, 96, 100, 128, 200, 256, 257, 512,
+                 768, 1000, 1024, 1536, 2048, 2049, 2880, 3072, 4096, 5120, 6144, 8192, 12288,
+                 16384, 24576, 32768, 49152, 65536, 131072, 262144, 300000, 524288, 1 << 20})
+
+
+@pytest.mark.parametrize("dtype", [pkg.BF16, pkg.F32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("N", WIDTHS)
+def test_width_ladder(lib, N, dtype):
+    """Every width maps to one kernel family whose slots cover the row, with
+    legal block, cluster and shared-memory sizes."""
+    vec = 8 if dtype == pkg.BF16 else 4
+    vector_ok = (N * (16 // vec)) % 16 == 0
+    for pass_ in (pkg.PASS_FWD, pkg.PASS_BWD):
+        p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
+        assert p.grid == 0  # no device queried
+        assert p.threads % 32 == 0 and 32 <= p.threads <= 1024
+        assert 1 <= p.cluster <= 8
+        assert p.smem_bytes <= 227 * 1024
+        name = pkg.VARIANTS[p.variant]
+        if not vector_ok:
+            assert name == "scalar"
+            continue
+        if name == "rowgroup":
+            assert p.threads_per_row in (4, 8, 16, 32)
+            assert p.threads_per_row * p.vectors_per_thread * vec >= N
+            assert p.rows_per_unit % (p.threads // p.threads_per_row) == 0
+        elif name in ("cta_row", "cluster_row"):
+            assert (name == "cluster_row") == (p.cluster > 1)
+            assert p.threads * p.vectors_per_thread * p.cluster * vec >= N
+            assert p.threads_per_row == p.threads * p.cluster
+        else:
+            # vector kernels cover every row up to 256 KiB; wider rows may
+            # outgrow registers (forward) or shared memory (backward)
+            assert name == "scalar" and N * (16 // vec) > 256 * 1024
+        if pass_ == pkg.PASS_BWD and name != "scalar":
+            assert 3 <= p.stages <= 6
+            if name == "rowgroup":
+                unit = p.rows_per_unit * N * (16 // vec)
+            else:
+                unit = p.vectors_per_thread * p.threads * 16
+            assert p.smem_bytes >= 2 * p.stages * unit
+
+
+def test_plan_rejects_bad_arguments(lib):
+    with pytest.raises(pkg.RMSNormError):
+        pkg.rmsnorm_plan(10, 0, pkg.BF16, pkg.PASS_FWD)
+    with pytest.raises(pkg.RMSNormError):
+        pkg.rmsnorm_plan(10, 64, pkg.BF16, 7)
+    p = pkg.rmsnorm_plan(0, 64, pkg.BF16, pkg.PASS_BWD)
+    assert pkg.VARIANTS[p.variant] == "none"

@@ -1,0 +1,236 @@
+"""CUDA library vs fp64 oracle, element by element, through the C ABI.
+
+Small shapes (the oracle finishes in seconds) cover every kernel family and
+both dtypes with several tiles and a ragged tail; the full workload sizes are
+checked on sampled rows (every column of >= 4096 random rows plus the first
+and last) and on the whole of dw, in the same launch configuration the
+benchmark times.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import check_dw, check_rows, check_rstd
+
+pytestmark = pytest.mark.gpu
+
+pkg = pytest.importorskip("memory_bound_normalization_gb300")
+from memory_bound_normalization_gb300 import synth  # noqa: E402
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    torch.cuda.set_device(0)
+    pkg.load_library(build_if_missing=True)
+    oracle.build()
+    yield
+
+
+def run(x, w, dy, eps):
+    """fwd + bwd on the GPU through the C ABI; returns host tensors."""
+    M, N = x.shape
+    code = pkg.dtype_code(x.dtype)
+    y = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=torch.float32, device=x.device)
+    pkg.check(pkg.rmsnorm_fwd(x, w, y, rstd, M, N, eps, code), "fwd")
+    pkg.check(pkg.rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, code), "bwd")
+    st = pkg.rmsnorm_get_last_device_error()
+    assert st == pkg.OK, pkg.rmsnorm_status_string(st)
+    return y, rstd, dx, dw
+
+
+def check_all(x, w, dy, eps, y, rstd, dx, dw, rows=None):
+    xc, wc, dyc = x.cpu(), w.cpu(), dy.cpu()
+    y_ref, r_ref = oracle.fwd(xc, wc, eps, rows=rows)
+    dx_ref = oracle.bwd_dx(xc, wc, dyc, eps, rows=rows)
+    dw_ref = oracle.bwd_dw(xc, dyc, eps)
+    sel = slice(None) if rows is None else torch.as_tensor(rows)
+    check_rows(y[sel], y_ref, x.dtype, "y")
+    check_rows(dx[sel], dx_ref, x.dtype, "dx")
+    check_rstd(rstd[sel], r_ref)
+    check_dw(dw, dw_ref)
+
+
+def inputs(M, N, dtype, seed=0, dy_scale=1.0):
+    wl = synth.Workload(f"t{M}x{N}", M, N, dtype, 1e-5, 100 + seed, 200 + seed, 300 + seed,
+                        dy_scale=dy_scale)
+    return synth.make_inputs(wl, device=DEV), wl.eps
+
+
+SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (37, 256),
+          (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (5, 6144), (4, 8192),
+          (3, 16384), (2, 32768), (2, 65536), (1, 65536), (1000, 40), (777, 96)]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("M,N", SHAPES, ids=[f"{m}x{n}" for m, n in SHAPES])
+def test_small_shapes(M, N, dtype):
+    inp, eps = inputs(M, N, dtype)
+    out = run(inp["x"], inp["w"], inp["dy"], eps)
+    check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("N", [128, 1024, 4096, 16384])
+def test_rows_around_persistent_grid(N, dtype):
+    """M just below, at and above the persistent grid size, and a few rows
+    per block, so that some blocks get one row (or tile) more than others."""
+    code = pkg.dtype_code(dtype)
+    plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_BWD, 0)
+    per_unit = plan.rows_per_unit
+    P = plan.partial_rows
+    for M in sorted({max(1, (P - 1) * per_unit), P * per_unit, P * per_unit + 1,
+                     3 * P * per_unit + per_unit // 2 + 1}):
+        inp, eps = inputs(M, N, dtype, seed=M % 7)
+        out = run(inp["x"], inp["w"], inp["dy"], eps)
+        check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("N", [128, 4096, 4104])
+def test_unaligned_pointers(N, dtype):
+    """Tensors starting one element past a 16-byte boundary take the scalar
+    kernels and still match."""
+    M = 50
+    inp, eps = inputs(M, N, dtype)
+    views = {}
+    for k in ("x", "dy"):
+        buf = torch.empty(M * N + 1, dtype=dtype, device=DEV)
+        buf[1:].copy_(inp[k].view(-1))
+        views[k] = buf[1:].view(M, N)
+    wbuf = torch.empty(N + 1, dtype=dtype, device=DEV)
+    wbuf[1:].copy_(inp["w"])
+    w = wbuf[1:]
+    assert views["x"].data_ptr() % 16 != 0
+    out = run(views["x"], w, views["dy"], eps)
+    check_all(views["x"], w, views["dy"], eps, *out)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_worked_examples(dtype):
+    """The printed examples of the hello-gpu Fused RMSNorm chapter, section
+    13.1 and Figure 13.1, on the GPU (values are exact in bf16)."""
+    x = torch.tensor([[3.0, 4.0]], dtype=dtype, device=DEV)
+    w = torch.tensor([1.0, 1.0], dtype=dtype, device=DEV)
+    y, rstd = pkg.forward(x, w, 1e-5)
+    tol = 5e-5 if dtype == torch.float32 else 4e-3
+    assert np.allclose(y.float().cpu().numpy()[0], [0.8485, 1.1314], atol=tol)
+    assert abs(rstd.item() - 0.2828) < 5e-5
+    x = torch.tensor([[3.0, 4.0, -3.0, -4.0]], dtype=dtype, device=DEV)
+    w = torch.tensor([1.0, 0.5, 2.0, 1.0], dtype=dtype, device=DEV)
+    y, rstd = pkg.forward(x, w, 1e-5)
+    assert abs(y.float()[0, 1].item() - 0.5657) < tol
+    assert abs(rstd.item() - 0.2828) < 5e-5
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("N", [128, 4096, 65536])
+def test_special_rows(N, dtype):
+    """Zero rows (y = 0, rstd = eps^-1/2), a row with a NaN (propagates to
+    that row only), huge values, and zero weights in some columns."""
+    M = 6
+    inp, eps = inputs(M, N, dtype)
+    x, w, dy = inp["x"].clone(), inp["w"].clone(), inp["dy"]
+    x[1].zero_()
+    x[3, N // 3] = float("nan")
+    x[4] *= 1e4 if dtype == torch.float32 else 1e3
+    w[: N // 8] = 0
+    out = run(x, w, dy, eps)
+    y, rstd, dx, dw = out
+    assert torch.all(y[1] == 0)
+    assert abs(rstd[1].item() - eps ** -0.5) / eps ** -0.5 < 1e-5
+    assert torch.isnan(y[3].float()).all() and not torch.isnan(y[2].float()).any()
+    keep = [0, 1, 2, 4, 5]
+    xc, wc, dyc = x.cpu(), w.cpu(), dy.cpu()
+    y_ref, r_ref = oracle.fwd(xc, wc, eps, rows=keep)
+    dx_ref = oracle.bwd_dx(xc, wc, dyc, eps, rows=keep)
+    check_rows(y[keep], y_ref, dtype, "y")
+    check_rows(dx[keep], dx_ref, dtype, "dx")
+    check_rstd(rstd[keep], r_ref)
+    assert torch.all(y[keep][:, : N // 8] == 0)
+    # dw has NaN exactly in the columns the NaN row touches: every column
+    assert torch.isnan(dw).all()
+
+
+def test_empty_and_degenerate():
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device=DEV)
+    w = torch.ones(64, dtype=torch.bfloat16, device=DEV)
+    y = torch.empty_like(x)
+    rstd = torch.empty(0, dtype=torch.float32, device=DEV)
+    dw = torch.full((64,), 7.0, device=DEV)
+    assert pkg.rmsnorm_fwd(x, w, y, rstd, 0, 64, 1e-6, pkg.BF16) == pkg.OK
+    assert pkg.rmsnorm_bwd(x, w, x, rstd, y, dw, 0, 64, pkg.BF16) == pkg.OK
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0), "empty backward must give dw = 0 (the empty sum)"
+    # invalid arguments are rejected before anything runs
+    assert pkg.rmsnorm_fwd(x, w, y, rstd, 4, 0, 1e-6, pkg.BF16) == pkg.ERR_INVALID_ARG
+    assert pkg.rmsnorm_fwd(x, w, y, rstd, 4, 64, -1.0, pkg.BF16) == pkg.ERR_INVALID_ARG
+    assert pkg.rmsnorm_fwd(x, w, y, rstd, 4, 64, 1e-6, 9) == pkg.ERR_INVALID_ARG
+    assert pkg.rmsnorm_fwd(0, w, y, rstd, 4, 64, 1e-6, pkg.BF16) == pkg.ERR_INVALID_ARG
+
+
+def test_workspace_entry_point():
+    M, N = 300, 4096
+    inp, eps = inputs(M, N, torch.bfloat16)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    y, rstd = pkg.forward(x, w, eps)
+    need = pkg.rmsnorm_bwd_workspace_size(M, N, pkg.BF16, 0)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=torch.float32, device=DEV)
+    assert pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, ws, need - 16) == \
+        pkg.ERR_INVALID_ARG
+    assert pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, ws.data_ptr() + 4, need) == \
+        pkg.ERR_MISALIGNED
+    pkg.check(pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, ws, need))
+    dx2, dw2 = pkg.backward(x, w, dy, rstd)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dx2) and torch.equal(dw, dw2)
+    check_all(x, w, dy, eps, y, rstd, dx, dw)
+
+
+@pytest.mark.parametrize("wl_name", ["hidden4096_16384x4096", "qknorm_1048576x128",
+                                     "sweep_bf16_N65536", "sweep_f32_N2880"])
+def test_dw_bitwise_repeatable(wl_name):
+    """Ten backward calls give bitwise-identical dw and dx."""
+    wl = synth.WORKLOADS[wl_name]
+    inp = synth.make_inputs(wl, device=DEV)
+    y, rstd = pkg.forward(inp["x"], inp["w"], wl.eps)
+    dx0, dw0 = pkg.backward(inp["x"], inp["w"], inp["dy"], rstd)
+    for _ in range(9):
+        dx, dw = pkg.backward(inp["x"], inp["w"], inp["dy"], rstd)
+        assert torch.equal(dw.view(torch.int32), dw0.view(torch.int32))
+        assert torch.equal(dx.view(torch.int16 if wl.dtype == torch.bfloat16 else torch.int32),
+                           dx0.view(torch.int16 if wl.dtype == torch.bfloat16 else torch.int32))
+
+
+FULL = ["small_256x1024", "hidden4096_16384x4096", "hidden8192_32768x8192_outliers",
+        "qknorm_1048576x128"] + [w.name for w in synth.width_sweep(torch.bfloat16)] + \
+       [w.name for w in synth.width_sweep(torch.float32)]
+
+
+@pytest.mark.parametrize("wl_name", FULL)
+def test_full_size_sampled(wl_name):
+    """Full workload sizes: every column of >= 4096 random rows (plus the
+    first and last) for y, rstd and dx; all of dw."""
+    wl = synth.WORKLOADS[wl_name]
+    inp = synth.make_inputs(wl, device=DEV)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    if wl.outlier_frac:
+        big = (x.float().abs() > 20).sum().item()
+        assert big >= 0.8 * synth.outlier_count(wl)
+    out = run(x, w, dy, wl.eps)
+    M = wl.M
+    rng = np.random.default_rng(12345)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, size=min(M, 4096), replace=False)]))
+    check_all(x, w, dy, wl.eps, *out, rows=rows)
