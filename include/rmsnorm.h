@@ -27,7 +27,8 @@
  *     results are valid once the stream has reached the call.
  *   - Return value is an rmsnorm_status_t. Arguments are checked before any
  *     CUDA call; nothing aborts or throws across this boundary.
- *     M == 0 is a no-op returning RMSNORM_OK. M < 0, N <= 0, N > 2^31-1, an
+ *     M == 0 launches no kernel and returns RMSNORM_OK (the backward then
+ *     sets dw to zero, the empty sum, when dw is not NULL). M < 0, N <= 0, N > 2^31-1, an
  *     unknown dtype, a negative or NaN eps, or a NULL tensor pointer when
  *     M > 0 return RMSNORM_ERR_INVALID_ARG. rstd or dw not 4-byte aligned,
  *     or an element pointer not aligned to its element size, return
@@ -180,8 +181,11 @@ typedef struct {
     int threads;            /* threads per block */
     int vectors_per_thread; /* 16-byte vectors of a row each thread owns */
     int threads_per_row;    /* lanes sharing one row (ROWGROUP), else threads */
-    int rows_per_unit;      /* rows moved per bulk copy / per block pass */
+    int rows_per_unit;      /* rows per block pass (row-group tile, or row groups) */
     int cluster;            /* blocks per row (1 unless CLUSTER_ROW) */
+    int row_groups;         /* independent row groups per block (backward
+                               CTA_ROW: each group of threads/row_groups
+                               threads owns its own rows; else 1) */
     int stages;             /* shared-memory pipeline depth (backward) */
     int smem_bytes;         /* dynamic shared memory per block */
     int grid;               /* blocks launched; 0 when device < 0 */

@@ -69,6 +69,7 @@ class Plan(ctypes.Structure):
         ("threads_per_row", ctypes.c_int),
         ("rows_per_unit", ctypes.c_int),
         ("cluster", ctypes.c_int),
+        ("row_groups", ctypes.c_int),
         ("stages", ctypes.c_int),
         ("smem_bytes", ctypes.c_int),
         ("grid", ctypes.c_int),

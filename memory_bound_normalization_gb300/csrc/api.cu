@@ -28,6 +28,15 @@ std::atomic<int64_t> g_drop_unit{-1};
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Maps a CUDA result to a status. A failure is also cleared from the
+// runtime's last-error slot, so it does not surface in the caller's next,
+// unrelated CUDA call.
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return RMSNORM_OK;
+    cudaGetLastError();
+    return RMSNORM_ERR_CUDA;
+}
+
 int shape_status(int64_t M, int64_t N, int dtype) {
     if (M < 0 || N <= 0 || N > INT32_MAX) return RMSNORM_ERR_INVALID_ARG;
     if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
@@ -36,7 +45,7 @@ int shape_status(int64_t M, int64_t N, int dtype) {
 
 int current_device(const DeviceInfo** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (cuda_status(cudaGetDevice(&dev)) != RMSNORM_OK) return RMSNORM_ERR_CUDA;
     *out = device_info(dev);
     return *out ? RMSNORM_OK : RMSNORM_ERR_CUDA;
 }
@@ -64,8 +73,7 @@ int bwd_prepare(const void* x, const void* w, const void* dy, const float* rstd,
     bwd_choose(N, dtype, vec, plan);
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
-    if (bwd_finish_plan(**dev, dtype, M, N, plan) != cudaSuccess) return RMSNORM_ERR_CUDA;
-    return RMSNORM_OK;
+    return cuda_status(bwd_finish_plan(**dev, dtype, M, N, plan));
 }
 
 int bwd_run(const void* x, const void* w, const void* dy, const float* rstd, void* dx, float* dw,
@@ -84,7 +92,7 @@ int bwd_run(const void* x, const void* w, const void* dy, const float* rstd, voi
     a.status = dev.status_word;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.drop_unit = plan.variant != RMSNORM_VARIANT_SCALAR ? g_drop_unit.exchange(-1) : -1;
-    return bwd_launch(plan, dtype, a, stream) == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+    return cuda_status(bwd_launch(plan, dtype, a, stream));
 }
 
 }  // namespace
@@ -94,8 +102,10 @@ const DeviceInfo* device_info(int device) {
     std::lock_guard<std::mutex> lk(g_dev_mu);
     if (g_dev_ready[device]) return &g_dev[device];
     int prev = -1;
-    if (cudaGetDevice(&prev) != cudaSuccess) return nullptr;
-    if (prev != device && cudaSetDevice(device) != cudaSuccess) return nullptr;
+    if (cudaGetDevice(&prev) != cudaSuccess || (prev != device && cudaSetDevice(device) != cudaSuccess)) {
+        cudaGetLastError();
+        return nullptr;
+    }
     DeviceInfo d;
     d.device = device;
     bool ok = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) == cudaSuccess &&
@@ -103,7 +113,10 @@ const DeviceInfo* device_info(int device) {
               cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, device) == cudaSuccess &&
               cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status_word), g_status_word) == cudaSuccess;
     if (prev != device) cudaSetDevice(prev);
-    if (!ok || d.sm_count <= 0) return nullptr;
+    if (!ok || d.sm_count <= 0) {
+        cudaGetLastError();
+        return nullptr;
+    }
     g_dev[device] = d;
     g_dev_ready[device] = true;
     return &g_dev[device];
@@ -131,14 +144,15 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     const DeviceInfo* dev = nullptr;
     st = current_device(&dev);
     if (st != RMSNORM_OK) return st;
-    if (fwd_finish_plan(*dev, dtype, M, &plan) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan));
+    if (st != RMSNORM_OK) return st;
     if (static_cast<int64_t>(plan.grid) <= 0 ||
         (plan.variant != RMSNORM_VARIANT_SCALAR &&
          cdiv(M, plan.variant == RMSNORM_VARIANT_ROWGROUP ? plan.rows_per_unit : 1) * plan.cluster >
              INT32_MAX))
         return RMSNORM_ERR_UNSUPPORTED;
     FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps};
-    return fwd_launch(plan, dtype, a, stream) == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+    return cuda_status(fwd_launch(plan, dtype, a, stream));
 }
 
 size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype, int device) {
@@ -152,7 +166,7 @@ size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype, int device) {
     for (int vec = 0; vec < 2; ++vec) {
         if (vec && (N * dtype_size(dtype)) % 16 != 0) continue;
         bwd_choose(N, dtype, vec != 0, &plan);
-        if (bwd_finish_plan(*dev, dtype, M, N, &plan) != cudaSuccess) return 0;
+        if (cuda_status(bwd_finish_plan(*dev, dtype, M, N, &plan)) != RMSNORM_OK) return 0;
         if (static_cast<size_t>(plan.workspace_bytes) > need) need = static_cast<size_t>(plan.workspace_bytes);
     }
     return need;
@@ -167,9 +181,7 @@ int rmsnorm_bwd_ws(const void* x, const void* w, const void* dy, const float* rs
     if (st != RMSNORM_OK) return st;
     if (M == 0) {
         if (dw == nullptr) return RMSNORM_OK;
-        return cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream) == cudaSuccess
-                   ? RMSNORM_OK
-                   : RMSNORM_ERR_CUDA;
+        return cuda_status(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream));
     }
     if (workspace == nullptr || workspace_bytes < static_cast<size_t>(plan.workspace_bytes))
         return RMSNORM_ERR_INVALID_ARG;
@@ -185,28 +197,27 @@ int rmsnorm_bwd(const void* x, const void* w, const void* dy, const float* rstd,
     if (st != RMSNORM_OK) return st;
     if (M == 0) {
         if (dw == nullptr) return RMSNORM_OK;
-        return cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream) == cudaSuccess
-                   ? RMSNORM_OK
-                   : RMSNORM_ERR_CUDA;
+        return cuda_status(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream));
     }
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, static_cast<size_t>(plan.workspace_bytes), stream) != cudaSuccess) {
-        cudaGetLastError();
+    if (cuda_status(cudaMallocAsync(&ws, static_cast<size_t>(plan.workspace_bytes), stream)) !=
+        RMSNORM_OK)
         return RMSNORM_ERR_NOMEM;
-    }
     st = bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, ws, stream);
-    if (cudaFreeAsync(ws, stream) != cudaSuccess && st == RMSNORM_OK) st = RMSNORM_ERR_CUDA;
+    const int freed = cuda_status(cudaFreeAsync(ws, stream));
+    if (st == RMSNORM_OK) st = freed;
     return st;
 }
 
 int rmsnorm_get_last_device_error(cudaStream_t stream) {
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (cuda_status(cudaStreamSynchronize(stream)) != RMSNORM_OK) return RMSNORM_ERR_CUDA;
     const DeviceInfo* dev = nullptr;
     if (current_device(&dev) != RMSNORM_OK) return RMSNORM_ERR_CUDA;
     int v = 0;
-    if (cudaMemcpy(&v, dev->status_word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (cuda_status(cudaMemcpy(&v, dev->status_word, sizeof v, cudaMemcpyDeviceToHost)) != RMSNORM_OK)
         return RMSNORM_ERR_CUDA;
-    if (v != 0 && cudaMemset(dev->status_word, 0, sizeof v) != cudaSuccess) return RMSNORM_ERR_CUDA;
+    if (v != 0 && cuda_status(cudaMemset(dev->status_word, 0, sizeof v)) != RMSNORM_OK)
+        return RMSNORM_ERR_CUDA;
     return v;
 }
 
@@ -243,8 +254,7 @@ int rmsnorm_probe(int kind, void* dst, const void* a, const void* b, size_t byte
     int st = current_device(&dev);
     if (st != RMSNORM_OK) return st;
     const int grid = dev->sm_count * blocks_per_sm;
-    return probe_launch(kind, dst, a, b, bytes, grid, stream) == cudaSuccess ? RMSNORM_OK
-                                                                              : RMSNORM_ERR_CUDA;
+    return cuda_status(probe_launch(kind, dst, a, b, bytes, grid, stream));
 }
 
 int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_plan_t* out) {
@@ -266,7 +276,7 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     if (!dev) return RMSNORM_ERR_CUDA;
     cudaError_t e = pass == RMSNORM_PASS_FWD ? fwd_finish_plan(*dev, dtype, M, out)
                                              : bwd_finish_plan(*dev, dtype, M, N, out);
-    return e == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+    return cuda_status(e);
 }
 
 const char* rmsnorm_version(void) { return "0.1.0"; }

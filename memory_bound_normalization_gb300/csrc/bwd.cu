@@ -24,8 +24,11 @@
 // short rows move as tiles of whole rows. Every wait on a copy is bounded in
 // time and reports a status instead of hanging.
 #include <algorithm>
+#include <cstdlib>
 #include <map>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <tuple>
 
 #include "common.cuh"
@@ -38,62 +41,101 @@ constexpr int kStageBudget = 96 * 1024;   // shared memory aimed at per block
 constexpr int kSliceBudget = 48 * 1024;   // x+dy bytes of one row slice per stage
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory a block may opt into
 
-// Dynamic shared memory: [S][unit] x | [S][unit] dy | mbarrier[S] |
-// reduction slots [2][32] | cluster slots [2] | failure flag.
+// Shared memory of the short-row kernel: [S][unit] x | [S][unit] dy |
+// mbarrier[S] | 66 floats of reduction slots | failure flag.
 __host__ __device__ inline int bwd_smem_bytes(int stages, int unit) {
     return 2 * stages * unit + stages * 8 + 64 * 4 + 2 * 4 + 16;
 }
 
-// ------------------------------------------------ block or cluster per row
+// Shared memory of the row kernel with `groups` row groups: per group
+// [S][unit] x | [S][unit] dy | mbarrier[S] | reduction slots [2][32] |
+// failure flag, padded to a multiple of 128 bytes so that every group's ring
+// starts 16-byte aligned (bulk copies and 16-byte shared loads need it); then
+// two cluster slots.
+__host__ __device__ inline int bwd_row_group_stride(int stages, int unit) {
+    return (2 * stages * unit + stages * 8 + 64 * 4 + 16 + 127) / 128 * 128;
+}
+__host__ __device__ inline int bwd_row_smem_bytes(int groups, int stages, int unit) {
+    return groups * bwd_row_group_stride(stages, unit) + 16;
+}
+
+__device__ __forceinline__ void group_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Lets the dependent column-sum grid launch while this grid finishes.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------- row groups, blocks or clusters per row
+// A block holds `groups` independent row groups of TG = blockDim.x / groups
+// threads. Group g of block b works as a virtual block v = b*groups + g of
+// P*groups: it owns rows v, v + P*groups, ..., has its own bulk-copy ring and
+// named barrier, and keeps its dw contribution in registers. At the end the
+// groups' dw are added in group order, so every block writes one partial row.
+// With a cluster launch (groups == 1) the cluster owns the row and block rank
+// q of the cluster holds vector slots [q*V*TG, (q+1)*V*TG) of it; the row sum
+// is exchanged through distributed shared memory.
 template <typename T, int V>
-__global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages) {
+__global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int groups) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int nthr = blockDim.x, tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    const int tid = threadIdx.x;
+    const int TG = blockDim.x / groups;
+    const int g = tid / TG, gt = tid % TG;
+    const int gwarp = gt >> 5, lane = tid & 31, gnw = TG >> 5;
     const uint32_t csize = cluster_size();
     const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
     const int64_t cid = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
     const int64_t ncl = csize > 1 ? static_cast<int64_t>(cluster_count()) : gridDim.x;
+    const int64_t vid = cid * groups + g;       // virtual block of this group
+    const int64_t nvirt = ncl * groups;
     const int N = a.N;
     const int nvec = N / VEC;
-    const int slots = V * nthr;
+    const int slots = V * TG;
     const int vbeg = static_cast<int>(crank) * slots;
     const int vcnt = max(0, min(slots, nvec - vbeg));
     const uint32_t bytes = static_cast<uint32_t>(vcnt) * 16u;
     const int S = stages;
     const int unit = slots * 16;
 
-    unsigned char* sx = smem;
-    unsigned char* sdy = smem + S * unit;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * S * unit);
+    const int gstride = bwd_row_group_stride(S, unit);
+    unsigned char* gbase = smem + g * gstride;
+    unsigned char* sx = gbase;
+    unsigned char* sdy = gbase + S * unit;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + 2 * S * unit);
     float* red = reinterpret_cast<float*>(bar + S);
-    float* cpart = red + 64;
-    volatile int* fail = reinterpret_cast<volatile int*>(cpart + 2);
+    volatile int* fail = reinterpret_cast<volatile int*>(red + 64);
+    float* cpart = reinterpret_cast<float*>(smem + groups * gstride);
 
     const T* X = static_cast<const T*>(a.x);
     const T* DY = static_cast<const T*>(a.dy);
     const T* W = static_cast<const T*>(a.w);
     T* DX = static_cast<T*>(a.dx);
+    const int bar_id = 1 + g;  // named barrier of this group (0 is __syncthreads)
 
-    // rows of this cluster: cid, cid+ncl, ...
-    const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
+    // rows of this group: vid, vid + nvirt, ...
+    const int64_t nrows = vid < a.M ? (a.M - 1 - vid) / nvirt + 1 : 0;
 
-    if (tid == 0) {
+    if (gt == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
         *fail = 0;
         fence_mbarrier_init();
     }
     __syncthreads();
 
-    // Producer state, meaningful in thread 0 only: stages with a copy in
-    // flight and the parity of the phase that copy completes.
+    // Producer state, meaningful in the group's thread 0 only: stages with a
+    // copy in flight and the parity of the phase that copy completes.
     uint32_t pending = 0, pending_parity = 0;
     auto issue = [&](int64_t t) {
         const int s = static_cast<int>(t % S);
-        const int64_t row = cid + t * ncl;
+        const int64_t row = vid + t * nvirt;
         if (bytes == 0) {
             mbar_arrive(&bar[s]);
             return;
@@ -106,13 +148,13 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages) {
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
-    if (tid == 0)
+    if (gt == 0)
         for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
 
     uint4 wv[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
-        const int k = j * nthr + tid;
+        const int k = j * TG + gt;
         wv[j] = k < vcnt ? ld_global_16(W + static_cast<int64_t>(vbeg + k) * VEC)
                          : make_uint4(0, 0, 0, 0);
     }
@@ -123,48 +165,50 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages) {
         for (int e = 0; e < VEC; ++e) acc[j][e] = 0.f;
 
     // rstd is read two rows ahead so its latency hides behind the rows before
-    float r1 = nrows > 0 ? __ldg(a.rstd + cid) : 0.f;
-    float r2 = nrows > 1 ? __ldg(a.rstd + cid + ncl) : 0.f;
+    float r1 = nrows > 0 ? __ldg(a.rstd + vid) : 0.f;
+    float r2 = nrows > 1 ? __ldg(a.rstd + vid + nvirt) : 0.f;
     bool failed = false;
 
     for (int64_t t = 0; t < nrows; ++t) {
-        const int64_t row = cid + t * ncl;
+        const int64_t row = vid + t * nvirt;
         const int s = static_cast<int>(t % S);
         const uint32_t parity = static_cast<uint32_t>((t / S) & 1);
         const float r = r1;
         r1 = r2;
-        if (t + 2 < nrows) r2 = __ldg(a.rstd + row + 2 * ncl);
+        if (t + 2 < nrows) r2 = __ldg(a.rstd + row + 2 * nvirt);
 
         if (!failed) {
             if (mbar_wait_bounded(&bar[s], parity, a.wait_limit_ns)) {
-                if (tid == 0) pending &= ~(1u << s);
+                if (gt == 0) pending &= ~(1u << s);
             } else {
                 *fail = 1;
                 report_status(a.status, kStatusTimeout);
             }
         }
         // pass 1: dot = sum_j (dy*w)*x over this thread's slots
+        const unsigned char* xs = sx + s * unit;
+        const unsigned char* ds = sdy + s * unit;
         float dot = 0.f;
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            const int k = j * nthr + tid;
+            const int k = j * TG + gt;
             if (k >= vcnt) continue;
             float fx[VEC], fd[VEC], fw[VEC];
-            P::unpack(ld_shared_16(sx + s * unit + k * 16), fx);
-            P::unpack(ld_shared_16(sdy + s * unit + k * 16), fd);
+            P::unpack(ld_shared_16(xs + k * 16), fx);
+            P::unpack(ld_shared_16(ds + k * 16), fd);
             P::unpack(wv[j], fw);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) dot = fmaf(fd[e] * fw[e], fx[e], dot);
         }
         dot = group_allreduce<32>(dot);
         float* rslot = red + (t & 1) * 32;
-        if (lane == 0) rslot[warp] = dot;
-        __syncthreads();  // partial sums published; every thread is done with row t-1
+        if (lane == 0) rslot[gwarp] = dot;
+        group_barrier(bar_id, TG);  // sums published; the group is done with row t-1
         failed = *fail != 0;
-        float tot = lane < nw ? rslot[lane] : 0.f;
+        float tot = lane < gnw ? rslot[lane] : 0.f;
         tot = group_allreduce<32>(tot);
         // the stage of row t-1 is free now: refill it with row t-1+S
-        if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+        if (gt == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
             fence_proxy_async_shared();
             issue(t - 1 + S);
         }
@@ -180,38 +224,65 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages) {
         // pass 2: dx and the dw contribution, reading the row from shared memory again
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            const int k = j * nthr + tid;
+            const int k = j * TG + gt;
             if (k >= vcnt) continue;
             float fx[VEC], fd[VEC], fw[VEC], o[VEC];
-            P::unpack(ld_shared_16(sx + s * unit + k * 16), fx);
-            P::unpack(ld_shared_16(sdy + s * unit + k * 16), fd);
+            P::unpack(ld_shared_16(xs + k * 16), fx);
+            P::unpack(ld_shared_16(ds + k * 16), fd);
             P::unpack(wv[j], fw);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 const float xh = fx[e] * r;
-                const float g = fd[e] * fw[e];
-                o[e] = r * (g - xh * c);
+                const float gg = fd[e] * fw[e];
+                o[e] = r * (gg - xh * c);
                 acc[j][e] = fmaf(fd[e], xh, acc[j][e]);
             }
             st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack(o));
         }
     }
+    allow_dependent_launch();
 
-    // one partial row per cluster; each block writes its column slice
-    float* prow = a.partial + cid * N + static_cast<int64_t>(vbeg) * VEC;
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int k = j * nthr + tid;
-        if (k >= vcnt) continue;
-#pragma unroll
-        for (int q = 0; q < VEC / 4; ++q)
-            *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
-                make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2], acc[j][4 * q + 3]);
-    }
-    // after a failure, let copies already in flight land before exiting
-    if (tid == 0 && failed)
+    // after a failure, let copies already in flight land before going on
+    if (gt == 0 && failed)
         for (int s = 0; s < S; ++s)
-            if ((pending >> s) & 1u) mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
+            if ((pending >> s) & 1u)
+                mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
+
+    float* prow = a.partial + cid * N + static_cast<int64_t>(vbeg) * VEC;
+    if (groups == 1) {
+        // one partial row per cluster; each block writes its column slice
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * TG + gt;
+            if (k >= vcnt) continue;
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q)
+                *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
+                    make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2],
+                                acc[j][4 * q + 3]);
+        }
+    } else {
+        // add the groups' dw in group order through shared memory (the rings
+        // are idle; groups*N*4 bytes fit in the groups*2*S*unit of the rings)
+        __syncthreads();
+        float* comb = reinterpret_cast<float*>(smem);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * TG + gt;
+            if (k >= vcnt) continue;
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q)
+                *reinterpret_cast<float4*>(comb + g * N + k * VEC + 4 * q) =
+                    make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2],
+                                acc[j][4 * q + 3]);
+        }
+        __syncthreads();
+        for (int col = tid; col < N; col += blockDim.x) {
+            float sum = 0.f;
+            for (int gi = 0; gi < groups; ++gi) sum += comb[gi * N + col];
+            prow[col] = sum;
+        }
+    }
     if (csize > 1) cluster_sync_all();
 }
 
@@ -219,7 +290,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages) {
 // A unit is a tile of RT = (threads/G)*R consecutive rows, moved by one bulk
 // copy per tensor. Group g (G lanes) handles tile rows r*groups + g.
 template <typename T, int G, int V, int R>
-__global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages) {
+__global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages, int /*groups*/) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -370,6 +441,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         }
     }
 
+    allow_dependent_launch();
     if (tid == 0 && failed)
         for (int s = 0; s < S; ++s)
             if ((pending >> s) & 1u) mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
@@ -399,7 +471,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
 // Any alignment, any N. Persistent: block b owns rows b, b+P, ... and its
 // partial row, which thread t updates at columns t, t+blockDim, ... only.
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages*/) {
+__global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages*/, int /*groups*/) {
     using P = Pack<T>;
     __shared__ float red[2][32];
     const int N = a.N;
@@ -442,6 +514,7 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
 __global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ partial,
                                                       float* __restrict__ dw, int P, int N) {
     __shared__ float part[32][33];
+    wait_for_prerequisite_grid();  // partial rows complete and visible
     const int cx = threadIdx.x, q = threadIdx.y;
     const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + cx;
     float s = 0.f;
@@ -511,6 +584,7 @@ struct OccKey {
 };
 std::mutex g_occ_mu;
 std::map<OccKey, int> g_occ;
+std::set<std::pair<int, const void*>> g_optin;
 
 cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, int smem,
                            int cluster, int* out) {
@@ -523,10 +597,23 @@ cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, i
             return cudaSuccess;
         }
     }
+    // Opt the kernel into the device's largest dynamic shared memory once,
+    // so plans of different sizes for the same kernel never lower the limit.
     cudaError_t err = cudaSuccess;
-    if (smem > 48 * 1024) {
-        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (err != cudaSuccess) return err;
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        if (g_optin.insert(std::make_pair(dev.device, fn)).second) {
+            // the opt-in covers dynamic memory only: leave room for static
+            cudaFuncAttributes fa;
+            err = cudaFuncGetAttributes(&fa, fn);
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
+            if (err != cudaSuccess) {
+                g_optin.erase(std::make_pair(dev.device, fn));
+                return err;
+            }
+        }
     }
     int units = 0;
     if (cluster <= 1) {
@@ -556,14 +643,47 @@ cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, i
     return cudaSuccess;
 }
 
+
+// Tuning overrides for sweeps (read once; unset = built-in ladder). They
+// change the persistent grid, hence the order of the dw sum: results stay
+// deterministic for a fixed setting.
+struct BwdTuning {
+    int vectors = 4;        // 16-byte vectors per thread in a row group
+    int groups = 0;         // row groups per block (0 = up to 4, 512 threads)
+    int stages = 0;         // ring depth (0 = from the shared-memory budget)
+    int smem_multi = 200 * 1024;   // shared memory aimed at, several groups
+    int smem_single = 100 * 1024;  // shared memory aimed at, one group
+};
+
+int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    if (v == nullptr || *v == 0) return dflt;
+    return atoi(v);
+}
+
+const BwdTuning& tuning() {
+    static const BwdTuning t = [] {
+        BwdTuning u;
+        u.vectors = env_int("RMSNORM_BWD_VECTORS", u.vectors);
+        if (u.vectors != 1 && u.vectors != 2 && u.vectors != 4 && u.vectors != 8) u.vectors = 4;
+        u.groups = std::max(0, std::min(4, env_int("RMSNORM_BWD_GROUPS", 0)));
+        u.stages = std::max(0, std::min(8, env_int("RMSNORM_BWD_STAGES", 0)));
+        u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
+        return u;
+    }();
+    return t;
+}
+
 }  // namespace
 
 void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     *p = rmsnorm_plan_t{};
     p->cluster = 1;
+    p->row_groups = 1;
     p->rows_per_unit = 1;
     const int sz = dtype_size(dtype);
     const int64_t nvec = N / dtype_vec(dtype);
+    const BwdTuning& tu = tuning();
     GroupShape g;
     if (vector_ok && group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
@@ -580,19 +700,27 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         int c = 1;
         while (2 * cdiv(nvec, c) * 16 > kSliceBudget && c < kMaxCluster) c *= 2;
         const int64_t slots = cdiv(nvec, c);
-        int v = 1;
-        while (v * 512 < slots && v < 8) v *= 2;
-        // at least three stages of the slice must fit in shared memory
-        const int threads = round_up(static_cast<int>(cdiv(slots, v)), 32);
-        if (v * 512 >= slots && bwd_smem_bytes(3, v * threads * 16) <= kSmemMax) {
+        int v = tu.vectors;
+        while (cdiv(slots, v) > 512 && v < 8) v *= 2;
+        const int tg = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
+        int groups = 1;
+        if (c == 1) groups = tu.groups > 0 ? tu.groups : std::max(1, std::min(4, 512 / tg));
+        while (groups > 1 && groups * tg > 512) --groups;
+        const int unit = v * tg * 16;
+        const int budget = groups > 1 ? tu.smem_multi : tu.smem_single;
+        int stages = tu.stages > 0 ? tu.stages : std::max(3, std::min(6, budget / (groups * 2 * unit)));
+        while (groups > 1 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --groups;
+        while (stages > 2 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --stages;
+        if (tg <= 512 && stages >= 3 && bwd_row_smem_bytes(groups, stages, unit) <= kSmemMax) {
             p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
             p->cluster = c;
+            p->row_groups = groups;
             p->vectors_per_thread = v;
-            p->threads = threads;
-            p->threads_per_row = p->threads * c;
-            const int unit = v * p->threads * 16;
-            p->stages = std::max(3, std::min(6, kStageBudget / (2 * unit)));
-            p->smem_bytes = bwd_smem_bytes(p->stages, unit);
+            p->threads = tg * groups;
+            p->threads_per_row = tg * c;
+            p->rows_per_unit = groups;
+            p->stages = stages;
+            p->smem_bytes = bwd_row_smem_bytes(groups, stages, unit);
             return;
         }
     }
@@ -612,8 +740,9 @@ cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t
     int units = 0;
     cudaError_t err = resident_units(dev, fn, p->threads, p->smem_bytes, p->cluster, &units);
     if (err != cudaSuccess) return err;
-    int64_t work = M;  // rows, or tiles of rows for the short-row kernel
-    if (p->variant == RMSNORM_VARIANT_ROWGROUP) work = cdiv(M, p->rows_per_unit);
+    int64_t work = M;  // rows, tiles of rows, or rows per block's row groups
+    if (p->variant == RMSNORM_VARIANT_ROWGROUP || p->variant == RMSNORM_VARIANT_CTA_ROW)
+        work = cdiv(M, p->rows_per_unit);
     const int64_t n = std::min<int64_t>(units, work);
     p->partial_rows = static_cast<int>(n);
     p->grid = static_cast<int>(n * p->cluster);
@@ -640,14 +769,23 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
         cfg.numAttrs = 1;
     }
     BwdArgs args = a;
-    int stages = p.stages;
-    void* kargs[2] = {&args, &stages};
+    int stages = p.stages, groups = p.row_groups;
+    void* kargs[3] = {&args, &stages, &groups};
     cudaError_t err = cudaLaunchKernelExC(&cfg, fn, kargs);
     if (err != cudaSuccess) return err;
-    const dim3 cs_block(32, 32);
-    const dim3 cs_grid(static_cast<unsigned>(cdiv(a.N, 32)));
-    colsum_kernel<<<cs_grid, cs_block, 0, s>>>(a.partial, a.dw, p.partial_rows, a.N);
-    return cudaGetLastError();
+    // the column sum may launch early and waits on the grid above
+    // (programmatic dependent launch) instead of a full stream boundary
+    cudaLaunchConfig_t cs = {};
+    cs.gridDim = dim3(static_cast<unsigned>(cdiv(a.N, 32)));
+    cs.blockDim = dim3(32, 32);
+    cs.stream = s;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cs.attrs = pdl;
+    cs.numAttrs = 1;
+    const float* part = a.partial;
+    return cudaLaunchKernelEx(&cs, colsum_kernel, part, a.dw, p.partial_rows, a.N);
 }
 
 }  // namespace rmsn

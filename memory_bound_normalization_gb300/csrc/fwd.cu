@@ -278,6 +278,7 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     *p = rmsnorm_plan_t{};
     p->stages = 0;
     p->cluster = 1;
+    p->row_groups = 1;
     p->rows_per_unit = 1;
     const int64_t nvec = N / dtype_vec(dtype);
     GroupShape g;

@@ -128,8 +128,11 @@ def test_width_ladder(lib, N, dtype):
             assert p.rows_per_unit % (p.threads // p.threads_per_row) == 0
         elif name in ("cta_row", "cluster_row"):
             assert (name == "cluster_row") == (p.cluster > 1)
-            assert p.threads * p.vectors_per_thread * p.cluster * vec >= N
-            assert p.threads_per_row == p.threads * p.cluster
+            assert p.threads % p.row_groups == 0 and (p.threads // p.row_groups) % 32 == 0
+            tg = p.threads // p.row_groups
+            assert tg * p.vectors_per_thread * p.cluster * vec >= N
+            assert p.threads_per_row == tg * p.cluster
+            assert p.cluster == 1 or p.row_groups == 1
         else:
             # vector kernels cover every row up to 256 KiB; wider rows may
             # outgrow registers (forward) or shared memory (backward)
@@ -139,7 +142,7 @@ def test_width_ladder(lib, N, dtype):
             if name == "rowgroup":
                 unit = p.rows_per_unit * N * (16 // vec)
             else:
-                unit = p.vectors_per_thread * p.threads * 16
+                unit = p.vectors_per_thread * (p.threads // p.row_groups) * 16 * p.row_groups
             assert p.smem_bytes >= 2 * p.stages * unit
 
 

@@ -188,7 +188,10 @@ def test_workspace_entry_point():
     ws = torch.empty(need, dtype=torch.uint8, device=DEV)
     dx = torch.empty_like(x)
     dw = torch.empty(N, dtype=torch.float32, device=DEV)
-    assert pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, ws, need - 16) == \
+    # the query covers every alignment class; this call needs the vector plan's
+    vec_need = pkg.rmsnorm_plan(M, N, pkg.BF16, pkg.PASS_BWD, 0).workspace_bytes
+    assert 0 < vec_need <= need
+    assert pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, ws, vec_need - 16) == \
         pkg.ERR_INVALID_ARG
     assert pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, ws.data_ptr() + 4, need) == \
         pkg.ERR_MISALIGNED
