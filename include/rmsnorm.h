@@ -115,6 +115,37 @@ int rmsnorm_bwd_ws(const void *x, const void *w, const void *dy,
                    cudaStream_t stream);
 
 /*
+ * Size of the fixed scratch array used by rmsnorm_bwd_noalloc (16 MiB per
+ * device that loads the library, held until the process exits).
+ */
+#define RMSNORM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * rmsnorm_bwd for callers that cannot allocate device memory: code running
+ * where cudaMalloc and the stream-ordered allocator are off limits, such as
+ * under a custom allocator that owns all device memory, in a real-time loop
+ * that must not allocate after start-up, or inside a runtime that forbids
+ * allocator calls from library code. No counterpart on the pages: it is an
+ * interface variant, same kernels and same results as rmsnorm_bwd.
+ *   - Allocates nothing: the dw partial rows go to a fixed scratch array of
+ *     RMSNORM_NOALLOC_SCRATCH_BYTES inside the library (one per device).
+ *     Shapes whose partial rows need more (rmsnorm_bwd_workspace_size
+ *     predicts the need) return RMSNORM_ERR_UNSUPPORTED and launch nothing.
+ *   - The first call on each device looks up that device's scratch address
+ *     (cudaGetSymbolAddress, with the device current); make that first call
+ *     before capturing the stream into a CUDA graph.
+ *   - Every call on a device shares the one scratch array, which keeps the
+ *     last call's contents (each call rewrites every partial row it reads,
+ *     so nothing needs clearing). Calls that overlap on the GPU race on it:
+ *     order them, e.g. on one stream.
+ *   - Arguments, outputs and other errors as rmsnorm_bwd; its bounded waits
+ *     use the default one-second limit.
+ */
+int rmsnorm_bwd_noalloc(const void *x, const void *w, const void *dy,
+                        const float *rstd, void *dx, float *dw,
+                        int64_t M, int64_t N, int dtype, cudaStream_t stream);
+
+/*
  * Device-side status. Every wait inside the kernels (on a bulk copy landing
  * in shared memory) is bounded in time; a wait that runs out records
  * RMSNORM_ERR_DEVICE_TIMEOUT in a status word on the device and the kernel

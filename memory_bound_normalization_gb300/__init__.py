@@ -30,7 +30,9 @@ from ._lib import (  # noqa: F401
     check,
     library_path,
     load_library,
+    NOALLOC_SCRATCH_BYTES,
     rmsnorm_bwd,
+    rmsnorm_bwd_noalloc,
     rmsnorm_bwd_workspace_size,
     rmsnorm_bwd_ws,
     rmsnorm_fwd,

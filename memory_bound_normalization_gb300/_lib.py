@@ -44,6 +44,7 @@ EXPORTS = (
     "rmsnorm_bwd",
     "rmsnorm_bwd_workspace_size",
     "rmsnorm_bwd_ws",
+    "rmsnorm_bwd_noalloc",
     "rmsnorm_get_last_device_error",
     "rmsnorm_status_string",
     "rmsnorm_set_wait_limit_ns",
@@ -113,6 +114,7 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i, i]
         lib.rmsnorm_bwd_workspace_size.restype = sz
         lib.rmsnorm_bwd_ws.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i, vp, sz, vp]
+        lib.rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i, vp]
         lib.rmsnorm_get_last_device_error.argtypes = [vp]
         lib.rmsnorm_status_string.argtypes = [i]
         lib.rmsnorm_status_string.restype = ctypes.c_char_p
@@ -124,7 +126,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.rmsnorm_plan.argtypes = [i64, i64, i, i, i, ctypes.POINTER(Plan)]
         lib.rmsnorm_version.argtypes = []
         lib.rmsnorm_version.restype = ctypes.c_char_p
-        for name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_ws", "rmsnorm_get_last_device_error",
+        for name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_ws", "rmsnorm_bwd_noalloc",
+                     "rmsnorm_get_last_device_error",
                      "rmsnorm_probe", "rmsnorm_plan"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -167,6 +170,16 @@ def rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M: int, N: int, dtype: int, workspace
     return load_library().rmsnorm_bwd_ws(_ptr(x), _ptr(w), _ptr(dy), _ptr(rstd), _ptr(dx),
                                          _ptr(dw), M, N, dtype, _ptr(workspace), workspace_bytes,
                                          _stream(stream))
+
+
+def rmsnorm_bwd_noalloc(x, w, dy, rstd, dx, dw, M: int, N: int, dtype: int, stream=None) -> int:
+    """rmsnorm_bwd without any device allocation (fixed in-library scratch),
+    for callers that cannot allocate; see include/rmsnorm.h."""
+    return load_library().rmsnorm_bwd_noalloc(_ptr(x), _ptr(w), _ptr(dy), _ptr(rstd), _ptr(dx),
+                                              _ptr(dw), M, N, dtype, _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def rmsnorm_get_last_device_error(stream=None) -> int:

@@ -22,7 +22,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "librmsnorm.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "probe.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "probe.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

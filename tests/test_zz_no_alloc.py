@@ -1,0 +1,84 @@
+"""rmsnorm_bwd_noalloc: the backward for callers that cannot allocate device
+memory (a custom allocator owns all of it, a real-time loop may not allocate
+after start-up, or a host runtime forbids allocator calls from libraries).
+
+It is called through the C ABI and must give what rmsnorm_bwd gives, within
+the parity tolerances of the other tests (and in fact bit for bit, since the
+same kernels run with the same plan), on two calls in a row: the second call
+reuses the scratch array the first one left behind. A shape whose partial
+rows do not fit in the fixed scratch is refused before anything runs.
+
+Kept in a file of its own that pytest collects last; it runs the same alone
+in a fresh process or after the rest of the suite.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from parity_util import check_dw, check_rows
+
+pytestmark = pytest.mark.gpu
+
+pkg = pytest.importorskip("memory_bound_normalization_gb300")
+from memory_bound_normalization_gb300 import synth  # noqa: E402
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    torch.cuda.set_device(0)
+    pkg.load_library(build_if_missing=True)
+    yield
+
+
+CASES = [(16384, 4096, torch.bfloat16), (4096, 128, torch.bfloat16), (64, 65536, torch.bfloat16),
+         (300, 2880, torch.float32), (50, 4104, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("M,N,dtype", CASES, ids=[f"{m}x{n}-{str(d)[6:]}" for m, n, d in CASES])
+def test_matches_allocating_backward_twice(M, N, dtype):
+    wl = synth.Workload(f"noalloc{M}x{N}", M, N, dtype, 1e-6, 51, 52, 53)
+    inp = synth.make_inputs(wl, device=DEV)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    code = pkg.dtype_code(dtype)
+    y, rstd = pkg.forward(x, w, wl.eps)
+    dx_ref, dw_ref = pkg.backward(x, w, dy, rstd)
+    for call in range(2):
+        dx = torch.full_like(x, float("nan"))
+        dw = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+        st = pkg.rmsnorm_bwd_noalloc(x, w, dy, rstd, dx, dw, M, N, code)
+        assert st == pkg.OK, pkg.rmsnorm_status_string(st)
+        assert pkg.rmsnorm_get_last_device_error() == pkg.OK
+        check_rows(dx, dx_ref.float().cpu().numpy(), dtype, f"dx (call {call})")
+        check_dw(dw, dw_ref.cpu().numpy(), f"dw (call {call})")
+        assert torch.equal(dx, dx_ref) and torch.equal(dw, dw_ref), f"call {call} differs in bits"
+
+
+def test_refuses_shapes_beyond_the_scratch():
+    # a row too wide for the vector kernels takes the scalar backward, whose
+    # partial rows (one per resident block, 512 KiB each) exceed 16 MiB
+    M, N = 200, 131072
+    need = pkg.rmsnorm_bwd_workspace_size(M, N, pkg.F32, 0)
+    assert need > pkg.NOALLOC_SCRATCH_BYTES
+    x = torch.zeros(M, N, dtype=torch.float32, device=DEV)
+    w = torch.ones(N, dtype=torch.float32, device=DEV)
+    rstd = torch.ones(M, dtype=torch.float32, device=DEV)
+    dx = torch.empty_like(x)
+    dw = torch.full((N,), 3.0, device=DEV)
+    st = pkg.rmsnorm_bwd_noalloc(x, w, x, rstd, dx, dw, M, N, pkg.F32)
+    assert st == pkg.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(dw == 3.0), "a refused call must not launch anything"
+
+
+def test_empty_and_invalid():
+    dw = torch.full((8,), 5.0, device=DEV)
+    assert pkg.rmsnorm_bwd_noalloc(0, 0, 0, 0, 0, dw, 0, 8, pkg.F32) == pkg.OK
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0)
+    assert pkg.rmsnorm_bwd_noalloc(0, 0, 0, 0, 0, dw, 4, 0, pkg.F32) == pkg.ERR_INVALID_ARG
+    assert pkg.rmsnorm_bwd_noalloc(None, dw, dw, dw, dw, dw, 1, 8, pkg.F32) == pkg.ERR_INVALID_ARG
