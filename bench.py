@@ -428,7 +428,7 @@ def run_ours(args):
     value = world * (fwd_bytes + bwd_bytes) / (step_ms * 1e-3) / 1e9
     bwd_gbs = bwd_bytes / (bwd_mean * 1e-3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_mean * 1e-3) / 1e9
-    traffic = read_profiled_traffic("rmsnorm_bwd", wl.name, libbuild.source_hash())
+    traffic = read_profiled_traffic("rmsnorm_bwd", wl.name, libbuild.kernel_source_hash())
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -451,10 +451,12 @@ def run_ours(args):
                   f"a {2 * l2 >> 20} MiB write then a {2 * l2 >> 20} MiB read (cold, clean L2)",
             "logical_bytes": {"fwd": fwd_bytes, "bwd": bwd_bytes},
         },
-        "fwd": {"ms": round(fwd_mean, 5), "gbs": round(fwd_gbs, 1),
+        "fwd": {"ms": round(fwd_mean, 5), "median_ms": round(statistics.median(fwd_ms), 5),
+                "gbs": round(fwd_gbs, 1),
                 "frac_of_peak": round(fwd_gbs / peak, 4),
                 "frac_of_probe": round(fwd_gbs / probes_open["best"], 4), "plan": plan_f},
-        "bwd": {"ms": round(bwd_mean, 5), "gbs": round(bwd_gbs, 1),
+        "bwd": {"ms": round(bwd_mean, 5), "median_ms": round(statistics.median(bwd_ms), 5),
+                "gbs": round(bwd_gbs, 1),
                 "frac_of_peak": round(bwd_gbs / peak, 4),
                 "frac_of_probe": round(bwd_gbs / probes_open["best"], 4), "plan": plan_b,
                 "workspace_bytes_overhead": 2 * plan_b["workspace_bytes"]},
@@ -478,6 +480,7 @@ def run_ours(args):
         "gpu_launches": 3 * K,
         "validation": errs,
         "library": {"path": pkg.library_path(), "source_hash": libbuild.source_hash(),
+                    "bwd_kernel_hash": libbuild.kernel_source_hash(),
                     "version": pkg.rmsnorm_version()},
     }
     if rank == 0 and not args.no_cpu_baseline:

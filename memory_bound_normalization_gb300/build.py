@@ -55,6 +55,20 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+BWD_KERNEL_FILES = ("bwd.cu", "common.cuh", "kernels.h")
+
+
+def kernel_source_hash(names=BWD_KERNEL_FILES) -> str:
+    """sha256 over the csrc files that define a kernel family (by default the
+    backward), so a profile can be matched to the kernel code it measured."""
+    h = hashlib.sha256()
+    for n in names:
+        h.update(n.encode())
+        with open(os.path.join(CSRC, n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def is_stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True

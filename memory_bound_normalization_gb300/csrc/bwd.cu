@@ -158,11 +158,12 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         wv[j] = k < vcnt ? ld_global_16(W + static_cast<int64_t>(vbeg + k) * VEC)
                          : make_uint4(0, 0, 0, 0);
     }
-    float acc[V][VEC];
+    constexpr int PR = P::PAIRS;
+    float2 acc[V][PR];
 #pragma unroll
     for (int j = 0; j < V; ++j)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[j][e] = 0.f;
+        for (int e = 0; e < PR; ++e) acc[j][e] = make_float2(0.f, 0.f);
 
     // rstd is read two rows ahead so its latency hides behind the rows before
     float r1 = nrows > 0 ? __ldg(a.rstd + vid) : 0.f;
@@ -188,19 +189,19 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         // pass 1: dot = sum_j (dy*w)*x over this thread's slots
         const unsigned char* xs = sx + s * unit;
         const unsigned char* ds = sdy + s * unit;
-        float dot = 0.f;
+        float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
-            float fx[VEC], fd[VEC], fw[VEC];
-            P::unpack(ld_shared_16(xs + k * 16), fx);
-            P::unpack(ld_shared_16(ds + k * 16), fd);
-            P::unpack(wv[j], fw);
+            float2 fx[PR], fd[PR], fw[PR];
+            P::unpack2(ld_shared_16(xs + k * 16), fx);
+            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            P::unpack2(wv[j], fw);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) dot = fmaf(fd[e] * fw[e], fx[e], dot);
+            for (int e = 0; e < PR; ++e) dot2 = __ffma2_rn(__fmul2_rn(fd[e], fw[e]), fx[e], dot2);
         }
-        dot = group_allreduce<32>(dot);
+        float dot = group_allreduce<32>(dot2.x + dot2.y);
         float* rslot = red + (t & 1) * 32;
         if (lane == 0) rslot[gwarp] = dot;
         group_barrier(bar_id, TG);  // sums published; the group is done with row t-1
@@ -220,24 +221,26 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         }
         // mean_j(g * xhat) = rstd * mean_j(g * x)
         const float c = r * (tot / static_cast<float>(N));
+        const float2 r2 = f2_splat(r), nc2 = f2_splat(-c);
         T* dxr = DX + row * N;
-        // pass 2: dx and the dw contribution, reading the row from shared memory again
+        // pass 2: dx = r*(g - xhat*c) and dw += dy*xhat, re-reading the row
+        // from shared memory
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
-            float fx[VEC], fd[VEC], fw[VEC], o[VEC];
-            P::unpack(ld_shared_16(xs + k * 16), fx);
-            P::unpack(ld_shared_16(ds + k * 16), fd);
-            P::unpack(wv[j], fw);
+            float2 fx[PR], fd[PR], fw[PR], o[PR];
+            P::unpack2(ld_shared_16(xs + k * 16), fx);
+            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            P::unpack2(wv[j], fw);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float xh = fx[e] * r;
-                const float gg = fd[e] * fw[e];
-                o[e] = r * (gg - xh * c);
-                acc[j][e] = fmaf(fd[e], xh, acc[j][e]);
+            for (int e = 0; e < PR; ++e) {
+                const float2 xh = __fmul2_rn(fx[e], r2);
+                const float2 gg = __fmul2_rn(fd[e], fw[e]);
+                o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
+                acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
             }
-            st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack(o));
+            st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(o));
         }
     }
     allow_dependent_launch();
@@ -256,10 +259,10 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
 #pragma unroll
-            for (int q = 0; q < VEC / 4; ++q)
+            for (int q = 0; q < PR / 2; ++q)
                 *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
-                    make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2],
-                                acc[j][4 * q + 3]);
+                    make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
+                                acc[j][2 * q + 1].y);
         }
     } else {
         // add the groups' dw in group order through shared memory (the rings
@@ -271,10 +274,10 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
 #pragma unroll
-            for (int q = 0; q < VEC / 4; ++q)
+            for (int q = 0; q < PR / 2; ++q)
                 *reinterpret_cast<float4*>(comb + g * N + k * VEC + 4 * q) =
-                    make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2],
-                                acc[j][4 * q + 3]);
+                    make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
+                                acc[j][2 * q + 1].y);
         }
         __syncthreads();
         for (int col = tid; col < N; col += blockDim.x) {
@@ -346,11 +349,12 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         const int k = j * G + lane;
         wv[j] = k < nvec ? ld_global_16(W + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
     }
-    float acc[V][VEC];
+    constexpr int PR = P::PAIRS;
+    float2 acc[V][PR];
 #pragma unroll
     for (int j = 0; j < V; ++j)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[j][e] = 0.f;
+        for (int e = 0; e < PR; ++e) acc[j][e] = make_float2(0.f, 0.f);
 
     float rnext[R];
     auto load_rstd = [&](int64_t t, float (&dst)[R]) {
@@ -387,19 +391,20 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         for (int r = 0; r < R; ++r) {
             const int lr = r * groups + group;
             const bool row_ok = tile * RT + lr < a.M;
-            dot[r] = 0.f;
+            float2 dot2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int k = j * G + lane;
                 if (!row_ok || k >= nvec) continue;
                 const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
-                float fx[VEC], fd[VEC], fw[VEC];
-                P::unpack(ld_shared_16(sx + s * unit + off), fx);
-                P::unpack(ld_shared_16(sdy + s * unit + off), fd);
-                P::unpack(wv[j], fw);
+                float2 fx[PR], fd[PR], fw[PR];
+                P::unpack2(ld_shared_16(sx + s * unit + off), fx);
+                P::unpack2(ld_shared_16(sdy + s * unit + off), fd);
+                P::unpack2(wv[j], fw);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) dot[r] = fmaf(fd[e] * fw[e], fx[e], dot[r]);
+                for (int e = 0; e < PR; ++e) dot2 = __ffma2_rn(__fmul2_rn(fd[e], fw[e]), fx[e], dot2);
             }
+            dot[r] = dot2.x + dot2.y;
         }
         __syncthreads();  // every thread is done with tile t-1
         failed = *fail != 0;
@@ -420,23 +425,24 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
             if (row >= a.M) continue;
             const float rs = rcur[r];
             const float c = rs * (dot[r] / static_cast<float>(N));
+            const float2 r2 = f2_splat(rs), nc2 = f2_splat(-c);
 #pragma unroll
             for (int j = 0; j < V; ++j) {
                 const int k = j * G + lane;
                 if (k >= nvec) continue;
                 const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
-                float fx[VEC], fd[VEC], fw[VEC], o[VEC];
-                P::unpack(ld_shared_16(sx + s * unit + off), fx);
-                P::unpack(ld_shared_16(sdy + s * unit + off), fd);
-                P::unpack(wv[j], fw);
+                float2 fx[PR], fd[PR], fw[PR], o[PR];
+                P::unpack2(ld_shared_16(sx + s * unit + off), fx);
+                P::unpack2(ld_shared_16(sdy + s * unit + off), fd);
+                P::unpack2(wv[j], fw);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xh = fx[e] * rs;
-                    const float g = fd[e] * fw[e];
-                    o[e] = rs * (g - xh * c);
-                    acc[j][e] = fmaf(fd[e], xh, acc[j][e]);
+                for (int e = 0; e < PR; ++e) {
+                    const float2 xh = __fmul2_rn(fx[e], r2);
+                    const float2 g = __fmul2_rn(fd[e], fw[e]);
+                    o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, g));
+                    acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
                 }
-                st_global_16(DX + row * N + static_cast<int64_t>(k) * VEC, P::pack(o));
+                st_global_16(DX + row * N + static_cast<int64_t>(k) * VEC, P::pack2(o));
             }
         }
     }
@@ -454,9 +460,10 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         const int k = j * G + lane;
         if (k >= nvec) continue;
 #pragma unroll
-        for (int q = 0; q < VEC / 4; ++q)
+        for (int q = 0; q < PR / 2; ++q)
             *reinterpret_cast<float4*>(comb + group * N + k * VEC + 4 * q) =
-                make_float4(acc[j][4 * q], acc[j][4 * q + 1], acc[j][4 * q + 2], acc[j][4 * q + 3]);
+                make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
+                            acc[j][2 * q + 1].y);
     }
     __syncthreads();
     float* prow = a.partial + b * N;

@@ -18,9 +18,21 @@ constexpr int kStatusTimeout = 6;
 template <typename T>
 struct Pack;
 
+// Pairs: a 16-byte vector seen as PAIRS float2 values, element 2e in .x and
+// 2e+1 in .y, so that the element math runs on packed fp32x2 instructions
+// (__ffma2_rn / __fmul2_rn: two IEEE round-to-nearest operations each).
 template <>
 struct Pack<float> {
     static constexpr int VEC = 4;
+    static constexpr int PAIRS = 2;
+    __device__ __forceinline__ static void unpack2(const uint4& v, float2 (&f)[PAIRS]) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2 (&f)[PAIRS]) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y),
+                          __float_as_uint(f[1].x), __float_as_uint(f[1].y));
+    }
     __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[VEC]) {
         f[0] = __uint_as_float(v.x);
         f[1] = __uint_as_float(v.y);
@@ -38,6 +50,25 @@ struct Pack<float> {
 template <>
 struct Pack<__nv_bfloat16> {
     static constexpr int VEC = 8;
+    static constexpr int PAIRS = 4;
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    // one bf16x2 word -> one float2 (low half is the lower-addressed element)
+    __device__ __forceinline__ static float2 word_to_f2(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static void unpack2(const uint4& v, float2 (&f)[PAIRS]) {
+        f[0] = word_to_f2(v.x);
+        f[1] = word_to_f2(v.y);
+        f[2] = word_to_f2(v.z);
+        f[3] = word_to_f2(v.w);
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2 (&f)[PAIRS]) {
+        return make_uint4(pack2(f[0].x, f[0].y), pack2(f[1].x, f[1].y), pack2(f[2].x, f[2].y),
+                          pack2(f[3].x, f[3].y));
+    }
     // bf16 is the high half of an fp32 bit pattern, so widening is a shift.
     __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[VEC]) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -46,10 +77,6 @@ struct Pack<__nv_bfloat16> {
             f[2 * k] = __uint_as_float(w[k] << 16);
             f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
         }
-    }
-    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-        return *reinterpret_cast<uint32_t*>(&h);
     }
     __device__ __forceinline__ static uint4 pack(const float (&f)[VEC]) {
         return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
@@ -62,6 +89,8 @@ struct Pack<__nv_bfloat16> {
         return __float2bfloat16_rn(v);
     }
 };
+
+__device__ __forceinline__ float2 f2_splat(float v) { return make_float2(v, v); }
 
 // ------------------------------------------------------------ global memory
 __device__ __forceinline__ uint4 ld_global_16(const void* p) {

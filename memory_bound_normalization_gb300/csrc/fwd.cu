@@ -59,18 +59,19 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
         wv[j] = k < nvec ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
     }
 
+    constexpr int PR = P::PAIRS;
     float ss[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        float acc = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-            float f[VEC];
-            P::unpack(xv[r][j], f);
+            float2 f[PR];
+            P::unpack2(xv[r][j], f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc = fmaf(f[e], f[e], acc);
+            for (int e = 0; e < PR; ++e) acc = __ffma2_rn(f[e], f[e], acc);
         }
-        ss[r] = acc;
+        ss[r] = acc.x + acc.y;
     }
 #pragma unroll
     for (int off = G / 2; off >= 1; off /= 2)
@@ -82,16 +83,17 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
         const int64_t row = tile + static_cast<int64_t>(r) * groups + group;
         if (row >= M) continue;
         const float rs = rsqrtf(ss[r] / static_cast<float>(N) + eps);
+        const float2 rs2 = f2_splat(rs);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = j * G + lane;
             if (k >= nvec) continue;
-            float fx[VEC], fw[VEC], fy[VEC];
-            P::unpack(xv[r][j], fx);
-            P::unpack(wv[j], fw);
+            float2 fx[PR], fw[PR], fy[PR];
+            P::unpack2(xv[r][j], fx);
+            P::unpack2(wv[j], fw);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) fy[e] = fx[e] * rs * fw[e];
-            st_global_16(y + row * N + static_cast<int64_t>(k) * VEC, P::pack(fy));
+            for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
+            st_global_16(y + row * N + static_cast<int64_t>(k) * VEC, P::pack2(fy));
         }
         if (lane == 0) rstd[row] = rs;
     }
@@ -112,8 +114,8 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
     __shared__ float cluster_part;
 
     const uint32_t csize = cluster_size();
-    const uint32_t crank = cluster_rank();
-    const int64_t row = cluster_index();
+    const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
+    const int64_t row = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
     const int nthr = blockDim.x;
     const int nvec = N / VEC;
     const int base = static_cast<int>(crank) * V * nthr;
@@ -127,16 +129,17 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
         xv[j] = ok ? ld_global_16_stream(xr + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
         wv[j] = ok ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
     }
-    float ss = 0.f;
+    constexpr int PR = P::PAIRS;
+    float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < V; ++j) {
-        float f[VEC];
-        P::unpack(xv[j], f);
+        float2 f[PR];
+        P::unpack2(xv[j], f);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) ss = fmaf(f[e], f[e], ss);
+        for (int e = 0; e < PR; ++e) ss2 = __ffma2_rn(f[e], f[e], ss2);
     }
     // block: butterfly per warp, then one shared-memory hop
-    ss = group_allreduce<32>(ss);
+    float ss = group_allreduce<32>(ss2.x + ss2.y);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) red[warp] = ss;
     __syncthreads();
@@ -151,17 +154,18 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
         for (uint32_t q = 0; q < csize; ++q) total += ld_cluster_f32(&cluster_part, q);
     }
     const float rs = rsqrtf(total / static_cast<float>(N) + eps);
+    const float2 rs2 = f2_splat(rs);
     T* yr = y + row * N;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int k = base + j * nthr + threadIdx.x;
         if (k >= nvec) continue;
-        float fx[VEC], fw[VEC], fy[VEC];
-        P::unpack(xv[j], fx);
-        P::unpack(wv[j], fw);
+        float2 fx[PR], fw[PR], fy[PR];
+        P::unpack2(xv[j], fx);
+        P::unpack2(wv[j], fw);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) fy[e] = fx[e] * rs * fw[e];
-        st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack(fy));
+        for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
+        st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
     }
     if (crank == 0 && threadIdx.x == 0) rstd[row] = rs;
     // a block's shared memory must outlive the other blocks' reads of it
