@@ -199,7 +199,9 @@ typedef enum {
     RMSNORM_VARIANT_ROWGROUP = 1,  /* short rows: a sub-warp or warp per row */
     RMSNORM_VARIANT_CTA_ROW = 2,   /* one thread block per row */
     RMSNORM_VARIANT_CLUSTER_ROW = 3, /* a thread-block cluster per row */
-    RMSNORM_VARIANT_SCALAR = 4     /* unaligned or ragged rows */
+    RMSNORM_VARIANT_SCALAR = 4,    /* unaligned or ragged rows */
+    RMSNORM_VARIANT_TWO_PASS = 5   /* wide rows (forward): a block per row,
+                                      two passes, the second served by L2 */
 } rmsnorm_variant_t;
 
 typedef enum {
@@ -212,7 +214,8 @@ typedef struct {
     int threads;            /* threads per block */
     int vectors_per_thread; /* 16-byte vectors of a row each thread owns */
     int threads_per_row;    /* lanes sharing one row (ROWGROUP), else threads */
-    int rows_per_unit;      /* rows per block pass (row-group tile, or row groups) */
+    int rows_per_unit;      /* rows per block pass (row-group tile, or row
+                               groups); TWO_PASS: blocks per SM */
     int cluster;            /* blocks per row (1 unless CLUSTER_ROW) */
     int row_groups;         /* independent row groups per block (backward
                                CTA_ROW: each group of threads/row_groups

@@ -35,7 +35,8 @@ PROBE_COPY = 0
 PROBE_WRITE = 1
 PROBE_2R1W = 2
 
-VARIANTS = {0: "none", 1: "rowgroup", 2: "cta_row", 3: "cluster_row", 4: "scalar"}
+VARIANTS = {0: "none", 1: "rowgroup", 2: "cta_row", 3: "cluster_row", 4: "scalar",
+            5: "two_pass"}
 
 # Exported symbols, in header order (tests check the library against this
 # list and the header against the library).

@@ -147,7 +147,8 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan));
     if (st != RMSNORM_OK) return st;
     if (static_cast<int64_t>(plan.grid) <= 0 ||
-        (plan.variant != RMSNORM_VARIANT_SCALAR &&
+        ((plan.variant == RMSNORM_VARIANT_ROWGROUP || plan.variant == RMSNORM_VARIANT_CTA_ROW ||
+          plan.variant == RMSNORM_VARIANT_CLUSTER_ROW) &&
          cdiv(M, plan.variant == RMSNORM_VARIANT_ROWGROUP ? plan.rows_per_unit : 1) * plan.cluster >
              INT32_MAX))
         return RMSNORM_ERR_UNSUPPORTED;

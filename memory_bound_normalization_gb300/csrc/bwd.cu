@@ -37,8 +37,8 @@
 namespace rmsn {
 namespace {
 
-constexpr int kStageBudget = 96 * 1024;   // shared memory aimed at per block
-constexpr int kSliceBudget = 48 * 1024;   // x+dy bytes of one row slice per stage
+constexpr int kStageBudget = 48 * 1024;   // ring bytes aimed at per short-row block
+constexpr int kSliceBudget = 64 * 1024;   // x+dy bytes of one row slice per stage
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory a block may opt into
 
 // Shared memory of the short-row kernel: [S][unit] x | [S][unit] dy |
@@ -47,16 +47,23 @@ __host__ __device__ inline int bwd_smem_bytes(int stages, int unit) {
     return 2 * stages * unit + stages * 8 + 64 * 4 + 2 * 4 + 16;
 }
 
-// Shared memory of the row kernel with `groups` row groups: per group
-// [S][unit] x | [S][unit] dy | mbarrier[S] | reduction slots [2][32] |
-// failure flag, padded to a multiple of 128 bytes so that every group's ring
-// starts 16-byte aligned (bulk copies and 16-byte shared loads need it); then
-// two cluster slots.
+// Shared memory of the grouped row kernel, per group: [S][unit] x |
+// [S][unit] dy | mbarrier[S] | reduction slots [2][32] | failure flag, padded
+// to a multiple of 128 bytes so that every group's ring starts 16-byte aligned
+// (bulk copies and 16-byte shared loads need it).
 __host__ __device__ inline int bwd_row_group_stride(int stages, int unit) {
     return (2 * stages * unit + stages * 8 + 64 * 4 + 16 + 127) / 128 * 128;
 }
+
+// Shared memory of the wide-row kernel: [S][unit] x | [S][unit] dy |
+// mbarrier[S] (copies) | mbarrier[4] (cluster exchange) | reduction slots
+// [2][32] | exchange slots [4][kMaxClusterSize] | failure flag.
+constexpr int kMaxClusterSize = 16;
+__host__ __device__ inline int bwd_wide_smem_bytes(int stages, int unit) {
+    return 2 * stages * unit + stages * 8 + 4 * 8 + 64 * 4 + 4 * kMaxClusterSize * 4 + 16;
+}
 __host__ __device__ inline int bwd_row_smem_bytes(int groups, int stages, int unit) {
-    return groups * bwd_row_group_stride(stages, unit) + 16;
+    return groups * bwd_row_group_stride(stages, unit);
 }
 
 __device__ __forceinline__ void group_barrier(int id, int threads) {
@@ -71,15 +78,12 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// ---------------------------------------- row groups, blocks or clusters per row
+// ------------------------------------------------------ row groups per block
 // A block holds `groups` independent row groups of TG = blockDim.x / groups
 // threads. Group g of block b works as a virtual block v = b*groups + g of
 // P*groups: it owns rows v, v + P*groups, ..., has its own bulk-copy ring and
 // named barrier, and keeps its dw contribution in registers. At the end the
 // groups' dw are added in group order, so every block writes one partial row.
-// With a cluster launch (groups == 1) the cluster owns the row and block rank
-// q of the cluster holds vector slots [q*V*TG, (q+1)*V*TG) of it; the row sum
-// is exchanged through distributed shared memory.
 template <typename T, int V>
 __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int groups) {
     using P = Pack<T>;
@@ -90,17 +94,15 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     const int TG = blockDim.x / groups;
     const int g = tid / TG, gt = tid % TG;
     const int gwarp = gt >> 5, lane = tid & 31, gnw = TG >> 5;
-    const uint32_t csize = cluster_size();
-    const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
-    const int64_t cid = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
-    const int64_t ncl = csize > 1 ? static_cast<int64_t>(cluster_count()) : gridDim.x;
+    const int64_t cid = blockIdx.x;
+    const int64_t ncl = gridDim.x;
     const int64_t vid = cid * groups + g;       // virtual block of this group
     const int64_t nvirt = ncl * groups;
     const int N = a.N;
     const int nvec = N / VEC;
     const int slots = V * TG;
-    const int vbeg = static_cast<int>(crank) * slots;
-    const int vcnt = max(0, min(slots, nvec - vbeg));
+    const int vbeg = 0;
+    const int vcnt = min(slots, nvec);
     const uint32_t bytes = static_cast<uint32_t>(vcnt) * 16u;
     const int S = stages;
     const int unit = slots * 16;
@@ -112,7 +114,6 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + 2 * S * unit);
     float* red = reinterpret_cast<float*>(bar + S);
     volatile int* fail = reinterpret_cast<volatile int*>(red + 64);
-    float* cpart = reinterpret_cast<float*>(smem + groups * gstride);
 
     const T* X = static_cast<const T*>(a.x);
     const T* DY = static_cast<const T*>(a.dy);
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     // rstd is read two rows ahead so its latency hides behind the rows before
     float r1 = nrows > 0 ? __ldg(a.rstd + vid) : 0.f;
     float r2 = nrows > 1 ? __ldg(a.rstd + vid + nvirt) : 0.f;
-    bool failed = false;
+    bool failed = false;  // a copy wait ran out in this group
 
     for (int64_t t = 0; t < nrows; ++t) {
         const int64_t row = vid + t * nvirt;
@@ -213,12 +214,6 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             fence_proxy_async_shared();
             issue(t - 1 + S);
         }
-        if (csize > 1) {
-            if (tid == 0) cpart[t & 1] = tot;
-            cluster_sync_all();
-            tot = 0.f;
-            for (uint32_t q = 0; q < csize; ++q) tot += ld_cluster_f32(&cpart[t & 1], q);
-        }
         // mean_j(g * xhat) = rstd * mean_j(g * x)
         const float c = r * (tot / static_cast<float>(N));
         const float2 r2 = f2_splat(r), nc2 = f2_splat(-c);
@@ -251,6 +246,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             if ((pending >> s) & 1u)
                 mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
 
+    // one partial row per cluster (or block); each block writes its column slice
     float* prow = a.partial + cid * N + static_cast<int64_t>(vbeg) * VEC;
     if (groups == 1) {
         // one partial row per cluster; each block writes its column slice
@@ -265,27 +261,256 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
                                 acc[j][2 * q + 1].y);
         }
     } else {
-        // add the groups' dw in group order through shared memory (the rings
-        // are idle; groups*N*4 bytes fit in the groups*2*S*unit of the rings)
+        // add the groups' dw in group order through shared memory; the rings
+        // are idle and the slice's groups*W*4 bytes (W = this block's
+        // columns) fit in the groups*2*S*unit bytes of the rings
         __syncthreads();
         float* comb = reinterpret_cast<float*>(smem);
+        const int W = vcnt * VEC;
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
 #pragma unroll
             for (int q = 0; q < PR / 2; ++q)
-                *reinterpret_cast<float4*>(comb + g * N + k * VEC + 4 * q) =
+                *reinterpret_cast<float4*>(comb + g * W + k * VEC + 4 * q) =
                     make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
                                 acc[j][2 * q + 1].y);
         }
         __syncthreads();
-        for (int col = tid; col < N; col += blockDim.x) {
+        for (int col = tid; col < W; col += blockDim.x) {
             float sum = 0.f;
-            for (int gi = 0; gi < groups; ++gi) sum += comb[gi * N + col];
+            for (int gi = 0; gi < groups; ++gi) sum += comb[gi * W + col];
             prow[col] = sum;
         }
     }
+}
+
+// ----------------------------------------------- wide rows, software-pipelined
+// One row pipeline per block. A row too wide for one block is split over a
+// cluster of C blocks (block rank q holds vector slots [q*V*T, (q+1)*V*T));
+// otherwise C = 1. Each row goes through: wait for its bulk copy, pass 1 (the
+// block's part of sum_j dy*w*x), block reduction, exchange of the C block
+// sums through distributed shared memory, pass 2 (dx and the dw partial).
+// The loop does pass 1 and the reduction of row t+1 before pass 2 of row t,
+// so the exchange of row t is in flight while row t+1 is read.
+//
+// Exchange: the block's sum of row t goes to slot [t&3][q] of every block of
+// the cluster (itself included), followed by a remote arrive (release) on
+// that block's barrier [t&3]; the receiver waits (acquire) and adds the C
+// slots in rank order, the same bits in every block. Four slots suffice: a
+// peer sends row r+1 only after receiving row r-1, which needs this block's
+// send of row r-1, made before this block reads the slots of row r-2; so a
+// writer is at most three rows ahead of a reader.
+template <typename T, int V>
+__global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, int /*groups*/) {
+    using P = Pack<T>;
+    constexpr int VEC = P::VEC;
+    constexpr int PR = P::PAIRS;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int nthr = blockDim.x, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    const uint32_t csize = cluster_size();
+    const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
+    const int64_t cid = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
+    const int64_t ncl = csize > 1 ? static_cast<int64_t>(cluster_count()) : gridDim.x;
+    const int N = a.N;
+    const int nvec = N / VEC;
+    const int slots = V * nthr;
+    const int vbeg = static_cast<int>(crank) * slots;
+    const int vcnt = max(0, min(slots, nvec - vbeg));
+    const uint32_t bytes = static_cast<uint32_t>(vcnt) * 16u;
+    const int S = stages;
+    const int unit = slots * 16;
+
+    unsigned char* sx = smem;
+    unsigned char* sdy = smem + S * unit;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * S * unit);
+    uint64_t* xbar = bar + S;                          // [4]
+    float* red = reinterpret_cast<float*>(xbar + 4);  // [2][32]
+    float* xslot = red + 64;                           // [4][kMaxClusterSize]
+    volatile int* fail = reinterpret_cast<volatile int*>(xslot + 4 * kMaxClusterSize);
+
+    const T* X = static_cast<const T*>(a.x);
+    const T* DY = static_cast<const T*>(a.dy);
+    const T* W = static_cast<const T*>(a.w);
+    T* DX = static_cast<T*>(a.dx);
+
+    // rows of this cluster: cid, cid+ncl, ...
+    const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&xbar[b], csize);
+        *fail = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    // every block's barriers must exist before any peer arrives on them
+    if (csize > 1) cluster_sync_all();
+
+    uint32_t pending = 0, pending_parity = 0;  // producer state (thread 0)
+    auto issue = [&](int64_t t) {
+        const int s = static_cast<int>(t % S);
+        const int64_t row = cid + t * ncl;
+        if (bytes == 0) {
+            mbar_arrive(&bar[s]);
+            return;
+        }
+        mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+        if (row == a.drop_unit) return;  // failure injection: this wait runs out
+        const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
+        bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
+        bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
+        pending |= 1u << s;
+        pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
+    };
+    if (tid == 0)
+        for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
+
+    uint4 wv[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * nthr + tid;
+        wv[j] = k < vcnt ? ld_global_16(W + static_cast<int64_t>(vbeg + k) * VEC)
+                         : make_uint4(0, 0, 0, 0);
+    }
+    float2 acc[V][PR];
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+#pragma unroll
+        for (int e = 0; e < PR; ++e) acc[j][e] = make_float2(0.f, 0.f);
+
+    bool failed = false;   // a copy wait ran out in this block
+    bool xfailed = false;  // an exchange wait ran out in this thread
+
+    // pass 1 of row t: wait for its copy, partial dot, warp sums to red[t&1]
+    auto pass1 = [&](int64_t t) {
+        const int s = static_cast<int>(t % S);
+        if (!failed) {
+            if (mbar_wait_bounded(&bar[s], static_cast<uint32_t>((t / S) & 1), a.wait_limit_ns)) {
+                if (tid == 0) pending &= ~(1u << s);
+            } else {
+                *fail = 1;
+                report_status(a.status, kStatusTimeout);
+            }
+        }
+        const unsigned char* xs = sx + s * unit;
+        const unsigned char* ds = sdy + s * unit;
+        float2 dot2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * nthr + tid;
+            if (k >= vcnt) continue;
+            float2 fx[PR], fd[PR], fw[PR];
+            P::unpack2(ld_shared_16(xs + k * 16), fx);
+            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            P::unpack2(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < PR; ++e) dot2 = __ffma2_rn(__fmul2_rn(fd[e], fw[e]), fx[e], dot2);
+        }
+        const float dot = group_allreduce<32>(dot2.x + dot2.y);
+        if (lane == 0) red[(t & 1) * 32 + warp] = dot;
+    };
+    // after the block barrier: the block's sum of row t, sent to the cluster
+    auto reduce_send = [&](int64_t t) -> float {
+        float tot = lane < nw ? red[(t & 1) * 32 + lane] : 0.f;
+        tot = group_allreduce<32>(tot);
+        if (csize > 1 && tid == 0) {
+            const int b = static_cast<int>(t & 3);
+            for (uint32_t q = 0; q < csize; ++q) {
+                st_cluster_f32(cluster_map(&xslot[b * kMaxClusterSize + crank], q), tot);
+                mbar_arrive_remote(cluster_map(&xbar[b], q));
+            }
+        }
+        return tot;
+    };
+    // the row sum of row t: the block's own, or the C blocks' in rank order
+    auto receive = [&](int64_t t, float own) -> float {
+        if (csize == 1) return own;
+        const int b = static_cast<int>(t & 3);
+        if (!xfailed &&
+            !mbar_wait_cluster_bounded(&xbar[b], static_cast<uint32_t>((t >> 2) & 1), a.wait_limit_ns)) {
+            xfailed = true;  // later exchanges are not waited for again
+            *fail = 1;
+            report_status(a.status, kStatusTimeout);
+        }
+        float tot = 0.f;
+        for (uint32_t q = 0; q < csize; ++q) tot += xslot[b * kMaxClusterSize + q];
+        return tot;
+    };
+    // pass 2 of row t: dx = r*(g - xhat*c), dw += dy*xhat
+    auto pass2 = [&](int64_t t, float r, float tot) {
+        const int s = static_cast<int>(t % S);
+        const unsigned char* xs = sx + s * unit;
+        const unsigned char* ds = sdy + s * unit;
+        const float c = r * (tot / static_cast<float>(N));
+        const float2 r2 = f2_splat(r), nc2 = f2_splat(-c);
+        T* dxr = DX + (cid + t * ncl) * N;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * nthr + tid;
+            if (k >= vcnt) continue;
+            float2 fx[PR], fd[PR], fw[PR], o[PR];
+            P::unpack2(ld_shared_16(xs + k * 16), fx);
+            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            P::unpack2(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < PR; ++e) {
+                const float2 xh = __fmul2_rn(fx[e], r2);
+                const float2 gg = __fmul2_rn(fd[e], fw[e]);
+                o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
+                acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
+            }
+            st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(o));
+        }
+    };
+
+    float r_cur = nrows > 0 ? __ldg(a.rstd + cid) : 0.f;
+    float r_next = nrows > 1 ? __ldg(a.rstd + cid + ncl) : 0.f;
+    float tot_cur = 0.f;
+    if (nrows > 0) {
+        pass1(0);
+        __syncthreads();
+        failed = *fail != 0;
+        tot_cur = reduce_send(0);
+    }
+    for (int64_t t = 0; t < nrows; ++t) {
+        const float r_after = t + 2 < nrows ? __ldg(a.rstd + cid + (t + 2) * ncl) : 0.f;
+        if (t + 1 < nrows) pass1(t + 1);
+        __syncthreads();  // sums of row t+1 published; every thread is done with row t-1
+        failed = *fail != 0;
+        const float tot_next = t + 1 < nrows ? reduce_send(t + 1) : 0.f;
+        // the stage of row t-1 is free now: refill it with row t-1+S
+        if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+            fence_proxy_async_shared();
+            issue(t - 1 + S);
+        }
+        pass2(t, r_cur, receive(t, tot_cur));
+        tot_cur = tot_next;
+        r_cur = r_next;
+        r_next = r_after;
+    }
+    allow_dependent_launch();
+
+    if (tid == 0 && failed)
+        for (int s = 0; s < S; ++s)
+            if ((pending >> s) & 1u)
+                mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, a.wait_limit_ns);
+
+    // one partial row per cluster; each block writes its column slice
+    float* prow = a.partial + cid * N + static_cast<int64_t>(vbeg) * VEC;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * nthr + tid;
+        if (k >= vcnt) continue;
+#pragma unroll
+        for (int q = 0; q < PR / 2; ++q)
+            *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
+                make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x, acc[j][2 * q + 1].y);
+    }
+    // no block may leave while a peer can still reach its shared memory
     if (csize > 1) cluster_sync_all();
 }
 
@@ -552,14 +777,23 @@ const void* row_kernel(int V) {
 }
 
 template <typename T>
+const void* wide_kernel(int V) {
+    switch (V) {
+        case 4: return reinterpret_cast<const void*>(&bwd_wide_kernel<T, 4>);
+        case 8: return reinterpret_cast<const void*>(&bwd_wide_kernel<T, 8>);
+        default: return nullptr;
+    }
+}
+
+template <typename T>
 const void* rowgroup_kernel(int G, int V) {
-    if (G == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 4, 1, 4>);
-    if (G == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 8, 1, 4>);
-    if (G == 16) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 16, 1, 4>);
-    if (V == 1) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 1, 2>);
-    if (V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 2, 2>);
-    if (V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 4, 1>);
-    if (V == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 8, 1>);
+    if (G == 4 && V == 1) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 4, 1, 4>);
+    if (G == 4 && V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 4, 2, 2>);
+    if (G == 8 && V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 8, 2, 2>);
+    if (G == 8 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 8, 4, 1>);
+    if (G == 16 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 16, 4, 1>);
+    if (G == 32 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 4, 1>);
+    if (G == 32 && V == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, 32, 8, 1>);
     return nullptr;
 }
 
@@ -568,7 +802,10 @@ const void* main_kernel(const rmsnorm_plan_t& p) {
     switch (p.variant) {
         case RMSNORM_VARIANT_ROWGROUP: return rowgroup_kernel<T>(p.threads_per_row, p.vectors_per_thread);
         case RMSNORM_VARIANT_CTA_ROW:
-        case RMSNORM_VARIANT_CLUSTER_ROW: return row_kernel<T>(p.vectors_per_thread);
+        case RMSNORM_VARIANT_CLUSTER_ROW:
+            // single blocks: the grouped kernel; clusters: the pipelined one
+            return p.cluster == 1 ? row_kernel<T>(p.vectors_per_thread)
+                                  : wide_kernel<T>(p.vectors_per_thread);
         case RMSNORM_VARIANT_SCALAR: return reinterpret_cast<const void*>(&bwd_scalar_kernel<T>);
         default: return nullptr;
     }
@@ -660,6 +897,7 @@ struct BwdTuning {
     int stages = 0;         // ring depth (0 = from the shared-memory budget)
     int smem_multi = 200 * 1024;   // shared memory aimed at, several groups
     int smem_single = 100 * 1024;  // shared memory aimed at, one group
+    int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
 };
 
 int env_int(const char* name, int dflt) {
@@ -676,6 +914,7 @@ const BwdTuning& tuning() {
         u.groups = std::max(0, std::min(4, env_int("RMSNORM_BWD_GROUPS", 0)));
         u.stages = std::max(0, std::min(8, env_int("RMSNORM_BWD_STAGES", 0)));
         u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
+        u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
         return u;
     }();
     return t;
@@ -692,42 +931,61 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     const int64_t nvec = N / dtype_vec(dtype);
     const BwdTuning& tu = tuning();
     GroupShape g;
-    if (vector_ok && group_shape(nvec, &g)) {
+    if (vector_ok && bwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
         p->threads = g.threads;
         p->threads_per_row = g.G;
         p->vectors_per_thread = g.V;
         p->rows_per_unit = (g.threads / g.G) * g.R;
         const int unit = static_cast<int>(p->rows_per_unit * N * sz);
-        p->stages = std::max(3, std::min(6, kStageBudget / (2 * unit)));
+        p->stages = tu.stages > 0 ? tu.stages : std::max(3, std::min(6, kStageBudget / (2 * unit)));
         p->smem_bytes = bwd_smem_bytes(p->stages, unit);
         return;
     }
     if (vector_ok) {
-        int c = 1;
-        while (2 * cdiv(nvec, c) * 16 > kSliceBudget && c < kMaxCluster) c *= 2;
-        const int64_t slots = cdiv(nvec, c);
-        int v = tu.vectors;
-        while (cdiv(slots, v) > 512 && v < 8) v *= 2;
-        const int tg = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
-        int groups = 1;
-        if (c == 1) groups = tu.groups > 0 ? tu.groups : std::max(1, std::min(4, 512 / tg));
+        // rows one block covers with 4 vectors per thread: up to four row
+        // groups per block (one for the widest of them)
+        const int tg = std::max(32, round_up(static_cast<int>(cdiv(nvec, tu.vectors)), 32));
+        int groups = tu.groups > 0 ? tu.groups : std::max(1, std::min(4, 512 / tg));
         while (groups > 1 && groups * tg > 512) --groups;
-        const int unit = v * tg * 16;
-        const int budget = groups > 1 ? tu.smem_multi : tu.smem_single;
-        int stages = tu.stages > 0 ? tu.stages : std::max(3, std::min(6, budget / (groups * 2 * unit)));
-        while (groups > 1 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --groups;
-        while (stages > 2 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --stages;
-        if (tg <= 512 && stages >= 3 && bwd_row_smem_bytes(groups, stages, unit) <= kSmemMax) {
+        if (tg <= 512) {
+            const int unit = tu.vectors * tg * 16;
+            int stages = tu.stages > 0 ? tu.stages
+                                       : std::max(3, std::min(6, tu.smem_multi / (groups * 2 * unit)));
+            while (groups > 1 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --groups;
+            while (stages > 3 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --stages;
+            if (bwd_row_smem_bytes(groups, stages, unit) <= kSmemMax) {
+                p->variant = RMSNORM_VARIANT_CTA_ROW;
+                p->row_groups = groups;
+                p->vectors_per_thread = tu.vectors;
+                p->threads = tg * groups;
+                p->threads_per_row = tg;
+                p->rows_per_unit = groups;
+                p->stages = stages;
+                p->smem_bytes = bwd_row_smem_bytes(groups, stages, unit);
+                return;
+            }
+        }
+        // wider rows: split over a cluster, one pipelined row per block
+        int c = 1;
+        while (2 * cdiv(nvec, c) * 16 > tu.slice && c < kMaxCluster) c *= 2;
+        const int64_t slots = cdiv(nvec, c);
+        int v = 4;
+        while (cdiv(slots, v) > 512 && v < 8) v *= 2;
+        const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
+        const int unit = v * t * 16;
+        int stages = tu.stages > 0 ? tu.stages : std::max(3, std::min(6, tu.smem_multi / (2 * unit)));
+        while (stages > 3 && bwd_wide_smem_bytes(stages, unit) > kSmemMax) --stages;
+        if (t <= 512 && bwd_wide_smem_bytes(stages, unit) <= kSmemMax) {
             p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
             p->cluster = c;
-            p->row_groups = groups;
+            p->row_groups = 1;
             p->vectors_per_thread = v;
-            p->threads = tg * groups;
-            p->threads_per_row = tg * c;
-            p->rows_per_unit = groups;
+            p->threads = t;
+            p->threads_per_row = t * c;
+            p->rows_per_unit = 1;
             p->stages = stages;
-            p->smem_bytes = bwd_row_smem_bytes(groups, stages, unit);
+            p->smem_bytes = bwd_wide_smem_bytes(stages, unit);
             return;
         }
     }

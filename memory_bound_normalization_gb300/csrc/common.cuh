@@ -108,6 +108,31 @@ __device__ __forceinline__ void st_global_16(void* p, const uint4& v) {
     *reinterpret_cast<uint4*>(p) = v;
 }
 
+// L2 eviction-priority policies (createpolicy): evict_last keeps lines that
+// will be read again soon, evict_first marks lines used for the last time.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ld_global_16_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_global_16_hint(void* p, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 // ------------------------------------------------------------ reductions
 // xor butterfly: every lane ends with the same bits (each step adds the
 // same two operands in both partner lanes, and fp32 addition commutes).
@@ -231,6 +256,49 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
     return v;
+}
+
+// Address of the same shared-memory location in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+// Store a float into another block's shared memory (distributed shared memory).
+__device__ __forceinline__ void st_cluster_f32(uint32_t remote, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+// Arrive on an mbarrier in another block of the cluster, releasing this
+// thread's prior writes (including distributed shared-memory stores) at
+// cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+                 : "memory");
+}
+// try_wait with acquire at cluster scope: makes the writes released by
+// remote arrivals on this barrier visible to the waiting thread.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          uint64_t limit_ns) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
 }
 
 // Records the first failure on the device status word.

@@ -16,6 +16,8 @@
 // Any input that is not 16-byte aligned, or whose row is not a whole number
 // of 16-byte vectors, takes the scalar kernel.
 #include <algorithm>
+#include <cstdlib>
+#include <string>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -172,6 +174,81 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
     if (csize > 1) cluster_sync_all();
 }
 
+// ---------------------------------------------------------------- wide rows
+// Rows too wide for one block's registers: a block per row (grid-strided over
+// a small persistent grid), the row streamed in chunks of blockDim.x*U
+// vectors twice. Pass 1 sums x^2 and asks L2 to keep x (evict_last); pass 2
+// reads x back from L2 (evict_first: last use), scales and stores y. HBM reads
+// x once; with one or two blocks per SM the rows in flight take a few tens
+// of MB of L2, far below its size.
+template <typename T, int U>
+__global__ void __launch_bounds__(512) fwd_wide_kernel(const T* __restrict__ x,
+                                                       const T* __restrict__ w,
+                                                       T* __restrict__ y, float* __restrict__ rstd,
+                                                       int64_t M, int N, float eps) {
+    using P = Pack<T>;
+    constexpr int VEC = P::VEC;
+    constexpr int PR = P::PAIRS;
+    __shared__ float red[2][32];
+    const int nthr = blockDim.x, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    const int nvec = N / VEC;
+    const uint64_t keep = l2_policy_evict_last();
+    const uint64_t last = l2_policy_evict_first();
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
+        const T* xr = x + row * N;
+        float2 ss2 = make_float2(0.f, 0.f);
+        for (int base = 0; base < nvec; base += nthr * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = base + u * nthr + tid;
+                v[u] = k < nvec ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, keep)
+                                : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float2 f[PR];
+                P::unpack2(v[u], f);
+#pragma unroll
+                for (int e = 0; e < PR; ++e) ss2 = __ffma2_rn(f[e], f[e], ss2);
+            }
+        }
+        float ss = group_allreduce<32>(ss2.x + ss2.y);
+        if (lane == 0) red[it & 1][warp] = ss;
+        __syncthreads();
+        float total = lane < nw ? red[it & 1][lane] : 0.f;
+        total = group_allreduce<32>(total);
+        const float rs = rsqrtf(total / static_cast<float>(N) + eps);
+        const float2 rs2 = f2_splat(rs);
+        T* yr = y + row * N;
+        for (int base = 0; base < nvec; base += nthr * U) {
+            uint4 v[U], wv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = base + u * nthr + tid;
+                const bool ok = k < nvec;
+                v[u] = ok ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, last)
+                          : make_uint4(0, 0, 0, 0);
+                wv[u] = ok ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = base + u * nthr + tid;
+                if (k >= nvec) continue;
+                float2 fx[PR], fw[PR], fy[PR];
+                P::unpack2(v[u], fx);
+                P::unpack2(wv[u], fw);
+#pragma unroll
+                for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
+                st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
+            }
+        }
+        if (tid == 0) rstd[row] = rs;
+    }
+}
+
 // -------------------------------------------------------------------- scalar
 // Any alignment, any N: one block per row (grid-strided over rows), two
 // passes over the row with scalar loads.
@@ -216,13 +293,13 @@ cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStrea
 template <typename T>
 cudaError_t dispatch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     const int G = p.threads_per_row, V = p.vectors_per_thread;
-    if (G == 4) return launch_rowgroup<T, 4, 1, 4>(p, a, s);
-    if (G == 8) return launch_rowgroup<T, 8, 1, 4>(p, a, s);
-    if (G == 16) return launch_rowgroup<T, 16, 1, 4>(p, a, s);
-    if (V == 1) return launch_rowgroup<T, 32, 1, 2>(p, a, s);
-    if (V == 2) return launch_rowgroup<T, 32, 2, 2>(p, a, s);
-    if (V == 4) return launch_rowgroup<T, 32, 4, 1>(p, a, s);
-    if (V == 8) return launch_rowgroup<T, 32, 8, 1>(p, a, s);
+    if (G == 4 && V == 1) return launch_rowgroup<T, 4, 1, 4>(p, a, s);
+    if (G == 4 && V == 2) return launch_rowgroup<T, 4, 2, 4>(p, a, s);
+    if (G == 8 && V == 2) return launch_rowgroup<T, 8, 2, 4>(p, a, s);
+    if (G == 8 && V == 4) return launch_rowgroup<T, 8, 4, 2>(p, a, s);
+    if (G == 16 && V == 4) return launch_rowgroup<T, 16, 4, 2>(p, a, s);
+    if (G == 32 && V == 4) return launch_rowgroup<T, 32, 4, 1>(p, a, s);
+    if (G == 32 && V == 8) return launch_rowgroup<T, 32, 8, 1>(p, a, s);
     return cudaErrorInvalidValue;
 }
 
@@ -260,6 +337,12 @@ cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t
 
 template <typename T>
 cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    if (p.variant == RMSNORM_VARIANT_TWO_PASS) {
+        fwd_wide_kernel<T, 8><<<p.grid, p.threads, 0, s>>>(
+            static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd,
+            a.M, a.N, a.eps);
+        return cudaGetLastError();
+    }
     switch (p.variant) {
         case RMSNORM_VARIANT_ROWGROUP: return dispatch_rowgroup<T>(p, a, s);
         case RMSNORM_VARIANT_CTA_ROW:
@@ -275,9 +358,18 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
 
 }  // namespace
 
-// Largest row (in 16-byte vectors) one block holds in registers: 1024
-// threads x 4 vectors. Wider rows are split over a cluster, then the vector
-// count per thread doubles; beyond that the scalar kernel runs.
+// Mid rows: a block holds the row in registers, up to 1024 threads x 4
+// vectors. Wider rows take the two-pass kernel, or, with RMSNORM_FWD_WIDE=cluster, a cluster of up to 8 blocks holding the
+// row in registers (kept for comparison sweeps); beyond that the scalar
+// kernel runs.
+bool fwd_wide_uses_clusters() {
+    static const bool c = [] {
+        const char* v = getenv("RMSNORM_FWD_WIDE");
+        return v != nullptr && std::string(v) == "cluster";
+    }();
+    return c;
+}
+
 void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     *p = rmsnorm_plan_t{};
     p->stages = 0;
@@ -286,7 +378,7 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     p->rows_per_unit = 1;
     const int64_t nvec = N / dtype_vec(dtype);
     GroupShape g;
-    if (vector_ok && group_shape(nvec, &g)) {
+    if (vector_ok && fwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
         p->threads = g.threads;
         p->threads_per_row = g.G;
@@ -294,7 +386,14 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         p->rows_per_unit = (g.threads / g.G) * g.R;
         return;
     }
-    if (vector_ok) {
+    if (vector_ok && nvec <= 1024 * 4) {
+        p->variant = RMSNORM_VARIANT_CTA_ROW;
+        p->vectors_per_thread = 4;
+        p->threads = round_up(static_cast<int>(cdiv(nvec, 4)), 32);
+        p->threads_per_row = p->threads;
+        return;
+    }
+    if (vector_ok && fwd_wide_uses_clusters()) {
         int c = 1, v = 4;
         while (cdiv(nvec, c) > 1024 * v && c < kMaxCluster) c *= 2;
         if (cdiv(nvec, c) > 1024 * v) v = 8;
@@ -307,6 +406,15 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
             p->threads_per_row = p->threads * c;
             return;
         }
+    }
+    if (vector_ok) {
+        p->variant = RMSNORM_VARIANT_TWO_PASS;
+        p->vectors_per_thread = 8;
+        // blocks per SM: rows in flight must stay far below L2
+        p->rows_per_unit = N * dtype_size(dtype) > 128 * 1024 ? 1 : 2;
+        p->threads = 512;
+        p->threads_per_row = 512;
+        return;
     }
     p->variant = RMSNORM_VARIANT_SCALAR;
     p->threads = 256;
@@ -322,6 +430,11 @@ cudaError_t fwd_finish_plan(const DeviceInfo& dev, int, int64_t M, rmsnorm_plan_
         case RMSNORM_VARIANT_CTA_ROW:
         case RMSNORM_VARIANT_CLUSTER_ROW:
             p->grid = static_cast<int>(M * p->cluster);
+            break;
+        case RMSNORM_VARIANT_TWO_PASS:
+            // rows_per_unit blocks per SM walk all rows
+            p->grid = static_cast<int>(
+                std::min<int64_t>(M, static_cast<int64_t>(p->rows_per_unit) * dev.sm_count));
             break;
         case RMSNORM_VARIANT_SCALAR:
             p->grid = static_cast<int>(std::min<int64_t>(M, static_cast<int64_t>(dev.sm_count) * 64));

@@ -63,18 +63,33 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
 cudaError_t probe_launch(int kind, void* dst, const void* a, const void* b, size_t bytes,
                          int grid, cudaStream_t s);
 
-// Row-group geometry shared by the forward and backward short-row kernels:
-// G lanes per row, V 16-byte vectors per lane, R rows per group per pass.
+// Row-group geometry of the short-row kernels: G lanes per row, V 16-byte
+// vectors per lane, R rows per group per pass, block size.
 struct GroupShape {
     int G, V, R, threads;
 };
-inline bool group_shape(int64_t nvec, GroupShape* g) {
+// Forward: each lane holds 16-32 elements and R rows in registers.
+inline bool fwd_group_shape(int64_t nvec, GroupShape* g) {
     if (nvec <= 4) *g = {4, 1, 4, 256};
-    else if (nvec <= 8) *g = {8, 1, 4, 256};
-    else if (nvec <= 16) *g = {16, 1, 4, 256};
-    else if (nvec <= 32) *g = {32, 1, 2, 256};
-    else if (nvec <= 64) *g = {32, 2, 2, 256};
+    else if (nvec <= 8) *g = {4, 2, 4, 128};
+    else if (nvec <= 16) *g = {8, 2, 4, 128};
+    else if (nvec <= 32) *g = {8, 4, 2, 128};
+    else if (nvec <= 64) *g = {16, 4, 2, 128};
     else if (nvec <= 128) *g = {32, 4, 1, 256};
+    else if (nvec <= 256) *g = {32, 8, 1, 128};
+    else return false;
+    return true;
+}
+// Backward: 128-thread blocks whose tile of rows is about 8 KB per tensor, so
+// a three-stage ring of x and dy fits in about 48 KB and four blocks (16
+// warps) share an SM. Wider rows take the grouped row kernel.
+inline bool bwd_group_shape(int64_t nvec, GroupShape* g) {
+    if (nvec <= 4) *g = {4, 1, 4, 128};
+    else if (nvec <= 8) *g = {4, 2, 2, 128};
+    else if (nvec <= 16) *g = {8, 2, 2, 128};
+    else if (nvec <= 32) *g = {8, 4, 1, 128};
+    else if (nvec <= 64) *g = {16, 4, 1, 128};
+    else if (nvec <= 128) *g = {32, 4, 1, 128};
     else if (nvec <= 256) *g = {32, 8, 1, 128};
     else return false;
     return true;

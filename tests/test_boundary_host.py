@@ -132,11 +132,13 @@ def test_width_ladder(lib, N, dtype):
             tg = p.threads // p.row_groups
             assert tg * p.vectors_per_thread * p.cluster * vec >= N
             assert p.threads_per_row == tg * p.cluster
-            assert p.cluster == 1 or p.row_groups == 1
+            assert 1 <= p.row_groups <= 4
+        elif name == "two_pass":
+            assert pass_ == pkg.PASS_FWD and N > 512 * 4 * vec
         else:
-            # vector kernels cover every row up to 256 KiB; wider rows may
-            # outgrow registers (forward) or shared memory (backward)
-            assert name == "scalar" and N * (16 // vec) > 256 * 1024
+            # the backward's vector kernels cover every row up to 256 KiB;
+            # wider rows outgrow shared memory
+            assert name == "scalar" and pass_ == pkg.PASS_BWD and N * (16 // vec) > 256 * 1024
         if pass_ == pkg.PASS_BWD and name != "scalar":
             assert 3 <= p.stages <= 6
             if name == "rowgroup":
