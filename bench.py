@@ -99,6 +99,27 @@ def read_profiled_traffic(kernel_tag: str, workload: str, source_hash: str):
     return int(t.group(1))
 
 
+# ------------------------------------------------------------ multi-rank
+
+def slowest_rank(dist, values, device):
+    """Elementwise maximum of `values` (floats) over all ranks; the values
+    themselves when not distributed. Timing reports the slowest replica."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_throughput(world: int, logical_bytes_per_replica: int, step_ms: float) -> float:
+    """Whole-job GB/s: every rank runs one replica of the workload (weak
+    scaling), so the job moves world x the logical bytes per step, in the
+    slowest rank's step time."""
+    return world * logical_bytes_per_replica / (step_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -402,10 +423,8 @@ def run_ours(args):
     bwd_mean = sum(bwd_ms) / K
     step_ms = fwd_mean + bwd_mean
     region_ms = event_ms(region0, region1)
-    if dist is not None:
-        t = torch.tensor([step_ms, fwd_mean, bwd_mean], device=base["x"].device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, fwd_mean, bwd_mean = (float(v) for v in t.tolist())
+    step_ms, fwd_mean, bwd_mean = slowest_rank(dist, [step_ms, fwd_mean, bwd_mean],
+                                               base["x"].device)
 
     if args.profile:
         line = {"profile": True, "workload": wl.name, "fwd_ms": round(fwd_mean, 5),
@@ -418,14 +437,12 @@ def run_ours(args):
     # end to end through pinned host buffers
     e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes)
     if dist is not None:
-        t = torch.tensor([e2e["step_ms"]], device=base["x"].device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["step_ms"] = float(t.item())
-        e2e["value"] = round(world * (fwd_bytes + bwd_bytes) / (e2e["step_ms"] * 1e-3) / 1e9, 2)
+        e2e["step_ms"] = slowest_rank(dist, [e2e["step_ms"]], base["x"].device)[0]
+        e2e["value"] = round(replica_throughput(world, fwd_bytes + bwd_bytes, e2e["step_ms"]), 2)
 
     plan_f = pkg.rmsnorm_plan(M, N, code, pkg.PASS_FWD, local).as_dict()
     plan_b = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD, local).as_dict()
-    value = world * (fwd_bytes + bwd_bytes) / (step_ms * 1e-3) / 1e9
+    value = replica_throughput(world, fwd_bytes + bwd_bytes, step_ms)
     bwd_gbs = bwd_bytes / (bwd_mean * 1e-3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_mean * 1e-3) / 1e9
     traffic = read_profiled_traffic("rmsnorm_bwd", wl.name, libbuild.kernel_source_hash())

@@ -41,6 +41,40 @@ constexpr int kStageBudget = 48 * 1024;   // ring bytes aimed at per short-row b
 constexpr int kSliceBudget = 64 * 1024;   // x+dy bytes of one row slice per stage
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory a block may opt into
 
+// Tuning overrides for sweeps (read once; unset = built-in ladder). They
+// change the persistent grid, hence the order of the dw sum: results stay
+// deterministic for a fixed setting.
+struct BwdTuning {
+    int vectors = 4;        // 16-byte vectors per thread in a row group
+    int groups = 0;         // row groups per block (0 = up to 4, 512 threads)
+    int stages = 0;         // ring depth (0 = from the shared-memory budget)
+    int smem_multi = 200 * 1024;   // shared memory aimed at, several groups
+    int smem_single = 100 * 1024;  // shared memory aimed at, one group
+    int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
+    bool pipelined = false;        // cluster rows: pass 1 of the next row first
+};
+
+int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    if (v == nullptr || *v == 0) return dflt;
+    return atoi(v);
+}
+
+const BwdTuning& tuning() {
+    static const BwdTuning t = [] {
+        BwdTuning u;
+        u.vectors = env_int("RMSNORM_BWD_VECTORS", u.vectors);
+        if (u.vectors != 1 && u.vectors != 2 && u.vectors != 4 && u.vectors != 8) u.vectors = 4;
+        u.groups = std::max(0, std::min(4, env_int("RMSNORM_BWD_GROUPS", 0)));
+        u.stages = std::max(0, std::min(8, env_int("RMSNORM_BWD_STAGES", 0)));
+        u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
+        u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
+        u.pipelined = env_int("RMSNORM_BWD_PIPE", 0) != 0;
+        return u;
+    }();
+    return t;
+}
+
 // Shared memory of the short-row kernel: [S][unit] x | [S][unit] dy |
 // mbarrier[S] | 66 floats of reduction slots | failure flag.
 __host__ __device__ inline int bwd_smem_bytes(int stages, int unit) {
@@ -302,7 +336,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
 // peer sends row r+1 only after receiving row r-1, which needs this block's
 // send of row r-1, made before this block reads the slots of row r-2; so a
 // writer is at most three rows ahead of a reader.
-template <typename T, int V>
+template <typename T, int V, bool PIPE>
 __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, int /*groups*/) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
@@ -469,28 +503,48 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
 
     float r_cur = nrows > 0 ? __ldg(a.rstd + cid) : 0.f;
     float r_next = nrows > 1 ? __ldg(a.rstd + cid + ncl) : 0.f;
-    float tot_cur = 0.f;
-    if (nrows > 0) {
-        pass1(0);
-        __syncthreads();
-        failed = *fail != 0;
-        tot_cur = reduce_send(0);
-    }
-    for (int64_t t = 0; t < nrows; ++t) {
-        const float r_after = t + 2 < nrows ? __ldg(a.rstd + cid + (t + 2) * ncl) : 0.f;
-        if (t + 1 < nrows) pass1(t + 1);
-        __syncthreads();  // sums of row t+1 published; every thread is done with row t-1
-        failed = *fail != 0;
-        const float tot_next = t + 1 < nrows ? reduce_send(t + 1) : 0.f;
-        // the stage of row t-1 is free now: refill it with row t-1+S
-        if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
-            fence_proxy_async_shared();
-            issue(t - 1 + S);
+    if (PIPE) {
+        // pass 1 of row t+1 runs before pass 2 of row t; the ring keeps two
+        // rows resident, so S-2 rows are in flight
+        float tot_cur = 0.f;
+        if (nrows > 0) {
+            pass1(0);
+            __syncthreads();
+            failed = *fail != 0;
+            tot_cur = reduce_send(0);
         }
-        pass2(t, r_cur, receive(t, tot_cur));
-        tot_cur = tot_next;
-        r_cur = r_next;
-        r_next = r_after;
+        for (int64_t t = 0; t < nrows; ++t) {
+            const float r_after = t + 2 < nrows ? __ldg(a.rstd + cid + (t + 2) * ncl) : 0.f;
+            if (t + 1 < nrows) pass1(t + 1);
+            __syncthreads();  // sums of row t+1 published; every thread is done with row t-1
+            failed = *fail != 0;
+            const float tot_next = t + 1 < nrows ? reduce_send(t + 1) : 0.f;
+            // the stage of row t-1 is free now: refill it with row t-1+S
+            if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+                fence_proxy_async_shared();
+                issue(t - 1 + S);
+            }
+            pass2(t, r_cur, receive(t, tot_cur));
+            tot_cur = tot_next;
+            r_cur = r_next;
+            r_next = r_after;
+        }
+    } else {
+        // one row at a time: S-1 rows in flight, the exchange waited for in place
+        for (int64_t t = 0; t < nrows; ++t) {
+            const float r_after = t + 2 < nrows ? __ldg(a.rstd + cid + (t + 2) * ncl) : 0.f;
+            pass1(t);
+            __syncthreads();  // sums of row t published; every thread is done with row t-1
+            failed = *fail != 0;
+            const float own = reduce_send(t);
+            if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+                fence_proxy_async_shared();
+                issue(t - 1 + S);
+            }
+            pass2(t, r_cur, receive(t, own));
+            r_cur = r_next;
+            r_next = r_after;
+        }
     }
     allow_dependent_launch();
 
@@ -777,12 +831,12 @@ const void* row_kernel(int V) {
 }
 
 template <typename T>
-const void* wide_kernel(int V) {
-    switch (V) {
-        case 4: return reinterpret_cast<const void*>(&bwd_wide_kernel<T, 4>);
-        case 8: return reinterpret_cast<const void*>(&bwd_wide_kernel<T, 8>);
-        default: return nullptr;
-    }
+const void* wide_kernel(int V, bool pipelined) {
+    if (V == 4) return pipelined ? reinterpret_cast<const void*>(&bwd_wide_kernel<T, 4, true>)
+                                 : reinterpret_cast<const void*>(&bwd_wide_kernel<T, 4, false>);
+    if (V == 8) return pipelined ? reinterpret_cast<const void*>(&bwd_wide_kernel<T, 8, true>)
+                                 : reinterpret_cast<const void*>(&bwd_wide_kernel<T, 8, false>);
+    return nullptr;
 }
 
 template <typename T>
@@ -805,7 +859,7 @@ const void* main_kernel(const rmsnorm_plan_t& p) {
         case RMSNORM_VARIANT_CLUSTER_ROW:
             // single blocks: the grouped kernel; clusters: the pipelined one
             return p.cluster == 1 ? row_kernel<T>(p.vectors_per_thread)
-                                  : wide_kernel<T>(p.vectors_per_thread);
+                                  : wide_kernel<T>(p.vectors_per_thread, tuning().pipelined);
         case RMSNORM_VARIANT_SCALAR: return reinterpret_cast<const void*>(&bwd_scalar_kernel<T>);
         default: return nullptr;
     }
@@ -888,37 +942,6 @@ cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, i
 }
 
 
-// Tuning overrides for sweeps (read once; unset = built-in ladder). They
-// change the persistent grid, hence the order of the dw sum: results stay
-// deterministic for a fixed setting.
-struct BwdTuning {
-    int vectors = 4;        // 16-byte vectors per thread in a row group
-    int groups = 0;         // row groups per block (0 = up to 4, 512 threads)
-    int stages = 0;         // ring depth (0 = from the shared-memory budget)
-    int smem_multi = 200 * 1024;   // shared memory aimed at, several groups
-    int smem_single = 100 * 1024;  // shared memory aimed at, one group
-    int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
-};
-
-int env_int(const char* name, int dflt) {
-    const char* v = getenv(name);
-    if (v == nullptr || *v == 0) return dflt;
-    return atoi(v);
-}
-
-const BwdTuning& tuning() {
-    static const BwdTuning t = [] {
-        BwdTuning u;
-        u.vectors = env_int("RMSNORM_BWD_VECTORS", u.vectors);
-        if (u.vectors != 1 && u.vectors != 2 && u.vectors != 4 && u.vectors != 8) u.vectors = 4;
-        u.groups = std::max(0, std::min(4, env_int("RMSNORM_BWD_GROUPS", 0)));
-        u.stages = std::max(0, std::min(8, env_int("RMSNORM_BWD_STAGES", 0)));
-        u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
-        u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
-        return u;
-    }();
-    return t;
-}
 
 }  // namespace
 

@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
 // x once; with one or two blocks per SM the rows in flight take a few tens
 // of MB of L2, far below its size.
 template <typename T, int U>
-__global__ void __launch_bounds__(512) fwd_wide_kernel(const T* __restrict__ x,
+__global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
                                                        const T* __restrict__ w,
                                                        T* __restrict__ y, float* __restrict__ rstd,
                                                        int64_t M, int N, float eps) {
@@ -338,7 +338,7 @@ cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t
 template <typename T>
 cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     if (p.variant == RMSNORM_VARIANT_TWO_PASS) {
-        fwd_wide_kernel<T, 8><<<p.grid, p.threads, 0, s>>>(
+        fwd_wide_kernel<T, 4><<<p.grid, p.threads, 0, s>>>(
             static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd,
             a.M, a.N, a.eps);
         return cudaGetLastError();
@@ -409,11 +409,12 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     }
     if (vector_ok) {
         p->variant = RMSNORM_VARIANT_TWO_PASS;
-        p->vectors_per_thread = 8;
-        // blocks per SM: rows in flight must stay far below L2
+        p->vectors_per_thread = 4;
+        // blocks per SM: rows in flight must stay far below L2; one block of
+        // 1024 threads for rows over 128 KB, else two of 512
         p->rows_per_unit = N * dtype_size(dtype) > 128 * 1024 ? 1 : 2;
-        p->threads = 512;
-        p->threads_per_row = 512;
+        p->threads = p->rows_per_unit == 1 ? 1024 : 512;
+        p->threads_per_row = p->threads;
         return;
     }
     p->variant = RMSNORM_VARIANT_SCALAR;

@@ -1,0 +1,60 @@
+"""bench.py's multi-rank logic on the CPU: two gloo ranks, each timing its
+own replica; the job reports the slowest rank's times and N x the bytes."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r measured step 1.0 + r ms, forward 0.3 + r, backward 0.7
+        got = bench.slowest_rank(dist, [1.0 + rank, 0.3 + rank, 0.7], "cpu")
+        out[rank] = got
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_over_gloo():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
+        results = dict(out)
+    assert set(results) == {0, 1}
+    for rank in range(world):
+        assert results[rank] == pytest.approx([2.0, 1.3, 0.7])
+
+
+def test_replica_throughput_is_whole_job():
+    one = bench.replica_throughput(1, 10**9, 1.0)
+    assert one == pytest.approx(1000.0)
+    assert bench.replica_throughput(4, 10**9, 1.0) == pytest.approx(4 * one)
+    assert bench.slowest_rank(None, [1, 2.5], "cpu") == [1.0, 2.5]
+
+
+def test_dist_env_defaults(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 1, 0)
+    monkeypatch.setenv("WORLD_SIZE", "8")
+    monkeypatch.setenv("RANK", "3")
+    monkeypatch.setenv("LOCAL_RANK", "3")
+    assert bench.dist_env() == (3, 8, 3)
