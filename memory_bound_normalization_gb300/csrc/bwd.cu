@@ -329,10 +329,14 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
 // The loop does pass 1 and the reduction of row t+1 before pass 2 of row t,
 // so the exchange of row t is in flight while row t+1 is read.
 //
-// Exchange: the block's sum of row t goes to slot [t&3][q] of every block of
-// the cluster (itself included), followed by a remote arrive (release) on
-// that block's barrier [t&3]; the receiver waits (acquire) and adds the C
-// slots in rank order, the same bits in every block. Four slots suffice: a
+// Exchange: the block's sum of row t goes to slot [t&3][q] of every block q
+// of the cluster (itself included; thread q does the sending) by an
+// asynchronous store whose completion counts 4 transaction bytes on that
+// block's barrier [t&3]; each block arms its barrier for 4*C bytes once per
+// row, waits (acquire), and adds the C slots in rank order, the same bits in
+// every block. A store may land before the arming: the barrier's transaction
+// count goes below zero, but the phase cannot end before the local arrival
+// that comes with the arming. Four slots suffice: a
 // peer sends row r+1 only after receiving row r-1, which needs this block's
 // send of row r-1, made before this block reads the slots of row r-2; so a
 // writer is at most three rows ahead of a reader.
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
-        for (int b = 0; b < 4; ++b) mbar_init(&xbar[b], csize);
+        for (int b = 0; b < 4; ++b) mbar_init(&xbar[b], 1);
         *fail = 0;
         fence_mbarrier_init();
     }
@@ -451,11 +455,15 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     auto reduce_send = [&](int64_t t) -> float {
         float tot = lane < nw ? red[(t & 1) * 32 + lane] : 0.f;
         tot = group_allreduce<32>(tot);
-        if (csize > 1 && tid == 0) {
+        if (csize > 1) {
             const int b = static_cast<int>(t & 3);
-            for (uint32_t q = 0; q < csize; ++q) {
-                st_cluster_f32(cluster_map(&xslot[b * kMaxClusterSize + crank], q), tot);
-                mbar_arrive_remote(cluster_map(&xbar[b], q));
+            // this block expects the C sums of row t as 4*C transaction bytes
+            if (tid == 0) mbar_arrive_expect_tx(&xbar[b], 4u * csize);
+            // thread q sends to block q (every thread holds the same sum)
+            if (static_cast<uint32_t>(tid) < csize) {
+                const uint32_t q = static_cast<uint32_t>(tid);
+                st_async_cluster_f32(cluster_map(&xslot[b * kMaxClusterSize + crank], q), tot,
+                                     cluster_map(&xbar[b], q));
             }
         }
         return tot;

@@ -268,6 +268,14 @@ __device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank
 __device__ __forceinline__ void st_cluster_f32(uint32_t remote, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
+// Asynchronous store of 4 bytes into another block's shared memory whose
+// completion is counted (4 transaction bytes) on that block's mbarrier.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t remote, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     remote),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
 // Arrive on an mbarrier in another block of the cluster, releasing this
 // thread's prior writes (including distributed shared-memory stores) at
 // cluster scope.
