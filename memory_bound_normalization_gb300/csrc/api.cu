@@ -152,7 +152,7 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
          cdiv(M, plan.variant == RMSNORM_VARIANT_ROWGROUP ? plan.rows_per_unit : 1) * plan.cluster >
              INT32_MAX))
         return RMSNORM_ERR_UNSUPPORTED;
-    FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps};
+    FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps, dev->status_word, g_wait_limit_ns.load()};
     return cuda_status(fwd_launch(plan, dtype, a, stream));
 }
 

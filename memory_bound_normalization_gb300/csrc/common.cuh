@@ -248,6 +248,14 @@ __device__ __forceinline__ void cluster_sync_all() {
         "barrier.cluster.wait.acquire.aligned;" ::
             : "memory");
 }
+// Split cluster barrier: arrive without ordering (after initialising
+// barriers that peers will use), wait with acquire before using theirs.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 // Reads a float from the same shared-memory variable in block `rank` of
 // this cluster (distributed shared memory).
 __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {

@@ -104,16 +104,21 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
 // ------------------------------------------------------- block/cluster per row
 // Cluster c (a single block when launched without clusters) owns row c; block
 // rank q of the cluster owns vector slots [q*S, (q+1)*S), S = V*blockDim.x,
-// thread t holding slots q*S + j*blockDim.x + t.
+// thread t holding slots q*S + j*blockDim.x + t. In a cluster the blocks'
+// sums of squares are exchanged by asynchronous stores into every block's
+// shared memory (thread q writes to block q), counted as transaction bytes on
+// that block's mbarrier, and added in rank order (the same bits everywhere).
 template <typename T, int V>
 __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
                                                        const T* __restrict__ w,
                                                        T* __restrict__ y, float* __restrict__ rstd,
-                                                       int64_t M, int N, float eps) {
+                                                       int64_t M, int N, float eps, int* status,
+                                                       uint64_t wait_limit_ns) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
     __shared__ float red[32];
-    __shared__ float cluster_part;
+    __shared__ float xslot[kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar;
 
     const uint32_t csize = cluster_size();
     const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
@@ -123,6 +128,13 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
     const int base = static_cast<int>(crank) * V * nthr;
     const T* xr = x + row * N;
 
+    if (csize > 1) {
+        if (threadIdx.x == 0) {
+            mbar_init(&xbar, 1);
+            fence_mbarrier_init();
+        }
+        cluster_arrive_relaxed();  // waited for below, after the loads
+    }
     uint4 xv[V], wv[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
@@ -148,12 +160,16 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
     float total = lane < (nthr >> 5) ? red[lane] : 0.f;
     total = group_allreduce<32>(total);
     if (csize > 1) {
-        // cluster: each block publishes its sum, then every thread adds the
-        // blocks' sums in rank order (same bits in every block)
-        if (threadIdx.x == 0) cluster_part = total;
-        cluster_sync_all();
+        cluster_wait();  // every block's barrier is initialised
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(&xbar, 4u * csize);
+        if (threadIdx.x < csize)
+            st_async_cluster_f32(cluster_map(&xslot[crank], threadIdx.x), total,
+                                 cluster_map(&xbar, threadIdx.x));
+        if (!mbar_wait_cluster_bounded(&xbar, 0u, wait_limit_ns)) report_status(status, kStatusTimeout);
         total = 0.f;
-        for (uint32_t q = 0; q < csize; ++q) total += ld_cluster_f32(&cluster_part, q);
+        for (uint32_t q = 0; q < csize; ++q) total += xslot[q];
+        // all C stores into this block have landed, so it may exit; the
+        // stores it sent are complete on their receivers' side the same way
     }
     const float rs = rsqrtf(total / static_cast<float>(N) + eps);
     const float2 rs2 = f2_splat(rs);
@@ -170,8 +186,6 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
         st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
     }
     if (crank == 0 && threadIdx.x == 0) rstd[row] = rs;
-    // a block's shared memory must outlive the other blocks' reads of it
-    if (csize > 1) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------- wide rows
@@ -321,18 +335,12 @@ cudaError_t launch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s
     }
     return cudaLaunchKernelEx(&cfg, fwd_row_kernel<T, V>, static_cast<const T*>(a.x),
                               static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
-                              a.eps);
+                              a.eps, a.status, a.wait_limit_ns);
 }
 
 template <typename T>
 cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
-    switch (p.vectors_per_thread) {
-        case 1: return launch_row<T, 1>(p, a, s);
-        case 2: return launch_row<T, 2>(p, a, s);
-        case 4: return launch_row<T, 4>(p, a, s);
-        case 8: return launch_row<T, 8>(p, a, s);
-        default: return cudaErrorInvalidValue;
-    }
+    return p.vectors_per_thread == 4 ? launch_row<T, 4>(p, a, s) : cudaErrorInvalidValue;
 }
 
 template <typename T>
@@ -358,16 +366,34 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
 
 }  // namespace
 
-// Mid rows: a block holds the row in registers, up to 1024 threads x 4
-// vectors. Wider rows take the two-pass kernel, or, with RMSNORM_FWD_WIDE=cluster, a cluster of up to 8 blocks holding the
-// row in registers (kept for comparison sweeps); beyond that the scalar
-// kernel runs.
-bool fwd_wide_uses_clusters() {
-    static const bool c = [] {
-        const char* v = getenv("RMSNORM_FWD_WIDE");
-        return v != nullptr && std::string(v) == "cluster";
+// Mid rows: a block holds the row in registers (4 vectors per thread). Wider
+// rows: a cluster of up to 8 blocks holding the row in registers, or the
+// two-pass kernel. RMSNORM_FWD_WIDE (cluster | two_pass),
+// RMSNORM_FWD_ROW_THREADS and RMSNORM_FWD_CLUSTER_THREADS override the
+// choices below for sweeps.
+// Measured on GB300 over the width sweep: bf16 rows do best in one block of
+// up to 512 threads and, wider, in the two-pass kernel; fp32 rows do best in
+// blocks of at most 256 threads, split over a cluster once the row needs
+// more (up to 8 blocks of up to 512 threads), then in the two-pass kernel.
+struct FwdTuning {
+    int wide = -1;             // -1: per dtype; 0: two passes; 1: clusters
+    int row_threads = 0;       // largest block holding a row (0: per dtype)
+    int cluster_threads = 256; // block size aimed at in a cluster
+};
+
+const FwdTuning& fwd_tuning() {
+    static const FwdTuning t = [] {
+        FwdTuning u;
+        const char* wide = getenv("RMSNORM_FWD_WIDE");
+        if (wide != nullptr && std::string(wide) == "cluster") u.wide = 1;
+        if (wide != nullptr && std::string(wide) == "two_pass") u.wide = 0;
+        const char* rt = getenv("RMSNORM_FWD_ROW_THREADS");
+        if (rt && *rt) u.row_threads = std::max(64, std::min(1024, atoi(rt) / 32 * 32));
+        const char* ct = getenv("RMSNORM_FWD_CLUSTER_THREADS");
+        if (ct && *ct) u.cluster_threads = std::max(64, std::min(1024, atoi(ct) / 32 * 32));
+        return u;
     }();
-    return c;
+    return t;
 }
 
 void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
@@ -386,18 +412,21 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         p->rows_per_unit = (g.threads / g.G) * g.R;
         return;
     }
-    if (vector_ok && nvec <= 1024 * 4) {
+    const FwdTuning& tu = fwd_tuning();
+    const bool bf16 = dtype == RMSNORM_BF16;
+    const int row_threads = tu.row_threads > 0 ? tu.row_threads : (bf16 ? 512 : 256);
+    const bool clusters = tu.wide >= 0 ? tu.wide == 1 : !bf16;
+    if (vector_ok && nvec <= static_cast<int64_t>(row_threads) * 4) {
         p->variant = RMSNORM_VARIANT_CTA_ROW;
         p->vectors_per_thread = 4;
         p->threads = round_up(static_cast<int>(cdiv(nvec, 4)), 32);
         p->threads_per_row = p->threads;
         return;
     }
-    if (vector_ok && fwd_wide_uses_clusters()) {
+    if (vector_ok && clusters) {
         int c = 1, v = 4;
-        while (cdiv(nvec, c) > 1024 * v && c < kMaxCluster) c *= 2;
-        if (cdiv(nvec, c) > 1024 * v) v = 8;
-        if (cdiv(nvec, c) <= 1024 * v) {
+        while (cdiv(nvec, c) > static_cast<int64_t>(tu.cluster_threads) * v && c < kMaxCluster) c *= 2;
+        if (cdiv(nvec, c) <= 512 * v) {
             const int64_t slots = cdiv(nvec, c);
             p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
             p->cluster = c;

@@ -28,6 +28,8 @@ struct FwdArgs {
     int64_t M;
     int N;
     float eps;
+    int* status;             // device status word (bounded waits)
+    uint64_t wait_limit_ns;
 };
 
 struct BwdArgs {
