@@ -61,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle budget for the cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-small-m", action="store_true",
+                   help="skip the small-M eager vs CUDA-graph latency table")
     p.add_argument("--profile", action="store_true",
                    help="lean run for profilers: no probes, validation, e2e or CPU baseline")
     p.add_argument("--json-out", default=None, help="also write the JSON line to this file")
@@ -440,6 +442,7 @@ def run_ours(args):
         e2e["step_ms"] = slowest_rank(dist, [e2e["step_ms"]], base["x"].device)[0]
         e2e["value"] = round(replica_throughput(world, fwd_bytes + bwd_bytes, e2e["step_ms"]), 2)
 
+    small_m = None if args.no_small_m else run_small_m(pkg, torch)
     plan_f = pkg.rmsnorm_plan(M, N, code, pkg.PASS_FWD, local).as_dict()
     plan_b = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD, local).as_dict()
     value = replica_throughput(world, fwd_bytes + bwd_bytes, step_ms)
@@ -494,6 +497,7 @@ def run_ours(args):
         "timed_region_ms": round(region_ms, 3),
         "clocks": clock_info,
         "e2e": e2e,
+        "small_m": small_m,
         "gpu_launches": 3 * K,
         "validation": errs,
         "library": {"path": pkg.library_path(), "source_hash": libbuild.source_hash(),
@@ -505,6 +509,55 @@ def run_ours(args):
     if dist is not None:
         dist.destroy_process_group()
     return line if rank == 0 else None
+
+
+def run_small_m(pkg, torch, steps: int = 200):
+    """Launch-bound shapes: microseconds per forward+backward step, back to
+    back, called eagerly through the C ABI versus replayed as one captured
+    CUDA graph (inputs stay in L2 here; this measures latency, not HBM)."""
+    from memory_bound_normalization_gb300 import synth
+
+    out = []
+    for M, N in ((1, 4096), (16, 4096), (256, 4096), (256, 1024)):
+        wl = synth.Workload(f"small{M}x{N}", M, N, torch.bfloat16, 1e-6, 71, 72, 73)
+        inp = synth.make_inputs(wl, device=torch.cuda.current_device())
+        x, w, dy = inp["x"], inp["w"], inp["dy"]
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        rstd = torch.empty(M, dtype=torch.float32, device=x.device)
+        dw = torch.empty(N, dtype=torch.float32, device=x.device)
+        side = torch.cuda.Stream()
+
+        def step():
+            pkg.check(pkg.rmsnorm_fwd(x, w, y, rstd, M, N, wl.eps, pkg.BF16, side))
+            pkg.check(pkg.rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, pkg.BF16, side))
+
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(10):
+                step()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(side)
+            for _ in range(steps):
+                step()
+            e1.record(side)
+        e1.synchronize()
+        eager_us = event_ms(e0, e1) * 1e3 / steps
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        with torch.cuda.stream(side):
+            for _ in range(10):
+                graph.replay()
+            e0.record(side)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(side)
+        e1.synchronize()
+        graph_us = event_ms(e0, e1) * 1e3 / steps
+        torch.cuda.current_stream().wait_stream(side)
+        out.append({"M": M, "N": N, "eager_us_per_step": round(eager_us, 2),
+                    "graph_us_per_step": round(graph_us, 2)})
+    return out
 
 
 def run_e2e(pkg, torch, wl, base, code, stream, steps, logical):
