@@ -15,9 +15,10 @@ Definitions followed:
   without the column reduction", sections "The backward pass" and "The naive
   kernel".
 
-Inputs may be numpy arrays (float64, float32, or uint16 holding bf16 bits with
-``dtype="bf16"``) or CPU torch tensors (float64, float32, bfloat16). Outputs
-are float64 numpy arrays.
+Inputs may be numpy arrays (float64, float32, float16, or uint16 holding bf16
+bits with ``dtype="bf16"``) or CPU torch tensors (float64, float32, bfloat16,
+float16). The weight may have its own type (e.g. fp32 with bf16 x and dy);
+x and dy share one. Outputs are float64 numpy arrays.
 """
 from __future__ import annotations
 
@@ -33,7 +34,7 @@ _SRC = os.path.join(_HERE, "rmsnorm_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-F64, F32, BF16 = 0, 1, 2
+F64, F32, BF16, F16 = 0, 1, 2, 3
 _lock = threading.Lock()
 _lib = None
 
@@ -52,8 +53,8 @@ def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
 
 def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     p, i64, d, i = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_int
-    lib.oracle_rmsnorm_fwd.argtypes = [p, p, i64, i64, d, i, p, i64, p, p]
-    lib.oracle_rmsnorm_bwd_dx.argtypes = [p, p, p, i64, i64, d, i, p, i64, p]
+    lib.oracle_rmsnorm_fwd.argtypes = [p, p, i64, i64, d, i, i, p, i64, p, p]
+    lib.oracle_rmsnorm_bwd_dx.argtypes = [p, p, p, i64, i64, d, i, i, p, i64, p]
     lib.oracle_rmsnorm_bwd_dw.argtypes = [p, p, i64, i64, d, i, p]
     for f in (lib.oracle_rmsnorm_fwd, lib.oracle_rmsnorm_bwd_dx, lib.oracle_rmsnorm_bwd_dw):
         f.restype = ctypes.c_int
@@ -88,12 +89,16 @@ def _as_host_array(a, dtype: str | None = None):
             return t.numpy(), F32
         if t.dtype == torch.bfloat16:
             return t.view(torch.int16).numpy().view(np.uint16), BF16
+        if t.dtype == torch.float16:
+            return t.view(torch.int16).numpy().view(np.uint16), F16
         raise TypeError(f"unsupported tensor dtype {t.dtype}")
     arr = np.ascontiguousarray(a)
-    if dtype == "bf16" or (dtype is None and arr.dtype == np.uint16):
+    if dtype in ("bf16", "f16") or (dtype is None and arr.dtype == np.uint16):
         if arr.dtype != np.uint16:
-            raise TypeError("bf16 arrays must be passed as uint16 bit patterns")
-        return arr, BF16
+            raise TypeError("16-bit arrays must be passed as uint16 bit patterns")
+        return arr, (F16 if dtype == "f16" else BF16)
+    if arr.dtype == np.float16:
+        return arr.view(np.uint16), F16
     if arr.dtype == np.float64:
         return arr, F64
     if arr.dtype == np.float32:
@@ -126,13 +131,11 @@ def _shape2(x_arr, N):
 def _fwd(lib, x, w, eps, rows=None, N=None, dtype=None):
     xa, code = _as_host_array(x, dtype)
     wa, wcode = _as_host_array(w, dtype)
-    if wcode != code:
-        raise TypeError("x and w must share a dtype")
     M, N = _shape2(xa, N)
     ra, nrows = _rows_arg(rows, M)
     y = np.empty((nrows, N), dtype=np.float64)
     r = np.empty((nrows,), dtype=np.float64)
-    rc = lib.oracle_rmsnorm_fwd(_ptr(xa), _ptr(wa), M, N, float(eps), code,
+    rc = lib.oracle_rmsnorm_fwd(_ptr(xa), _ptr(wa), M, N, float(eps), code, wcode,
                                 _ptr(ra), nrows, _ptr(y), _ptr(r))
     if rc:
         raise ValueError(f"oracle_rmsnorm_fwd rejected its arguments ({rc})")
@@ -143,12 +146,12 @@ def _bwd_dx(lib, x, w, dy, eps, rows=None, N=None, dtype=None):
     xa, code = _as_host_array(x, dtype)
     wa, wcode = _as_host_array(w, dtype)
     da, dcode = _as_host_array(dy, dtype)
-    if not (code == wcode == dcode):
-        raise TypeError("x, w and dy must share a dtype")
+    if code != dcode:
+        raise TypeError("x and dy must share a dtype")
     M, N = _shape2(xa, N)
     ra, nrows = _rows_arg(rows, M)
     dx = np.empty((nrows, N), dtype=np.float64)
-    rc = lib.oracle_rmsnorm_bwd_dx(_ptr(xa), _ptr(wa), _ptr(da), M, N, float(eps), code,
+    rc = lib.oracle_rmsnorm_bwd_dx(_ptr(xa), _ptr(wa), _ptr(da), M, N, float(eps), code, wcode,
                                    _ptr(ra), nrows, _ptr(dx))
     if rc:
         raise ValueError(f"oracle_rmsnorm_bwd_dx rejected its arguments ({rc})")

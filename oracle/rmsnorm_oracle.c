@@ -34,10 +34,12 @@
  * squares in double as well. r_i is always recomputed from x here; the
  * backward never reads an rstd produced elsewhere.
  *
- * Inputs are read in their stored type (fp64, fp32 or bf16) and converted to
- * double exactly; outputs are double. Where the caller passes a list of row
- * indices, only those rows of y, r and dx are produced (so huge matrices can
- * be checked on a sample); dw always covers every row.
+ * Inputs are read in their stored type (fp64, fp32, bf16 or fp16; the weight
+ * may have its own type, e.g. an fp32 master weight with bf16 activations --
+ * "What a tuned RMSNorm kernel actually costs on Hopper", section 07) and
+ * converted to double exactly; outputs are double. Where the caller passes a
+ * list of row indices, only those rows of y, r and dx are produced (so huge
+ * matrices can be checked on a sample); dw always covers every row.
  *
  * Parity status: every function here is pinned by the tests under tests/
  * (printed worked examples, closed forms, finite differences and an
@@ -50,9 +52,27 @@
 #define ORACLE_F64 0
 #define ORACLE_F32 1
 #define ORACLE_BF16 2
+#define ORACLE_F16 3
 
 #define ORACLE_OK 0
 #define ORACLE_BAD_ARG 1
+
+/* IEEE 754 binary16: sign bit, 5 exponent bits (bias 15), 10 fraction bits;
+ * exponent 0 encodes subnormals (fraction * 2^-24), exponent 31 inf/NaN. */
+static double half_bits_to_double(uint16_t h)
+{
+    int sign = h >> 15;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+    return sign ? -v : v;
+}
 
 /* Element k of an array stored as dtype, as an exact double. */
 static double load_as_double(const void *base, int dtype, int64_t k)
@@ -61,6 +81,8 @@ static double load_as_double(const void *base, int dtype, int64_t k)
         return ((const double *)base)[k];
     if (dtype == ORACLE_F32)
         return (double)((const float *)base)[k];
+    if (dtype == ORACLE_F16)
+        return half_bits_to_double(((const uint16_t *)base)[k]);
     /* bf16: the 16 stored bits are the high half of an IEEE binary32. */
     {
         uint32_t bits = ((uint32_t)((const uint16_t *)base)[k]) << 16;
@@ -70,11 +92,17 @@ static double load_as_double(const void *base, int dtype, int64_t k)
     }
 }
 
+static int dtype_ok(int dtype)
+{
+    return dtype == ORACLE_F64 || dtype == ORACLE_F32 || dtype == ORACLE_BF16 ||
+           dtype == ORACLE_F16;
+}
+
 static int check_args(const void *x, int64_t M, int64_t N, int dtype)
 {
     if (M < 0 || N <= 0)
         return ORACLE_BAD_ARG;
-    if (dtype != ORACLE_F64 && dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+    if (!dtype_ok(dtype))
         return ORACLE_BAD_ARG;
     if (M > 0 && x == NULL)
         return ORACLE_BAD_ARG;
@@ -111,15 +139,16 @@ static int check_rows(const int64_t *rows, int64_t nrows, int64_t M)
 }
 
 /*
- * Forward. y_out is nrows x N (row k of y_out is row pick_row(k) of the
- * matrix), r_out has nrows entries. Either output may be NULL.
+ * Forward. x is stored as dtype, w as w_dtype. y_out is nrows x N (row k of
+ * y_out is row pick_row(k) of the matrix), r_out has nrows entries. Either
+ * output may be NULL.
  */
 int oracle_rmsnorm_fwd(const void *x, const void *w, int64_t M, int64_t N,
-                       double eps, int dtype, const int64_t *rows,
+                       double eps, int dtype, int w_dtype, const int64_t *rows,
                        int64_t nrows, double *y_out, double *r_out)
 {
     int64_t k, j;
-    if (check_args(x, M, N, dtype) || check_rows(rows, nrows, M))
+    if (check_args(x, M, N, dtype) || check_rows(rows, nrows, M) || !dtype_ok(w_dtype))
         return ORACLE_BAD_ARG;
     if (nrows > 0 && y_out && w == NULL)
         return ORACLE_BAD_ARG;
@@ -131,18 +160,19 @@ int oracle_rmsnorm_fwd(const void *x, const void *w, int64_t M, int64_t N,
         if (y_out)
             for (j = 0; j < N; ++j)
                 y_out[k * N + j] = load_as_double(x, dtype, i * N + j) * r *
-                                   load_as_double(w, dtype, j);
+                                   load_as_double(w, w_dtype, j);
     }
     return ORACLE_OK;
 }
 
-/* Backward input gradient for the requested rows; dx_out is nrows x N. */
+/* Backward input gradient for the requested rows; dx_out is nrows x N. x
+ * and dy are stored as dtype, w as w_dtype. */
 int oracle_rmsnorm_bwd_dx(const void *x, const void *w, const void *dy,
-                          int64_t M, int64_t N, double eps, int dtype,
+                          int64_t M, int64_t N, double eps, int dtype, int w_dtype,
                           const int64_t *rows, int64_t nrows, double *dx_out)
 {
     int64_t k, j;
-    if (check_args(x, M, N, dtype) || check_rows(rows, nrows, M))
+    if (check_args(x, M, N, dtype) || check_rows(rows, nrows, M) || !dtype_ok(w_dtype))
         return ORACLE_BAD_ARG;
     if (nrows > 0 && (w == NULL || dy == NULL || dx_out == NULL))
         return ORACLE_BAD_ARG;
@@ -153,14 +183,14 @@ int oracle_rmsnorm_bwd_dx(const void *x, const void *w, const void *dy,
         for (j = 0; j < N; ++j) {
             double xhat = load_as_double(x, dtype, i * N + j) * r;
             double g = load_as_double(dy, dtype, i * N + j) *
-                       load_as_double(w, dtype, j);
+                       load_as_double(w, w_dtype, j);
             c += g * xhat;
         }
         c /= (double)N;
         for (j = 0; j < N; ++j) {
             double xhat = load_as_double(x, dtype, i * N + j) * r;
             double g = load_as_double(dy, dtype, i * N + j) *
-                       load_as_double(w, dtype, j);
+                       load_as_double(w, w_dtype, j);
             dx_out[k * N + j] = r * (g - xhat * c);
         }
     }

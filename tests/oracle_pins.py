@@ -261,6 +261,49 @@ def pin_bf16_decoding(o):
     assert np.array_equal(y_f, y_d) and np.array_equal(r_f, r_d)
 
 
+def pin_f16_decoding(o):
+    """binary16 bit patterns decode exactly: 0x3C00 = 1, 0xC000 = -2,
+    0x0001 = 2^-24 (smallest subnormal), 0x0400 = 2^-14 (smallest normal),
+    0x7BFF = 65504 (largest finite); every pattern agrees with numpy's
+    float16 conversion, and fp16 input gives the same outputs as the same
+    values in fp64."""
+    bits = np.array([[0x3C00, 0xC000, 0x3555, 0x0001, 0x7BFF, 0x0400, 0x8001, 0x3FFF]],
+                    dtype=np.uint16)
+    vals = bits.view(np.float16).astype(np.float64)
+    assert vals[0, 0] == 1.0 and vals[0, 1] == -2.0 and vals[0, 3] == 2.0 ** -24
+    assert vals[0, 4] == 65504.0 and vals[0, 5] == 2.0 ** -14 and vals[0, 6] == -(2.0 ** -24)
+    w = np.ones(8)
+    y_h, r_h = o.fwd(bits.view(np.float16), w, 1e-5)
+    y_d, r_d = o.fwd(vals, w, 1e-5)
+    assert np.array_equal(y_h, y_d) and np.array_equal(r_h, r_d), (y_h, y_d)
+    every = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16).reshape(256, 256)
+    finite = np.isfinite(every.view(np.float16))
+    y_all, r_all = o.fwd(every.view(np.float16), np.ones(256), 1.0)
+    x_all = every.view(np.float16).astype(np.float64)
+    rows_ok = finite.all(axis=1)
+    y_ref = x_all[rows_ok] * r_all[rows_ok][:, None]
+    assert np.array_equal(y_all[rows_ok], y_ref)
+
+
+def pin_mixed_weight_dtype(o):
+    """A weight stored in its own type (an fp32 master weight with bf16 or
+    fp16 activations, "What a tuned RMSNorm kernel actually costs on Hopper",
+    section 07) gives exactly what the same values give in fp64."""
+    import torch
+
+    g = torch.Generator().manual_seed(50)
+    for act in (torch.bfloat16, torch.float16):
+        x = torch.randn(3, 16, generator=g).to(act)
+        dy = torch.randn(3, 16, generator=g).to(act)
+        w = (1.0 + 0.1 * torch.randn(16, generator=g)).float()
+        y1, r1 = o.fwd(x, w, 1e-5)
+        y2, r2 = o.fwd(x.double(), w.double(), 1e-5)
+        assert np.array_equal(y1, y2) and np.array_equal(r1, r2)
+        dx1 = o.bwd_dx(x, w, dy, 1e-5)
+        dx2 = o.bwd_dx(x.double(), w.double(), dy.double(), 1e-5)
+        assert np.array_equal(dx1, dx2)
+
+
 def pin_row_selection(o):
     """A requested row list returns exactly those rows, in the order given."""
     x = _rows(6, 5, 40)
@@ -293,5 +336,7 @@ ALL_PINS = [
     pin_finite_differences,
     pin_torch_rms_norm,
     pin_bf16_decoding,
+    pin_f16_decoding,
+    pin_mixed_weight_dtype,
     pin_row_selection,
 ]

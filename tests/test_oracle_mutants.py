@@ -23,22 +23,26 @@ MUTANTS = [
     ("mean_over_padded_width", "sum_sq / (double)N", "sum_sq / (double)(N + 1)", None),
     ("no_square_root", "1.0 / sqrt(", "1.0 / (", None),
     ("sum_not_squared", "sum_sq += v * v;", "sum_sq += v;", None),
-    ("fwd_weight_by_row", "load_as_double(w, dtype, j);\n    }\n    return ORACLE_OK;",
-     "load_as_double(w, dtype, i);\n    }\n    return ORACLE_OK;", None),
-    ("fwd_weight_dropped", "* r *\n                                   load_as_double(w, dtype, j);",
+    ("fwd_weight_by_row", "load_as_double(w, w_dtype, j);\n    }\n    return ORACLE_OK;",
+     "load_as_double(w, w_dtype, i);\n    }\n    return ORACLE_OK;", None),
+    ("fwd_weight_dropped", "* r *\n                                   load_as_double(w, w_dtype, j);",
      "* r;", None),
+    ("fwd_weight_decoded_as_x", "load_as_double(w, w_dtype, j);\n    }\n    return ORACLE_OK;",
+     "load_as_double(w, dtype, j);\n    }\n    return ORACLE_OK;", None),
     ("dx_sign_flipped", "r * (g - xhat * c)", "r * (g + xhat * c)", None),
     ("dx_correction_dropped", "r * (g - xhat * c)", "r * g", None),
     ("dx_outer_r_dropped", "r * (g - xhat * c)", "(g - xhat * c)", None),
     ("dx_mean_not_divided", "c /= (double)N;", "", None),
     ("dx_gain_dropped", "double g = load_as_double(dy, dtype, i * N + j) *\n"
-                        "                       load_as_double(w, dtype, j);\n"
+                        "                       load_as_double(w, w_dtype, j);\n"
                         "            dx_out", "double g = load_as_double(dy, dtype, i * N + j);\n"
                                             "            dx_out", None),
     ("dx_x_for_dy", "double g = load_as_double(dy, dtype, i * N + j) *\n"
-                    "                       load_as_double(w, dtype, j);\n            c +=",
+                    "                       load_as_double(w, w_dtype, j);\n            c +=",
      "double g = load_as_double(x, dtype, i * N + j) *\n"
-     "                       load_as_double(w, dtype, j);\n            c +=", None),
+     "                       load_as_double(w, w_dtype, j);\n            c +=", None),
+    ("dx_weight_decoded_as_x", "load_as_double(w, w_dtype, j);\n            dx_out",
+     "load_as_double(w, dtype, j);\n            dx_out", None),
     ("dw_extra_r", "dw_out[j] += load_as_double(dy, dtype, i * N + j) * xhat;",
      "dw_out[j] += load_as_double(dy, dtype, i * N + j) * xhat * r;", None),
     ("dw_x_for_dy", "dw_out[j] += load_as_double(dy,", "dw_out[j] += load_as_double(x,", None),
@@ -46,6 +50,11 @@ MUTANTS = [
     ("dw_transposed_index", "dw_out[j] += load_as_double(dy, dtype, i * N + j)",
      "dw_out[j] += load_as_double(dy, dtype, j * M + i)", None),
     ("bf16_wrong_shift", "<< 16;", "<< 15;", None),
+    ("f16_wrong_bias", "ldexp(1.0 + (double)m / 1024.0, e - 15)",
+     "ldexp(1.0 + (double)m / 1024.0, e - 16)", None),
+    ("f16_subnormal_scale", "ldexp((double)m, -24)", "ldexp((double)m, -25)", None),
+    ("f16_sign_dropped", "return sign ? -v : v;", "return v;", None),
+    ("f16_implicit_one_dropped", "ldexp(1.0 + (double)m / 1024.0", "ldexp((double)m / 1024.0", None),
     ("row_selection_ignored", "return rows ? rows[k] : k;", "return k;", None),
 ]
 
