@@ -20,9 +20,12 @@
  *   - Tensors are caller-owned DEVICE memory on the current CUDA device,
  *     contiguous and row-major: x, y, dy, dx are M x N (row stride N), w is
  *     N, rstd is M, dw is N. The library keeps no pointer after a call.
- *   - `dtype` is the element type of x, w, y, dy and dx (one type for all
- *     five): RMSNORM_F32 or RMSNORM_BF16. rstd and dw are always fp32.
- *     Arithmetic is fp32; each 16-bit output is rounded once, to nearest.
+ *   - `dtype` names the element types (rmsnorm_dtype_t): x, y, dy and dx
+ *     share one activation type (fp32, bf16 or fp16); w has that type too,
+ *     or fp32 with 16-bit activations (an fp32 master weight, "What a tuned
+ *     RMSNorm kernel actually costs on Hopper", section 07). rstd and dw are
+ *     always fp32. Arithmetic is fp32; each 16-bit output is rounded once,
+ *     to nearest even (fp16 results beyond 65504 become infinities).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream);
  *     results are valid once the stream has reached the call.
  *   - Return value is an rmsnorm_status_t. Arguments are checked before any
@@ -54,8 +57,11 @@ extern "C" {
 #endif
 
 typedef enum {
-    RMSNORM_F32 = 0,
-    RMSNORM_BF16 = 1
+    RMSNORM_F32 = 0,        /* x, y, dy, dx, w: fp32 */
+    RMSNORM_BF16 = 1,       /* x, y, dy, dx, w: bf16 */
+    RMSNORM_F16 = 2,        /* x, y, dy, dx, w: fp16 (IEEE binary16) */
+    RMSNORM_BF16_W_F32 = 3, /* x, y, dy, dx: bf16; w: fp32 */
+    RMSNORM_F16_W_F32 = 4   /* x, y, dy, dx: fp16; w: fp32 */
 } rmsnorm_dtype_t;
 
 typedef enum {
@@ -139,7 +145,8 @@ int rmsnorm_bwd_ws(const void *x, const void *w, const void *dy,
  *     so nothing needs clearing). Calls that overlap on the GPU race on it:
  *     order them, e.g. on one stream.
  *   - Arguments, outputs and other errors as rmsnorm_bwd; its bounded waits
- *     use the default one-second limit.
+ *     use the default one-second limit. dtype is RMSNORM_F32 or
+ *     RMSNORM_BF16 only: other codes return RMSNORM_ERR_INVALID_ARG.
  */
 int rmsnorm_bwd_noalloc(const void *x, const void *w, const void *dy,
                         const float *rstd, void *dx, float *dw,

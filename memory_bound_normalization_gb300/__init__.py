@@ -10,6 +10,7 @@ from __future__ import annotations
 
 from ._lib import (  # noqa: F401
     BF16,
+    BF16_W_F32,
     ERR_CUDA,
     ERR_DEVICE_TIMEOUT,
     ERR_INVALID_ARG,
@@ -17,6 +18,8 @@ from ._lib import (  # noqa: F401
     ERR_NOMEM,
     ERR_UNSUPPORTED,
     EXPORTS,
+    F16,
+    F16_W_F32,
     F32,
     OK,
     PASS_BWD,
@@ -48,15 +51,21 @@ from ._lib import (  # noqa: F401
 __version__ = "0.1.0"
 
 
-def dtype_code(torch_dtype) -> int:
-    """C-ABI dtype code of a torch dtype (float32 or bfloat16)."""
+def dtype_code(torch_dtype, w_dtype=None) -> int:
+    """C-ABI dtype code of an activation dtype (float32, bfloat16 or float16)
+    and a weight dtype (None or the same dtype, or float32 with 16-bit
+    activations)."""
     import torch
 
-    if torch_dtype == torch.bfloat16:
-        return BF16
-    if torch_dtype == torch.float32:
-        return F32
-    raise RMSNormError(ERR_INVALID_ARG, f"unsupported dtype {torch_dtype}")
+    same = w_dtype is None or w_dtype == torch_dtype
+    codes = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+    if torch_dtype in codes and same:
+        return codes[torch_dtype]
+    if w_dtype == torch.float32 and torch_dtype == torch.bfloat16:
+        return BF16_W_F32
+    if w_dtype == torch.float32 and torch_dtype == torch.float16:
+        return F16_W_F32
+    raise RMSNormError(ERR_INVALID_ARG, f"unsupported dtypes x={torch_dtype} w={w_dtype}")
 
 
 def forward(x, w, eps: float = 1e-6, stream=None):
@@ -67,7 +76,8 @@ def forward(x, w, eps: float = 1e-6, stream=None):
     M = x.numel() // N if N else 0
     y = torch.empty_like(x)
     rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    check(rmsnorm_fwd(x, w, y, rstd, M, N, eps, dtype_code(x.dtype), stream), "rmsnorm_fwd")
+    check(rmsnorm_fwd(x, w, y, rstd, M, N, eps, dtype_code(x.dtype, w.dtype), stream),
+          "rmsnorm_fwd")
     return y, rstd
 
 
@@ -79,5 +89,6 @@ def backward(x, w, dy, rstd, stream=None):
     M = x.numel() // N if N else 0
     dx = torch.empty_like(x)
     dw = torch.empty((N,), dtype=torch.float32, device=x.device)
-    check(rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, dtype_code(x.dtype), stream), "rmsnorm_bwd")
+    check(rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, dtype_code(x.dtype, w.dtype), stream),
+          "rmsnorm_bwd")
     return dx, dw

@@ -19,6 +19,9 @@ from . import build as _build
 
 F32 = 0
 BF16 = 1
+F16 = 2
+BF16_W_F32 = 3  # bf16 activations, fp32 weight
+F16_W_F32 = 4  # fp16 activations, fp32 weight
 
 OK = 0
 ERR_INVALID_ARG = 1

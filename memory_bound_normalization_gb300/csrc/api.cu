@@ -39,7 +39,7 @@ int cuda_status(cudaError_t e) {
 
 int shape_status(int64_t M, int64_t N, int dtype) {
     if (M < 0 || N <= 0 || N > INT32_MAX) return RMSNORM_ERR_INVALID_ARG;
-    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16) return RMSNORM_ERR_INVALID_ARG;
+    if (!dtype_known(dtype)) return RMSNORM_ERR_INVALID_ARG;
     return RMSNORM_OK;
 }
 
@@ -64,12 +64,12 @@ int bwd_prepare(const void* x, const void* w, const void* dy, const float* rstd,
         return RMSNORM_OK;
     }
     if (!x || !w || !dy || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
-    const int sz = dtype_size(dtype);
-    if (!aligned(x, sz) || !aligned(w, sz) || !aligned(dy, sz) || !aligned(dx, sz) ||
+    const int sz = dtype_size(dtype), wsz = weight_size(dtype);
+    if (!aligned(x, sz) || !aligned(w, wsz) || !aligned(dy, sz) || !aligned(dx, sz) ||
         !aligned(rstd, 4) || !aligned(dw, 4))
         return RMSNORM_ERR_MISALIGNED;
     const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(dy, 16) && aligned(dx, 16) &&
-                     (N * sz) % 16 == 0;
+                     (N * sz) % 16 == 0 && (N * wsz) % 16 == 0;
     bwd_choose(N, dtype, vec, plan);
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
@@ -135,10 +135,11 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     if (!(eps >= 0.f)) return RMSNORM_ERR_INVALID_ARG;  // negative or NaN
     if (M == 0) return RMSNORM_OK;
     if (!x || !w || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;
-    const int sz = dtype_size(dtype);
-    if (!aligned(x, sz) || !aligned(w, sz) || !aligned(y, sz) || !aligned(rstd, 4))
+    const int sz = dtype_size(dtype), wsz = weight_size(dtype);
+    if (!aligned(x, sz) || !aligned(w, wsz) || !aligned(y, sz) || !aligned(rstd, 4))
         return RMSNORM_ERR_MISALIGNED;
-    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(y, 16) && (N * sz) % 16 == 0;
+    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(y, 16) && (N * sz) % 16 == 0 &&
+                     (N * wsz) % 16 == 0;
     rmsnorm_plan_t plan;
     fwd_choose(N, dtype, vec, &plan);
     const DeviceInfo* dev = nullptr;

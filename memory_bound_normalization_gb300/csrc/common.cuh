@@ -1,12 +1,15 @@
-// Device helpers shared by the RMSNorm kernels: 16-byte packing of bf16/fp32
-// rows, warp reductions, and inline-PTX wrappers for mbarriers, 1-D bulk
+// Device helpers shared by the RMSNorm kernels: 16-byte packing of
+// fp32/bf16/fp16 rows and of weights stored in their own type, warp reductions, and inline-PTX wrappers for mbarriers, 1-D bulk
 // copies (cp.async.bulk, no tensor map), thread-block clusters and the
 // global timer used by the bounded waits.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace rmsn {
 
@@ -87,6 +90,70 @@ struct Pack<__nv_bfloat16> {
     }
     __device__ __forceinline__ static __nv_bfloat16 from_float(float v) {
         return __float2bfloat16_rn(v);
+    }
+};
+
+template <>
+struct Pack<__half> {
+    static constexpr int VEC = 8;
+    static constexpr int PAIRS = 4;
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    // one f16x2 word -> one float2 (low half is the lower-addressed element)
+    __device__ __forceinline__ static float2 word_to_f2(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+    __device__ __forceinline__ static void unpack2(const uint4& v, float2 (&f)[PAIRS]) {
+        f[0] = word_to_f2(v.x);
+        f[1] = word_to_f2(v.y);
+        f[2] = word_to_f2(v.z);
+        f[3] = word_to_f2(v.w);
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2 (&f)[PAIRS]) {
+        return make_uint4(pack2(f[0].x, f[0].y), pack2(f[1].x, f[1].y), pack2(f[2].x, f[2].y),
+                          pack2(f[3].x, f[3].y));
+    }
+    __device__ __forceinline__ static float to_float(__half v) { return __half2float(v); }
+    __device__ __forceinline__ static __half from_float(float v) { return __float2half_rn(v); }
+};
+
+// Scalar widening of any stored element type.
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+
+// The weights that go with one 16-byte activation vector of T, stored as TW:
+// WORDS 16-byte words (one when TW is T; two for an fp32 weight with 16-bit
+// activations), unpacked into the same float2 pairs as the activations.
+template <typename T, typename TW>
+struct WPack {
+    static constexpr int VEC = Pack<T>::VEC;
+    static constexpr int PAIRS = Pack<T>::PAIRS;
+    static constexpr int WORDS = VEC * static_cast<int>(sizeof(TW)) / 16;
+    static_assert(std::is_same<T, TW>::value || std::is_same<TW, float>::value,
+                  "the weight has the activation type or fp32");
+    // weights of activation vector k (elements k*VEC .. k*VEC+VEC-1)
+    __device__ __forceinline__ static void load(const TW* w, int64_t k, uint4 (&o)[WORDS]) {
+        const uint4* p = reinterpret_cast<const uint4*>(w + k * VEC);
+#pragma unroll
+        for (int q = 0; q < WORDS; ++q) o[q] = __ldg(p + q);
+    }
+    __device__ __forceinline__ static void zero(uint4 (&o)[WORDS]) {
+#pragma unroll
+        for (int q = 0; q < WORDS; ++q) o[q] = make_uint4(0, 0, 0, 0);
+    }
+    __device__ __forceinline__ static void unpack2(const uint4 (&o)[WORDS], float2 (&f)[PAIRS]) {
+        if constexpr (std::is_same<T, TW>::value) {
+            Pack<T>::unpack2(o[0], f);
+        } else {
+#pragma unroll
+            for (int q = 0; q < WORDS; ++q) {
+                f[2 * q] = make_float2(__uint_as_float(o[q].x), __uint_as_float(o[q].y));
+                f[2 * q + 1] = make_float2(__uint_as_float(o[q].z), __uint_as_float(o[q].w));
+            }
+        }
     }
 };
 

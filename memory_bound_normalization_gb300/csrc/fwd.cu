@@ -28,9 +28,9 @@ namespace {
 // ---------------------------------------------------------------- short rows
 // Block = threads/G groups; group g handles rows tile + r*groups + g for
 // r < R, so at each r the block touches consecutive rows.
-template <typename T, int G, int V, int R>
+template <typename T, typename TW, int G, int V, int R>
 __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__ x,
-                                                           const T* __restrict__ w,
+                                                           const TW* __restrict__ w,
                                                            T* __restrict__ y,
                                                            float* __restrict__ rstd, int64_t M,
                                                            int N, float eps) {
@@ -54,11 +54,13 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
                            : make_uint4(0, 0, 0, 0);
         }
     }
-    uint4 wv[V];
+    using WP = WPack<T, TW>;
+    uint4 wv[V][WP::WORDS];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int k = j * G + lane;
-        wv[j] = k < nvec ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+        if (k < nvec) WP::load(w, k, wv[j]);
+        else WP::zero(wv[j]);
     }
 
     constexpr int PR = P::PAIRS;
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
             if (k >= nvec) continue;
             float2 fx[PR], fw[PR], fy[PR];
             P::unpack2(xv[r][j], fx);
-            P::unpack2(wv[j], fw);
+            WP::unpack2(wv[j], fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
             st_global_16(y + row * N + static_cast<int64_t>(k) * VEC, P::pack2(fy));
@@ -108,9 +110,15 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
 // sums of squares are exchanged by asynchronous stores into every block's
 // shared memory (thread q writes to block q), counted as transaction bytes on
 // that block's mbarrier, and added in rank order (the same bits everywhere).
-template <typename T, int V>
-__global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
-                                                       const T* __restrict__ w,
+// An fp32 weight with 16-bit activations doubles the weight registers: that
+// instantiation is bounded to 512 threads (the ladder never gives it more),
+// which leaves it 128 registers a thread instead of 64.
+template <typename T, typename TW>
+constexpr int row_kernel_max_threads() { return std::is_same<T, TW>::value ? 1024 : 512; }
+
+template <typename T, typename TW, int V>
+__global__ void __launch_bounds__(row_kernel_max_threads<T, TW>()) fwd_row_kernel(const T* __restrict__ x,
+                                                       const TW* __restrict__ w,
                                                        T* __restrict__ y, float* __restrict__ rstd,
                                                        int64_t M, int N, float eps, int* status,
                                                        uint64_t wait_limit_ns) {
@@ -135,13 +143,15 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
         }
         cluster_arrive_relaxed();  // waited for below, after the loads
     }
-    uint4 xv[V], wv[V];
+    using WP = WPack<T, TW>;
+    uint4 xv[V], wv[V][WP::WORDS];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int k = base + j * nthr + threadIdx.x;
         const bool ok = k < nvec;
         xv[j] = ok ? ld_global_16_stream(xr + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
-        wv[j] = ok ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+        if (ok) WP::load(w, k, wv[j]);
+        else WP::zero(wv[j]);
     }
     constexpr int PR = P::PAIRS;
     float2 ss2 = make_float2(0.f, 0.f);
@@ -180,7 +190,7 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
         if (k >= nvec) continue;
         float2 fx[PR], fw[PR], fy[PR];
         P::unpack2(xv[j], fx);
-        P::unpack2(wv[j], fw);
+        WP::unpack2(wv[j], fw);
 #pragma unroll
         for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
         st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
@@ -195,12 +205,13 @@ __global__ void __launch_bounds__(1024) fwd_row_kernel(const T* __restrict__ x,
 // reads x back from L2 (evict_first: last use), scales and stores y. HBM reads
 // x once; with one or two blocks per SM the rows in flight take a few tens
 // of MB of L2, far below its size.
-template <typename T, int U>
+template <typename T, typename TW, int U>
 __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
-                                                       const T* __restrict__ w,
+                                                       const TW* __restrict__ w,
                                                        T* __restrict__ y, float* __restrict__ rstd,
                                                        int64_t M, int N, float eps) {
     using P = Pack<T>;
+    using WP = WPack<T, TW>;
     constexpr int VEC = P::VEC;
     constexpr int PR = P::PAIRS;
     __shared__ float red[2][32];
@@ -238,14 +249,15 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
         const float2 rs2 = f2_splat(rs);
         T* yr = y + row * N;
         for (int base = 0; base < nvec; base += nthr * U) {
-            uint4 v[U], wv[U];
+            uint4 v[U], wv[U][WP::WORDS];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int k = base + u * nthr + tid;
                 const bool ok = k < nvec;
                 v[u] = ok ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, last)
                           : make_uint4(0, 0, 0, 0);
-                wv[u] = ok ? ld_global_16(w + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
+                if (ok) WP::load(w, k, wv[u]);
+                else WP::zero(wv[u]);
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
                 if (k >= nvec) continue;
                 float2 fx[PR], fw[PR], fy[PR];
                 P::unpack2(v[u], fx);
-                P::unpack2(wv[u], fw);
+                WP::unpack2(wv[u], fw);
 #pragma unroll
                 for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
                 st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
@@ -266,9 +278,9 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
 // -------------------------------------------------------------------- scalar
 // Any alignment, any N: one block per row (grid-strided over rows), two
 // passes over the row with scalar loads.
-template <typename T>
+template <typename T, typename TW>
 __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x,
-                                                         const T* __restrict__ w,
+                                                         const TW* __restrict__ w,
                                                          T* __restrict__ y,
                                                          float* __restrict__ rstd, int64_t M,
                                                          int N, float eps) {
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x
         const T* xr = x + row * N;
         float ss = 0.f;
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            const float v = P::to_float(xr[j]);
+            const float v = to_f32(xr[j]);
             ss = fmaf(v, v, ss);
         }
         ss = group_allreduce<32>(ss);
@@ -291,33 +303,33 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x
         const float rs = rsqrtf(total / static_cast<float>(N) + eps);
         T* yr = y + row * N;
         for (int j = threadIdx.x; j < N; j += blockDim.x)
-            yr[j] = P::from_float(P::to_float(xr[j]) * rs * P::to_float(w[j]));
+            yr[j] = P::from_float(to_f32(xr[j]) * rs * to_f32(w[j]));
         if (threadIdx.x == 0) rstd[row] = rs;
     }
 }
 
-template <typename T, int G, int V, int R>
+template <typename T, typename TW, int G, int V, int R>
 cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
-    fwd_rowgroup_kernel<T, G, V, R><<<p.grid, p.threads, 0, s>>>(
-        static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd, a.M,
+    fwd_rowgroup_kernel<T, TW, G, V, R><<<p.grid, p.threads, 0, s>>>(
+        static_cast<const T*>(a.x), static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M,
         a.N, a.eps);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, typename TW>
 cudaError_t dispatch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     const int G = p.threads_per_row, V = p.vectors_per_thread;
-    if (G == 4 && V == 1) return launch_rowgroup<T, 4, 1, 4>(p, a, s);
-    if (G == 4 && V == 2) return launch_rowgroup<T, 4, 2, 4>(p, a, s);
-    if (G == 8 && V == 2) return launch_rowgroup<T, 8, 2, 4>(p, a, s);
-    if (G == 8 && V == 4) return launch_rowgroup<T, 8, 4, 2>(p, a, s);
-    if (G == 16 && V == 4) return launch_rowgroup<T, 16, 4, 2>(p, a, s);
-    if (G == 32 && V == 4) return launch_rowgroup<T, 32, 4, 1>(p, a, s);
-    if (G == 32 && V == 8) return launch_rowgroup<T, 32, 8, 1>(p, a, s);
+    if (G == 4 && V == 1) return launch_rowgroup<T, TW, 4, 1, 4>(p, a, s);
+    if (G == 4 && V == 2) return launch_rowgroup<T, TW, 4, 2, 4>(p, a, s);
+    if (G == 8 && V == 2) return launch_rowgroup<T, TW, 8, 2, 4>(p, a, s);
+    if (G == 8 && V == 4) return launch_rowgroup<T, TW, 8, 4, 2>(p, a, s);
+    if (G == 16 && V == 4) return launch_rowgroup<T, TW, 16, 4, 2>(p, a, s);
+    if (G == 32 && V == 4) return launch_rowgroup<T, TW, 32, 4, 1>(p, a, s);
+    if (G == 32 && V == 8) return launch_rowgroup<T, TW, 32, 8, 1>(p, a, s);
     return cudaErrorInvalidValue;
 }
 
-template <typename T, int V>
+template <typename T, typename TW, int V>
 cudaError_t launch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
@@ -333,31 +345,31 @@ cudaError_t launch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fwd_row_kernel<T, V>, static_cast<const T*>(a.x),
-                              static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
+    return cudaLaunchKernelEx(&cfg, fwd_row_kernel<T, TW, V>, static_cast<const T*>(a.x),
+                              static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
                               a.eps, a.status, a.wait_limit_ns);
 }
 
-template <typename T>
+template <typename T, typename TW>
 cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
-    return p.vectors_per_thread == 4 ? launch_row<T, 4>(p, a, s) : cudaErrorInvalidValue;
+    return p.vectors_per_thread == 4 ? launch_row<T, TW, 4>(p, a, s) : cudaErrorInvalidValue;
 }
 
-template <typename T>
+template <typename T, typename TW>
 cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     if (p.variant == RMSNORM_VARIANT_TWO_PASS) {
-        fwd_wide_kernel<T, 4><<<p.grid, p.threads, 0, s>>>(
-            static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y), a.rstd,
+        fwd_wide_kernel<T, TW, 4><<<p.grid, p.threads, 0, s>>>(
+            static_cast<const T*>(a.x), static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd,
             a.M, a.N, a.eps);
         return cudaGetLastError();
     }
     switch (p.variant) {
-        case RMSNORM_VARIANT_ROWGROUP: return dispatch_rowgroup<T>(p, a, s);
+        case RMSNORM_VARIANT_ROWGROUP: return dispatch_rowgroup<T, TW>(p, a, s);
         case RMSNORM_VARIANT_CTA_ROW:
-        case RMSNORM_VARIANT_CLUSTER_ROW: return dispatch_row<T>(p, a, s);
+        case RMSNORM_VARIANT_CLUSTER_ROW: return dispatch_row<T, TW>(p, a, s);
         case RMSNORM_VARIANT_SCALAR:
-            fwd_scalar_kernel<T><<<p.grid, p.threads, 0, s>>>(
-                static_cast<const T*>(a.x), static_cast<const T*>(a.w), static_cast<T*>(a.y),
+            fwd_scalar_kernel<T, TW><<<p.grid, p.threads, 0, s>>>(
+                static_cast<const T*>(a.x), static_cast<const TW*>(a.w), static_cast<T*>(a.y),
                 a.rstd, a.M, a.N, a.eps);
             return cudaGetLastError();
         default: return cudaErrorInvalidValue;
@@ -372,7 +384,8 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
 // RMSNORM_FWD_ROW_THREADS and RMSNORM_FWD_CLUSTER_THREADS override the
 // choices below for sweeps.
 // Measured on GB300 over the width sweep: bf16 rows do best in one block of
-// up to 512 threads and, wider, in the two-pass kernel; fp32 rows do best in
+// up to 512 threads and, wider, in the two-pass kernel (fp16 rows, the same
+// bytes per element, follow bf16); fp32 rows do best in
 // blocks of at most 256 threads, split over a cluster once the row needs
 // more (up to 8 blocks of up to 512 threads), then in the two-pass kernel.
 struct FwdTuning {
@@ -413,9 +426,10 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         return;
     }
     const FwdTuning& tu = fwd_tuning();
-    const bool bf16 = dtype == RMSNORM_BF16;
-    const int row_threads = tu.row_threads > 0 ? tu.row_threads : (bf16 ? 512 : 256);
-    const bool clusters = tu.wide >= 0 ? tu.wide == 1 : !bf16;
+    const bool half = dtype_size(dtype) == 2;  // 16-bit activations
+    const bool clusters = tu.wide >= 0 ? tu.wide == 1 : !half;
+    const int row_cap = dtype_size(dtype) == weight_size(dtype) ? 1024 : 512;
+    const int row_threads = std::min(row_cap, tu.row_threads > 0 ? tu.row_threads : (half ? 512 : 256));
     if (vector_ok && nvec <= static_cast<int64_t>(row_threads) * 4) {
         p->variant = RMSNORM_VARIANT_CTA_ROW;
         p->vectors_per_thread = 4;
@@ -477,8 +491,14 @@ cudaError_t fwd_finish_plan(const DeviceInfo& dev, int, int64_t M, rmsnorm_plan_
 
 cudaError_t fwd_launch(const rmsnorm_plan_t& p, int dtype, const FwdArgs& a, cudaStream_t s) {
     if (p.grid <= 0) return cudaSuccess;
-    if (dtype == RMSNORM_BF16) return dispatch<__nv_bfloat16>(p, a, s);
-    return dispatch<float>(p, a, s);
+    switch (dtype) {
+        case RMSNORM_BF16: return dispatch<__nv_bfloat16, __nv_bfloat16>(p, a, s);
+        case RMSNORM_F16: return dispatch<__half, __half>(p, a, s);
+        case RMSNORM_BF16_W_F32: return dispatch<__nv_bfloat16, float>(p, a, s);
+        case RMSNORM_F16_W_F32: return dispatch<__half, float>(p, a, s);
+        case RMSNORM_F32: return dispatch<float, float>(p, a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace rmsn

@@ -97,7 +97,11 @@ inline bool bwd_group_shape(int64_t nvec, GroupShape* g) {
     return true;
 }
 
-inline int dtype_size(int dtype) { return dtype == RMSNORM_BF16 ? 2 : 4; }
+inline bool dtype_known(int dtype) { return dtype >= RMSNORM_F32 && dtype <= RMSNORM_F16_W_F32; }
+// bytes of one activation element (x, y, dy, dx)
+inline int dtype_size(int dtype) { return dtype == RMSNORM_F32 ? 4 : 2; }
+// bytes of one weight element
+inline int weight_size(int dtype) { return dtype == RMSNORM_BF16 || dtype == RMSNORM_F16 ? 2 : 4; }
 inline int dtype_vec(int dtype) { return 16 / dtype_size(dtype); }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int round_up(int a, int b) { return (a + b - 1) / b * b; }

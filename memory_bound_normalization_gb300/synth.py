@@ -9,7 +9,8 @@ device, then rounded to nearest-even into the working dtype):
   x  ~ N(0, 1); optionally a fraction of entries, chosen as exactly
        round(frac * M * N) distinct positions, multiplied by 100 (outliers);
   dy ~ N(0, 1) * dy_scale;
-  w  = 1 + 0.1 * N(0, 1).
+  w  = 1 + 0.1 * N(0, 1), rounded into the weight dtype (the working dtype
+       unless the workload names another, e.g. an fp32 master weight).
 """
 from __future__ import annotations
 
@@ -33,10 +34,19 @@ class Workload:
     outlier_frac: float = 0.0
     seed_outliers: int = 0
     about: str = ""
+    w_dtype: torch.dtype | None = None  # None: the working dtype
+
+    @property
+    def weight_dtype(self) -> torch.dtype:
+        return self.dtype if self.w_dtype is None else self.w_dtype
 
     @property
     def dtype_name(self) -> str:
-        return {torch.bfloat16: "bf16", torch.float32: "f32"}[self.dtype]
+        names = {torch.bfloat16: "bf16", torch.float32: "f32", torch.float16: "f16"}
+        name = names[self.dtype]
+        if self.weight_dtype != self.dtype:
+            name += "_w" + names[self.weight_dtype]
+        return name
 
 
 def width_sweep(dtype: torch.dtype) -> list[Workload]:
@@ -54,6 +64,11 @@ SMALL = Workload("small_256x1024", 256, 1024, torch.bfloat16, 1e-6, 1, 2, 3,
                  about="256 x 1024 bf16, fits in L2")
 HIDDEN_4096 = Workload("hidden4096_16384x4096", 16384, 4096, torch.bfloat16, 1e-6, 11, 12, 13,
                        dy_scale=1e-2, about="7B-class hidden size, 4 x 4096 tokens")
+HIDDEN_4096_F16 = Workload("hidden4096_16384x4096_f16", 16384, 4096, torch.float16, 1e-6, 11, 12,
+                           13, dy_scale=1e-2, about="hidden 4096 workload in fp16")
+HIDDEN_4096_W_F32 = Workload("hidden4096_16384x4096_bf16_wf32", 16384, 4096, torch.bfloat16, 1e-6,
+                             11, 12, 13, dy_scale=1e-2, w_dtype=torch.float32,
+                             about="hidden 4096 workload, bf16 activations, fp32 weight")
 HIDDEN_8192 = Workload("hidden8192_32768x8192_outliers", 32768, 8192, torch.bfloat16, 1e-6,
                        21, 22, 23, dy_scale=1e-2, outlier_frac=1e-3, seed_outliers=24,
                        about="70B-class hidden size, 0.1% of x scaled by 100")
@@ -61,7 +76,7 @@ QK_NORM = Workload("qknorm_1048576x128", 1048576, 128, torch.bfloat16, 1e-6, 31,
                    about="per-head QK norm: 8 x 4096 x 32 rows of head_dim 128")
 
 WORKLOADS = {w.name: w for w in
-             [SMALL, HIDDEN_4096, HIDDEN_8192, QK_NORM, *width_sweep(torch.bfloat16),
+             [SMALL, HIDDEN_4096, HIDDEN_4096_F16, HIDDEN_4096_W_F32, HIDDEN_8192, QK_NORM, *width_sweep(torch.bfloat16),
               *width_sweep(torch.float32)]}
 
 
@@ -87,7 +102,7 @@ def make_inputs(wl: Workload, device="cuda", M: int | None = None):
         dy *= wl.dy_scale
     w = 1.0 + 0.1 * torch.randn(N, generator=_gen(device, wl.seed_w), device=device,
                                 dtype=torch.float32)
-    return {"x": x.to(wl.dtype), "w": w.to(wl.dtype), "dy": dy.to(wl.dtype)}
+    return {"x": x.to(wl.dtype), "w": w.to(wl.weight_dtype), "dy": dy.to(wl.dtype)}
 
 
 def random_rows(wl: Workload, count: int, device="cuda", M: int | None = None,
@@ -97,11 +112,14 @@ def random_rows(wl: Workload, count: int, device="cuda", M: int | None = None,
     return make_inputs(dataclasses.replace(wl, M=count), device=device)
 
 
-def logical_bytes(M: int, N: int, elem: int) -> tuple[int, int]:
+def logical_bytes(M: int, N: int, elem: int, w_elem: int | None = None) -> tuple[int, int]:
     """Bytes the method must move: forward = x read + y write + w read + rstd
-    write; backward = x, dy read + dx write + w, rstd read + dw write."""
-    fwd = 2 * M * N * elem + N * elem + 4 * M
-    bwd = 3 * M * N * elem + N * elem + 4 * M + 4 * N
+    write; backward = x, dy read + dx write + w, rstd read + dw write.
+    `elem` is the activation element size, `w_elem` the weight's (default
+    `elem`)."""
+    w_elem = elem if w_elem is None else w_elem
+    fwd = 2 * M * N * elem + N * w_elem + 4 * M
+    bwd = 3 * M * N * elem + N * w_elem + 4 * M + 4 * N
     return fwd, bwd
 
 

@@ -1,6 +1,11 @@
 """Tolerances and comparison helpers for CUDA-vs-oracle parity tests.
 
 bf16 (y, dx): elementwise |err| <= 1e-2*|ref| + 1e-3.
+fp16 (y, dx): elementwise |err| <= 2^-10*|ref| + 1e-5*rms_row(ref) + 2^-24:
+    one rounding to fp16 costs at most 2^-11 relative (half an ulp, normal
+    range) plus 2^-25 absolute (subnormal range), applied to an fp32 result
+    whose own error is ~1e-6 relative to the row's terms; the bound doubles
+    the rounding terms and gives the fp32 error the fp32 margin below.
 fp32 (y, dx): 1e-5 relative, read as a per-row normwise bound
     ||err||_2 <= 1e-5 * ||ref||_2 together with an elementwise bound
     |err| <= 1e-5*|ref| + 1e-5*rms_row(ref); elementwise relative error alone
@@ -38,6 +43,13 @@ def check_rows(got, ref, dtype: torch.dtype, what: str) -> None:
         bad = err > bound
         assert not bad.any(), (
             f"{what}: {bad.sum()} of {bad.size} elements out of bf16 tolerance; "
+            f"worst err {err.max():.3g} at ref {r.flat[np.argmax(err - bound)]:.3g}")
+    elif dtype == torch.float16:
+        rms = np.sqrt(np.mean(r ** 2, axis=-1, keepdims=True))
+        bound = 2.0 ** -10 * np.abs(r) + 1e-5 * rms + 2.0 ** -24
+        bad = err > bound
+        assert not bad.any(), (
+            f"{what}: {bad.sum()} of {bad.size} elements out of fp16 tolerance; "
             f"worst err {err.max():.3g} at ref {r.flat[np.argmax(err - bound)]:.3g}")
     else:
         rms = np.sqrt(np.mean(r ** 2, axis=-1, keepdims=True))

@@ -68,7 +68,16 @@ def test_argument_checks_need_no_device(lib):
     # null tensors
     assert fwd(None, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
     assert fwd(FAKE, FAKE, FAKE, None, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
-    # misaligned element or fp32 pointers
+    for code in (-1, 5, 6):
+        assert fwd(FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, code, 0) == pkg.ERR_INVALID_ARG
+    # misaligned element or fp32 pointers; an fp32 weight must be 4-byte
+    # aligned even with 16-bit activations
+    for code in (pkg.F16, pkg.BF16_W_F32, pkg.F16_W_F32):
+        assert fwd(FAKE + 1, FAKE, FAKE, FAKE, 4, 64, 1e-6, code, 0) == pkg.ERR_MISALIGNED
+    for code in (pkg.BF16_W_F32, pkg.F16_W_F32):
+        assert fwd(FAKE, FAKE + 2, FAKE, FAKE, 4, 64, 1e-6, code, 0) == pkg.ERR_MISALIGNED
+        assert pkg.rmsnorm_bwd(FAKE, FAKE + 2, FAKE, FAKE, FAKE, FAKE, 4, 64, code, 0) == \
+            pkg.ERR_MISALIGNED
     assert fwd(FAKE + 1, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_MISALIGNED
     assert fwd(FAKE + 2, FAKE, FAKE, FAKE, 4, 64, 1e-6, F, 0) == pkg.ERR_MISALIGNED
     assert fwd(FAKE, FAKE, FAKE, FAKE + 2, 4, 64, 1e-6, B, 0) == pkg.ERR_MISALIGNED
@@ -81,10 +90,14 @@ def test_argument_checks_need_no_device(lib):
     assert bwd(FAKE, FAKE, FAKE, FAKE + 1, FAKE, FAKE, 4, 64, B, 0) == pkg.ERR_MISALIGNED
     ws = pkg.rmsnorm_bwd_ws
     assert ws(FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 64, B, None, 0, 0) == pkg.OK
-    assert ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 3, FAKE, 1 << 20, 0) == \
+    assert ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 7, FAKE, 1 << 20, 0) == \
         pkg.ERR_INVALID_ARG
     assert pkg.rmsnorm_bwd_workspace_size(0, 64, B, 0) == 0
     assert pkg.rmsnorm_bwd_workspace_size(4, 0, B, 0) == 0
+    # the no-alloc backward takes fp32 and bf16 only
+    for code in (pkg.F16, pkg.BF16_W_F32, pkg.F16_W_F32):
+        assert pkg.rmsnorm_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, code, 0) == \
+            pkg.ERR_INVALID_ARG
 
     probe = pkg.rmsnorm_probe
     assert probe(7, FAKE, FAKE, FAKE, 1024, 1, 0) == pkg.ERR_INVALID_ARG
@@ -105,12 +118,17 @@ WIDTHS = sorted({1, 2, 3, 4, 7, 8, 13, 16, 24, 32, 40, 64, 96, 100, 128, 200, 25
                  16384, 24576, 32768, 49152, 65536, 131072, 262144, 300000, 524288, 1 << 20})
 
 
-@pytest.mark.parametrize("dtype", [pkg.BF16, pkg.F32], ids=["bf16", "f32"])
+DTYPES = [pkg.BF16, pkg.F32, pkg.F16, pkg.BF16_W_F32, pkg.F16_W_F32]
+DTYPE_IDS = ["bf16", "f32", "f16", "bf16_wf32", "f16_wf32"]
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=DTYPE_IDS)
 @pytest.mark.parametrize("N", WIDTHS)
 def test_width_ladder(lib, N, dtype):
     """Every width maps to one kernel family whose slots cover the row, with
     legal block, cluster and shared-memory sizes."""
-    vec = 8 if dtype == pkg.BF16 else 4
+    vec = 4 if dtype == pkg.F32 else 8  # elements per 16-byte activation vector
+    mixed = dtype in (pkg.BF16_W_F32, pkg.F16_W_F32)
     vector_ok = (N * (16 // vec)) % 16 == 0
     for pass_ in (pkg.PASS_FWD, pkg.PASS_BWD):
         p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
@@ -133,6 +151,8 @@ def test_width_ladder(lib, N, dtype):
             assert tg * p.vectors_per_thread * p.cluster * vec >= N
             assert p.threads_per_row == tg * p.cluster
             assert 1 <= p.row_groups <= 4
+            if mixed and pass_ == pkg.PASS_FWD:
+                assert p.threads <= 512  # the fp32-weight row kernel's launch bound
         elif name == "two_pass":
             assert pass_ == pkg.PASS_FWD and N > 512 * 4 * vec
         else:

@@ -26,17 +26,22 @@ def _lib():
     yield
 
 
-CASES = [(1, 4096, torch.bfloat16), (16, 4096, torch.bfloat16), (256, 1024, torch.bfloat16),
-         (300, 128, torch.bfloat16), (64, 16384, torch.float32), (8, 65536, torch.bfloat16),
-         (33, 257, torch.float32)]
+F32 = torch.float32
+CASES = [(1, 4096, torch.bfloat16, None), (16, 4096, torch.bfloat16, None),
+         (256, 1024, torch.bfloat16, None), (300, 128, torch.bfloat16, None),
+         (64, 16384, F32, None), (8, 65536, torch.bfloat16, None), (33, 257, F32, None),
+         (64, 4096, torch.float16, None), (16, 8192, torch.bfloat16, F32),
+         (100, 128, torch.float16, F32)]
 
 
-@pytest.mark.parametrize("M,N,dtype", CASES, ids=[f"{m}x{n}-{str(d)[6:]}" for m, n, d in CASES])
-def test_graph_replay_matches_eager(M, N, dtype):
-    wl = synth.Workload(f"graph{M}x{N}", M, N, dtype, 1e-6, 61, 62, 63)
+@pytest.mark.parametrize("M,N,dtype,w_dtype", CASES,
+                         ids=[f"{m}x{n}-{str(d)[6:]}" + (f"-w{str(wd)[6:]}" if wd else "")
+                              for m, n, d, wd in CASES])
+def test_graph_replay_matches_eager(M, N, dtype, w_dtype):
+    wl = synth.Workload(f"graph{M}x{N}", M, N, dtype, 1e-6, 61, 62, 63, w_dtype=w_dtype)
     inp = synth.make_inputs(wl, device=DEV)
     x, w, dy = inp["x"], inp["w"], inp["dy"]
-    code = pkg.dtype_code(dtype)
+    code = pkg.dtype_code(dtype, w_dtype)
     y = torch.empty_like(x)
     rstd = torch.empty(M, dtype=torch.float32, device=DEV)
     dx = torch.empty_like(x)

@@ -1,7 +1,8 @@
 """CUDA library vs fp64 oracle, element by element, through the C ABI.
 
 Small shapes (the oracle finishes in seconds) cover every kernel family and
-both dtypes with several tiles and a ragged tail; the full workload sizes are
+every dtype code (fp32, bf16, fp16, and bf16/fp16 activations with an fp32
+weight) with several tiles and a ragged tail; the full workload sizes are
 checked on sampled rows (every column of >= 4096 random rows plus the first
 and last) and on the whole of dw, in the same launch configuration the
 benchmark times.
@@ -36,7 +37,7 @@ def _lib():
 def run(x, w, dy, eps):
     """fwd + bwd on the GPU through the C ABI; returns host tensors."""
     M, N = x.shape
-    code = pkg.dtype_code(x.dtype)
+    code = pkg.dtype_code(x.dtype, w.dtype)
     y = torch.empty_like(x)
     rstd = torch.empty(M, dtype=torch.float32, device=x.device)
     dx = torch.empty_like(x)
@@ -60,10 +61,16 @@ def check_all(x, w, dy, eps, y, rstd, dx, dw, rows=None):
     check_dw(dw, dw_ref)
 
 
-def inputs(M, N, dtype, seed=0, dy_scale=1.0):
+def inputs(M, N, dtype, seed=0, dy_scale=1.0, w_dtype=None):
     wl = synth.Workload(f"t{M}x{N}", M, N, dtype, 1e-5, 100 + seed, 200 + seed, 300 + seed,
-                        dy_scale=dy_scale)
+                        dy_scale=dy_scale, w_dtype=w_dtype)
     return synth.make_inputs(wl, device=DEV), wl.eps
+
+
+# (activation dtype, weight dtype) for every dtype code
+TYPES = [(torch.bfloat16, None), (torch.float32, None), (torch.float16, None),
+         (torch.bfloat16, torch.float32), (torch.float16, torch.float32)]
+TYPE_IDS = ["bf16", "f32", "f16", "bf16_wf32", "f16_wf32"]
 
 
 SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (37, 256),
@@ -71,43 +78,43 @@ SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (
           (3, 16384), (2, 32768), (2, 65536), (1, 65536), (1000, 40), (777, 96)]
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
 @pytest.mark.parametrize("M,N", SHAPES, ids=[f"{m}x{n}" for m, n in SHAPES])
-def test_small_shapes(M, N, dtype):
-    inp, eps = inputs(M, N, dtype)
+def test_small_shapes(M, N, dtype, w_dtype):
+    inp, eps = inputs(M, N, dtype, w_dtype=w_dtype)
     out = run(inp["x"], inp["w"], inp["dy"], eps)
     check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
 @pytest.mark.parametrize("N", [128, 1024, 4096, 16384])
-def test_rows_around_persistent_grid(N, dtype):
+def test_rows_around_persistent_grid(N, dtype, w_dtype):
     """M just below, at and above the persistent grid size, and a few rows
     per block, so that some blocks get one row (or tile) more than others."""
-    code = pkg.dtype_code(dtype)
+    code = pkg.dtype_code(dtype, w_dtype)
     plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_BWD, 0)
     per_unit = plan.rows_per_unit
     P = plan.partial_rows
     for M in sorted({max(1, (P - 1) * per_unit), P * per_unit, P * per_unit + 1,
                      3 * P * per_unit + per_unit // 2 + 1}):
-        inp, eps = inputs(M, N, dtype, seed=M % 7)
+        inp, eps = inputs(M, N, dtype, seed=M % 7, w_dtype=w_dtype)
         out = run(inp["x"], inp["w"], inp["dy"], eps)
         check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
 @pytest.mark.parametrize("N", [128, 4096, 4104])
-def test_unaligned_pointers(N, dtype):
+def test_unaligned_pointers(N, dtype, w_dtype):
     """Tensors starting one element past a 16-byte boundary take the scalar
     kernels and still match."""
     M = 50
-    inp, eps = inputs(M, N, dtype)
+    inp, eps = inputs(M, N, dtype, w_dtype=w_dtype)
     views = {}
     for k in ("x", "dy"):
         buf = torch.empty(M * N + 1, dtype=dtype, device=DEV)
         buf[1:].copy_(inp[k].view(-1))
         views[k] = buf[1:].view(M, N)
-    wbuf = torch.empty(N + 1, dtype=dtype, device=DEV)
+    wbuf = torch.empty(N + 1, dtype=inp["w"].dtype, device=DEV)
     wbuf[1:].copy_(inp["w"])
     w = wbuf[1:]
     assert views["x"].data_ptr() % 16 != 0
@@ -115,14 +122,15 @@ def test_unaligned_pointers(N, dtype):
     check_all(views["x"], w, views["dy"], eps, *out)
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32, torch.float16],
+                         ids=["bf16", "f32", "f16"])
 def test_worked_examples(dtype):
     """The printed examples of the hello-gpu Fused RMSNorm chapter, section
     13.1 and Figure 13.1, on the GPU (values are exact in bf16)."""
     x = torch.tensor([[3.0, 4.0]], dtype=dtype, device=DEV)
     w = torch.tensor([1.0, 1.0], dtype=dtype, device=DEV)
     y, rstd = pkg.forward(x, w, 1e-5)
-    tol = 5e-5 if dtype == torch.float32 else 4e-3
+    tol = {torch.float32: 5e-5, torch.float16: 5e-4, torch.bfloat16: 4e-3}[dtype]
     assert np.allclose(y.float().cpu().numpy()[0], [0.8485, 1.1314], atol=tol)
     assert abs(rstd.item() - 0.2828) < 5e-5
     x = torch.tensor([[3.0, 4.0, -3.0, -4.0]], dtype=dtype, device=DEV)
@@ -132,13 +140,13 @@ def test_worked_examples(dtype):
     assert abs(rstd.item() - 0.2828) < 5e-5
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
 @pytest.mark.parametrize("N", [128, 4096, 65536])
-def test_special_rows(N, dtype):
+def test_special_rows(N, dtype, w_dtype):
     """Zero rows (y = 0, rstd = eps^-1/2), a row with a NaN (propagates to
     that row only), huge values, and zero weights in some columns."""
     M = 6
-    inp, eps = inputs(M, N, dtype)
+    inp, eps = inputs(M, N, dtype, w_dtype=w_dtype)
     x, w, dy = inp["x"].clone(), inp["w"].clone(), inp["dy"]
     x[1].zero_()
     x[3, N // 3] = float("nan")
@@ -203,7 +211,9 @@ def test_workspace_entry_point():
 
 
 @pytest.mark.parametrize("wl_name", ["hidden4096_16384x4096", "qknorm_1048576x128",
-                                     "sweep_bf16_N65536", "sweep_f32_N2880"])
+                                     "sweep_bf16_N65536", "sweep_f32_N2880",
+                                     "hidden4096_16384x4096_f16",
+                                     "hidden4096_16384x4096_bf16_wf32"])
 def test_dw_bitwise_repeatable(wl_name):
     """Ten backward calls give bitwise-identical dw and dx."""
     wl = synth.WORKLOADS[wl_name]
@@ -213,11 +223,12 @@ def test_dw_bitwise_repeatable(wl_name):
     for _ in range(9):
         dx, dw = pkg.backward(inp["x"], inp["w"], inp["dy"], rstd)
         assert torch.equal(dw.view(torch.int32), dw0.view(torch.int32))
-        assert torch.equal(dx.view(torch.int16 if wl.dtype == torch.bfloat16 else torch.int32),
-                           dx0.view(torch.int16 if wl.dtype == torch.bfloat16 else torch.int32))
+        bits = torch.int32 if wl.dtype == torch.float32 else torch.int16
+        assert torch.equal(dx.view(bits), dx0.view(bits))
 
 
-FULL = ["small_256x1024", "hidden4096_16384x4096", "hidden8192_32768x8192_outliers",
+FULL = ["small_256x1024", "hidden4096_16384x4096", "hidden4096_16384x4096_f16",
+        "hidden4096_16384x4096_bf16_wf32", "hidden8192_32768x8192_outliers",
         "qknorm_1048576x128"] + [w.name for w in synth.width_sweep(torch.bfloat16)] + \
        [w.name for w in synth.width_sweep(torch.float32)]
 
