@@ -14,6 +14,10 @@ Definitions followed:
   ``xhat = x * r`` and ``dw = sum_rows dy * xhat`` -- "RMSNorm backward (almost)
   without the column reduction", sections "The backward pass" and "The naive
   kernel".
+* residual add ``h = x + res`` stored in the activation type, then the
+  forward on h; backward: the norm's input gradient at h plus the gradient
+  reaching h from elsewhere -- "Profiling, GPU utilisation and writing a
+  fused kernel", Problem 15 (the step that adds the residual to the kernel).
 
 Inputs may be numpy arrays (float64, float32, float16, or uint16 holding bf16
 bits with ``dtype="bf16"``) or CPU torch tensors (float64, float32, bfloat16,
@@ -56,7 +60,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_rmsnorm_fwd.argtypes = [p, p, i64, i64, d, i, i, p, i64, p, p]
     lib.oracle_rmsnorm_bwd_dx.argtypes = [p, p, p, i64, i64, d, i, i, p, i64, p]
     lib.oracle_rmsnorm_bwd_dw.argtypes = [p, p, i64, i64, d, i, p]
-    for f in (lib.oracle_rmsnorm_fwd, lib.oracle_rmsnorm_bwd_dx, lib.oracle_rmsnorm_bwd_dw):
+    lib.oracle_round_to_dtype.argtypes = [p, i64, i, p]
+    lib.oracle_rmsnorm_add_fwd.argtypes = [p, p, p, i64, i64, d, i, i, p, i64, p, p, p]
+    lib.oracle_rmsnorm_add_bwd_dx.argtypes = [p, p, p, p, i64, i64, d, i, i, p, i64, p]
+    for f in (lib.oracle_rmsnorm_fwd, lib.oracle_rmsnorm_bwd_dx, lib.oracle_rmsnorm_bwd_dw,
+              lib.oracle_round_to_dtype, lib.oracle_rmsnorm_add_fwd,
+              lib.oracle_rmsnorm_add_bwd_dx):
         f.restype = ctypes.c_int
     return lib
 
@@ -171,13 +180,66 @@ def _bwd_dw(lib, x, dy, eps, N=None, dtype=None):
     return dw
 
 
+def _round(lib, v, dtype: str):
+    code = {"f64": F64, "f32": F32, "bf16": BF16, "f16": F16}[dtype]
+    va = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    out = np.empty_like(va)
+    rc = lib.oracle_round_to_dtype(_ptr(va), va.size, code, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_round_to_dtype rejected its arguments ({rc})")
+    return out
+
+
+def _add_fwd(lib, x, res, w, eps, rows=None, N=None, dtype=None):
+    xa, code = _as_host_array(x, dtype)
+    sa, scode = _as_host_array(res, dtype)
+    wa, wcode = _as_host_array(w, dtype)
+    if code != scode:
+        raise TypeError("x and the residual must share a dtype")
+    M, N = _shape2(xa, N)
+    ra, nrows = _rows_arg(rows, M)
+    h = np.empty((nrows, N), dtype=np.float64)
+    y = np.empty((nrows, N), dtype=np.float64)
+    r = np.empty((nrows,), dtype=np.float64)
+    rc = lib.oracle_rmsnorm_add_fwd(_ptr(xa), _ptr(sa), _ptr(wa), M, N, float(eps), code, wcode,
+                                    _ptr(ra), nrows, _ptr(h), _ptr(y), _ptr(r))
+    if rc:
+        raise ValueError(f"oracle_rmsnorm_add_fwd rejected its arguments ({rc})")
+    return h, y, r
+
+
+def _add_bwd_dx(lib, h, w, dy, dres, eps, rows=None, N=None, dtype=None):
+    ha, code = _as_host_array(h, dtype)
+    wa, wcode = _as_host_array(w, dtype)
+    da, dcode = _as_host_array(dy, dtype)
+    ga = None
+    if dres is not None:
+        ga, gcode = _as_host_array(dres, dtype)
+        if gcode != code:
+            raise TypeError("h and dres must share a dtype")
+    if code != dcode:
+        raise TypeError("h and dy must share a dtype")
+    M, N = _shape2(ha, N)
+    ra, nrows = _rows_arg(rows, M)
+    dx = np.empty((nrows, N), dtype=np.float64)
+    rc = lib.oracle_rmsnorm_add_bwd_dx(_ptr(ha), _ptr(wa), _ptr(da), _ptr(ga), M, N, float(eps),
+                                       code, wcode, _ptr(ra), nrows, _ptr(dx))
+    if rc:
+        raise ValueError(f"oracle_rmsnorm_add_bwd_dx rejected its arguments ({rc})")
+    return dx
+
+
 class Oracle:
     """The oracle entry points bound to one compiled library: the real one by
     default, or a deliberately broken copy that the mutation tests build.
 
     ``fwd(x, w, eps, rows=None)`` returns (y[nrows, N], r[nrows]);
     ``bwd_dx(x, w, dy, eps, rows=None)`` returns dx[nrows, N];
-    ``bwd_dw(x, dy, eps)`` returns dw[N] summed over every row.
+    ``bwd_dw(x, dy, eps)`` returns dw[N] summed over every row;
+    ``round_to(v, dtype)`` rounds doubles into "f32", "bf16" or "f16" values;
+    ``add_fwd(x, res, w, eps, rows=None)`` returns (h, y, r) of the residual
+    add and norm; ``add_bwd_dx(h, w, dy, dres, eps, rows=None)`` returns the
+    gradient of x and res (dres may be None).
     """
 
     def __init__(self, lib: ctypes.CDLL | None = None):
@@ -191,6 +253,15 @@ class Oracle:
 
     def bwd_dw(self, x, dy, eps, N=None, dtype=None):
         return _bwd_dw(self.lib, x, dy, eps, N, dtype)
+
+    def round_to(self, v, dtype: str):
+        return _round(self.lib, v, dtype)
+
+    def add_fwd(self, x, res, w, eps, rows=None, N=None, dtype=None):
+        return _add_fwd(self.lib, x, res, w, eps, rows, N, dtype)
+
+    def add_bwd_dx(self, h, w, dy, dres, eps, rows=None, N=None, dtype=None):
+        return _add_bwd_dx(self.lib, h, w, dy, dres, eps, rows, N, dtype)
 
 
 def fwd(x, w, eps: float, rows=None, N: int | None = None, dtype: str | None = None):
@@ -206,3 +277,21 @@ def bwd_dx(x, w, dy, eps: float, rows=None, N: int | None = None, dtype: str | N
 def bwd_dw(x, dy, eps: float, N: int | None = None, dtype: str | None = None):
     """Weight gradient over all rows on the host. Returns dw[N] in float64."""
     return _bwd_dw(load(), x, dy, eps, N, dtype)
+
+
+def round_to(v, dtype: str):
+    """Doubles rounded (nearest even) into "f32", "bf16" or "f16" values."""
+    return _round(load(), v, dtype)
+
+
+def add_fwd(x, res, w, eps: float, rows=None, N: int | None = None, dtype: str | None = None):
+    """Residual add and forward on the host. Returns (h, y, r) in float64:
+    h = x + res as stored in x's type, y and r the forward of that h."""
+    return _add_fwd(load(), x, res, w, eps, rows, N, dtype)
+
+
+def add_bwd_dx(h, w, dy, dres, eps: float, rows=None, N: int | None = None,
+               dtype: str | None = None):
+    """Gradient of x and of the residual (they are equal) on the host: the
+    norm's input gradient at the stored sum h plus dres (None for none)."""
+    return _add_bwd_dx(load(), h, w, dy, dres, eps, rows, N, dtype)

@@ -321,6 +321,137 @@ def pin_row_selection(o):
     assert np.array_equal(y_last[0], y_all[5])
 
 
+# ------------------------------------------------- rounding and residual add
+
+def _f16_ties(rng, n):
+    """Doubles exactly halfway between adjacent finite fp16 values (both
+    signs), with the expected round-to-nearest-even result."""
+    bits = rng.integers(0, 0x7BFF, size=n, dtype=np.uint16)  # a, a+1 both finite
+    lo = bits.view(np.float16).astype(np.float64)
+    hi = (bits + 1).view(np.float16).astype(np.float64)
+    mid = (lo + hi) / 2
+    want = np.where(bits % 2 == 0, lo, hi)
+    return np.concatenate([mid, -mid]), np.concatenate([want, -want])
+
+
+def pin_rounding_matches_numpy(o):
+    """Rounding a double into fp16 or fp32 agrees with numpy's conversions
+    (IEEE 754 round to nearest even) on normal, subnormal, overflow and
+    signed-zero inputs, and every exact fp16 tie goes to the even neighbour."""
+    rng = _rng(60)
+    v = rng.standard_normal(6000) * 10.0 ** rng.uniform(-10, 6, 6000)
+    v = np.concatenate([v, [0.0, -0.0, 65504.0, 65519.99, 65520.0, -65520.0, 1e6, 2.0 ** -25,
+                            -(2.0 ** -25), 3 * 2.0 ** -26, 2.0 ** -24, 1e-30, 3.4e38, 3.5e38,
+                            -3.5e38, 1e-46, 2.0 ** -150, 3 * 2.0 ** -151]])
+    with np.errstate(over="ignore"):
+        want16 = v.astype(np.float16).astype(np.float64)
+        want32 = v.astype(np.float32).astype(np.float64)
+    got16, got32 = o.round_to(v, "f16"), o.round_to(v, "f32")
+    assert np.array_equal(got16, want16), v[got16 != want16][:5]
+    assert np.array_equal(np.signbit(got16), np.signbit(want16))
+    assert np.array_equal(got32, want32), v[got32 != want32][:5]
+    ties, want = _f16_ties(rng, 3000)
+    assert np.array_equal(o.round_to(ties, "f16"), want)
+
+
+def pin_bf16_rounding(o):
+    """bf16 rounding: float32 inputs round as torch's float32 -> bfloat16
+    conversion (nearest even); exact ties between adjacent bf16 values go to
+    the even bit pattern and a nudge either side goes to the nearer one;
+    rounding up past the largest finite bf16 gives an infinity."""
+    import torch
+
+    rng = _rng(61)
+    v32 = (rng.standard_normal(6000) * 10.0 ** rng.uniform(-30, 30, 6000)).astype(np.float32)
+    want = torch.from_numpy(v32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.round_to(v32.astype(np.float64), "bf16"), want)
+    bits = rng.integers(0, 0x7F7F, size=3000).astype(np.int16)  # a, a+1 both finite
+    lo = torch.from_numpy(bits).view(torch.bfloat16).double().numpy()
+    hi = torch.from_numpy(bits + 1).view(torch.bfloat16).double().numpy()
+    mid, gap = (lo + hi) / 2, hi - lo
+    assert np.array_equal(o.round_to(mid, "bf16"), np.where(bits % 2 == 0, lo, hi))
+    assert np.array_equal(o.round_to(mid + gap / 8, "bf16"), hi)
+    assert np.array_equal(o.round_to(mid - gap / 8, "bf16"), lo)
+    assert np.array_equal(o.round_to(-mid - gap / 8, "bf16"), -hi)
+    big = float(torch.finfo(torch.bfloat16).max)
+    half_ulp = 2.0 ** (127 - 8)
+    r = o.round_to([big, big + half_ulp * 0.99, big + half_ulp, -(big + half_ulp)], "bf16")
+    assert r[0] == big and r[1] == big and r[2] == math.inf and r[3] == -math.inf
+
+
+def pin_add_printed_example(o):
+    """hello-gpu ch. 13 section 13.1 values through the residual path: x = [1, 1]
+    plus residual [2, 3] is the printed row [3, 4], so h = [3, 4], r ~ 0.2828
+    and y ~ [0.8485, 1.1314]."""
+    c = _golden()["two_columns"]
+    p = c["printed"]
+    d = c["decimals"]
+    xr = np.array([c["x"]])
+    res = np.array([[2.0, 3.0]])
+    h, y, r = o.add_fwd(xr - res, res, np.array(c["w"]), c["eps"])
+    assert np.array_equal(h, xr)
+    assert np.allclose(np.round(y[0], d), p["y"], atol=0, rtol=0), y
+    assert round(float(r[0]), d) == p["r"], r
+
+
+def pin_add_stored_sum(o):
+    """The stored sum h equals the addition done in the stored type by numpy
+    (fp32, fp16) and torch (bf16), and y, r equal the forward of that stored
+    h: adding in the type, then normalising."""
+    import torch
+
+    rng = _rng(62)
+    M, N = 7, 33
+    a = rng.standard_normal((M, N)) * 10.0 ** rng.uniform(-3, 3, (M, N))
+    b = rng.standard_normal((M, N)) * 10.0 ** rng.uniform(-3, 3, (M, N))
+    w = 1.0 + 0.1 * rng.standard_normal(N)
+    cases = []
+    a32, b32 = a.astype(np.float32), b.astype(np.float32)
+    cases.append((a32, b32, a32 + b32))
+    with np.errstate(over="ignore"):
+        a16, b16 = a.astype(np.float16), b.astype(np.float16)
+    cases.append((a16, b16, a16 + b16))
+    ab, bb = torch.from_numpy(a32).bfloat16(), torch.from_numpy(b32).bfloat16()
+    cases.append((ab, bb, ab + bb))
+    for xx, rr, hh in cases:
+        h, y, r = o.add_fwd(xx, rr, w, 1e-5)
+        want_h = hh.double().numpy() if isinstance(hh, torch.Tensor) else hh.astype(np.float64)
+        assert np.array_equal(h, want_h)
+        y2, r2 = o.fwd(hh, w, 1e-5)
+        assert np.array_equal(y, y2) and np.array_equal(r, r2)
+
+
+def pin_add_finite_differences(o):
+    """The residual backward is the gradient of L = sum(dy * y(x + res)) +
+    sum(dres * (x + res)) with respect to x and to res (central differences
+    in float64, h = 1e-6); without dres it is the norm's gradient alone."""
+    hstep = 1e-6
+    M, N, eps = 2, 6, 1e-4
+    x, res = _rows(M, N, 63), _rows(M, N, 64)
+    w = 1.0 + 0.3 * _rng(65).standard_normal(N)
+    dy, dres = _rows(M, N, 66), _rows(M, N, 67)
+    for g_extra in (dres, None):
+        def loss(xx, rr):
+            hh, y, _ = o.add_fwd(xx, rr, w, eps)
+            extra = 0.0 if g_extra is None else float(np.sum(g_extra * hh))
+            return float(np.sum(dy * y)) + extra
+
+        h, _, _ = o.add_fwd(x, res, w, eps)
+        got = o.add_bwd_dx(h, w, dy, g_extra, eps)
+        for which in (0, 1):
+            fd = np.zeros_like(x)
+            for i in range(M):
+                for j in range(N):
+                    args_p, args_m = [x.copy(), res.copy()], [x.copy(), res.copy()]
+                    args_p[which][i, j] += hstep
+                    args_m[which][i, j] -= hstep
+                    fd[i, j] = (loss(*args_p) - loss(*args_m)) / (2 * hstep)
+            assert np.allclose(got, fd, rtol=1e-6, atol=1e-8), (which, got - fd)
+        # a row subset gives the same rows
+        sub = o.add_bwd_dx(h, w, dy, g_extra, eps, rows=[1, 0])
+        assert np.array_equal(sub, got[[1, 0]])
+
+
 ALL_PINS = [
     pin_printed_two_columns,
     pin_printed_four_columns,
@@ -339,4 +470,9 @@ ALL_PINS = [
     pin_f16_decoding,
     pin_mixed_weight_dtype,
     pin_row_selection,
+    pin_rounding_matches_numpy,
+    pin_bf16_rounding,
+    pin_add_printed_example,
+    pin_add_stored_sum,
+    pin_add_finite_differences,
 ]

@@ -56,6 +56,33 @@ MUTANTS = [
     ("f16_sign_dropped", "return sign ? -v : v;", "return v;", None),
     ("f16_implicit_one_dropped", "ldexp(1.0 + (double)m / 1024.0", "ldexp((double)m / 1024.0", None),
     ("row_selection_ignored", "return rows ? rows[k] : k;", "return k;", None),
+    ("add_sum_not_rounded",
+     "return round_to_dtype(load_as_double(x, dtype, k) + load_as_double(res, dtype, k), dtype);",
+     "return load_as_double(x, dtype, k) + load_as_double(res, dtype, k);", None),
+    ("add_residual_dropped",
+     "load_as_double(x, dtype, k) + load_as_double(res, dtype, k)",
+     "load_as_double(x, dtype, k)", None),
+    ("add_y_of_x_not_h", "y_out[k * N + j] = h * r * load_as_double(w, w_dtype, j);",
+     "y_out[k * N + j] = load_as_double(x, dtype, i * N + j) * r * load_as_double(w, w_dtype, j);",
+     None),
+    ("add_sum_sq_of_x", "double h = stored_sum(x, res, dtype, i * N + j);\n            sum_sq += h * h;",
+     "double h = load_as_double(x, dtype, i * N + j);\n            sum_sq += h * h;", None),
+    ("add_dres_dropped", "dx_out[k * N + j] += load_as_double(dres, dtype, i * N + j);",
+     "dx_out[k * N + j] += 0.0;", None),
+    ("add_dres_sign", "dx_out[k * N + j] += load_as_double(dres",
+     "dx_out[k * N + j] -= load_as_double(dres", None),
+    ("add_dres_row_index", "load_as_double(dres, dtype, i * N + j)",
+     "load_as_double(dres, dtype, k * N + j)", None),
+    ("round_ties_away", "nearbyint(v / q)", "round(v / q)", None),
+    ("round_one_bit_short", "e - (p - 1)", "e - (p - 2)", None),
+    ("round_no_subnormal_floor", "if (e < emin)\n        e = emin;", "", None),
+    ("round_no_overflow", "return copysign(INFINITY, v);", "return r;", None),
+    ("round_f16_exponent_range", "round_to_format(v, 11, -14, 15)",
+     "round_to_format(v, 11, -15, 15)", None),
+    ("round_bf16_precision", "round_to_format(v, 8, -126, 127)",
+     "round_to_format(v, 7, -126, 127)", None),
+    ("round_bf16_as_f32", "round_to_format(v, 8, -126, 127)",
+     "round_to_format(v, 24, -126, 127)", None),
 ]
 
 
