@@ -30,6 +30,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import dataclasses
 import io
 import json
 import os
@@ -57,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--op", choices=["norm", "residual"], default="norm",
+                   help="norm: rmsnorm_fwd + rmsnorm_bwd; residual: rmsnorm_add_fwd + "
+                        "rmsnorm_add_bwd with dres (residual and dres drawn like x and dy)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle budget for the cpu_baseline sample")
@@ -230,7 +234,7 @@ def run_probes(pkg, torch, nbytes: int, samples: int = 10):
     return res
 
 
-def validate(torch, x, w, dy, eps, y, rstd, dx, dw):
+def validate(torch, x, w, dy, eps, y, rstd, dx, dw, dres=None):
     """Compare against a float32 PyTorch reference on the GPU (the check
     happens before timing; the tests' rule for each dtype, with the fp32
     margins widened tenfold for a reference that is itself fp32)."""
@@ -242,7 +246,8 @@ def validate(torch, x, w, dy, eps, y, rstd, dx, dw):
     y32 = F.rms_norm(x32, (N,), w32, eps)
     y32.backward(dy.float())
     errs = {}
-    for name, got, ref in (("y", y, y32.detach()), ("dx", dx, x32.grad)):
+    dx_ref = x32.grad if dres is None else x32.grad + dres.float()
+    for name, got, ref in (("y", y, y32.detach()), ("dx", dx, dx_ref)):
         err = (got.float() - ref).abs()
         if x.dtype == torch.bfloat16:
             bad = (err > 1e-2 * ref.abs() + 1e-3).sum().item()
@@ -322,10 +327,16 @@ def run_ours(args):
     pkg.load_library()  # raises if librmsnorm.so is missing
     wl = synth.WORKLOADS[args.workload]
     M, N, eps = wl.M, wl.N, wl.eps
+    residual = args.op == "residual"
     code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
     elem = torch.empty(0, dtype=wl.dtype).element_size()
     w_elem = torch.empty(0, dtype=wl.weight_dtype).element_size()
     fwd_bytes, bwd_bytes = synth.logical_bytes(M, N, elem, w_elem)
+    if residual:
+        # the residual is read and h written in the forward; dres is read in
+        # the backward
+        fwd_bytes += 2 * M * N * elem
+        bwd_bytes += M * N * elem
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
 
@@ -334,12 +345,18 @@ def run_ours(args):
 
     # inputs, rotated over clone sets covering >= 3x L2
     base = synth.make_inputs(wl, device=f"cuda:{local}")
-    set_bytes = (base["x"].numel() + base["dy"].numel()) * elem
+    if residual:
+        more = synth.make_inputs(dataclasses.replace(wl, seed_x=wl.seed_x + 1000,
+                                                     seed_dy=wl.seed_dy + 1000),
+                                 device=f"cuda:{local}")
+        base["res"], base["dres"] = more["x"], more["dy"]
+    set_bytes = sum(v.numel() for k, v in base.items() if k != "w") * elem
     nsets = max(2, -(-3 * l2 // set_bytes))
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
     outs = []
     for _ in range(nsets):
         outs.append({"y": torch.empty_like(base["x"]), "dx": torch.empty_like(base["x"]),
+                     "h": torch.empty_like(base["x"]) if residual else None,
                      "rstd": torch.empty(M, dtype=torch.float32, device=base["x"].device),
                      "dw": torch.empty(N, dtype=torch.float32, device=base["x"].device)})
     # L2 flush between timed calls: write a 2x L2 buffer, then read another
@@ -357,10 +374,16 @@ def run_ours(args):
 
     def fwd(i):
         s, o = sets[i], outs[i]
+        if residual:
+            return pkg.rmsnorm_add_fwd(s["x"], s["res"], s["w"], o["h"], o["y"], o["rstd"], M, N,
+                                       eps, code, stream)
         return pkg.rmsnorm_fwd(s["x"], s["w"], o["y"], o["rstd"], M, N, eps, code, stream)
 
     def bwd(i):
         s, o = sets[i], outs[i]
+        if residual:
+            return pkg.rmsnorm_add_bwd(o["h"], s["w"], s["dy"], o["rstd"], s["dres"], o["dx"],
+                                       o["dw"], M, N, code, stream)
         return pkg.rmsnorm_bwd(s["x"], s["w"], s["dy"], o["rstd"], o["dx"], o["dw"], M, N, code,
                                stream)
 
@@ -373,8 +396,15 @@ def run_ours(args):
         st = pkg.rmsnorm_get_last_device_error(stream)
         pkg.check(st, "device status")
         for i in range(nsets):
-            ok, errs_i = validate(torch, sets[i]["x"], sets[i]["w"], sets[i]["dy"], eps,
-                                  outs[i]["y"], outs[i]["rstd"], outs[i]["dx"], outs[i]["dw"])
+            xin = sets[i]["x"]
+            if residual:
+                h_ref = sets[i]["x"] + sets[i]["res"]  # added in the activation type
+                if not torch.equal(outs[i]["h"], h_ref):
+                    raise SystemExit("validation failed before timing: h != x + residual")
+                xin = h_ref
+            ok, errs_i = validate(torch, xin, sets[i]["w"], sets[i]["dy"], eps,
+                                  outs[i]["y"], outs[i]["rstd"], outs[i]["dx"], outs[i]["dw"],
+                                  sets[i]["dres"] if residual else None)
             if not ok:
                 raise SystemExit(f"validation failed before timing: {json.dumps(errs_i)}")
             errs = errs if errs is not None else errs_i
@@ -442,18 +472,21 @@ def run_ours(args):
     probes_close = run_probes(pkg, torch, 1 << 30)
 
     # end to end through pinned host buffers
-    e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes)
+    e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes,
+                  residual)
     if dist is not None:
         e2e["step_ms"] = slowest_rank(dist, [e2e["step_ms"]], base["x"].device)[0]
         e2e["value"] = round(replica_throughput(world, fwd_bytes + bwd_bytes, e2e["step_ms"]), 2)
 
     small_m = None if args.no_small_m else run_small_m(pkg, torch)
     plan_f = pkg.rmsnorm_plan(M, N, code, pkg.PASS_FWD, local).as_dict()
-    plan_b = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD, local).as_dict()
+    plan_b = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD_RES if residual else pkg.PASS_BWD,
+                              local).as_dict()
     value = replica_throughput(world, fwd_bytes + bwd_bytes, step_ms)
     bwd_gbs = bwd_bytes / (bwd_mean * 1e-3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_mean * 1e-3) / 1e9
-    traffic = read_profiled_traffic("rmsnorm_bwd", wl.name, libbuild.kernel_source_hash())
+    traffic = read_profiled_traffic("rmsnorm_add_bwd" if residual else "rmsnorm_bwd", wl.name,
+                                    libbuild.kernel_source_hash())
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -468,7 +501,8 @@ def run_ours(args):
         "dtype": wl.dtype_name,
         "data": "synthetic",
         "config": {
-            "workload": wl.name, "M": M, "N": N, "eps": eps, "io_dtype": wl.dtype_name,
+            "workload": wl.name, "op": "residual add + rmsnorm" if residual else "rmsnorm",
+            "M": M, "N": N, "eps": eps, "io_dtype": wl.dtype_name,
             "accumulate": "f32", "rstd_dw_dtype": "f32", "about": wl.about,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": f"inputs rotated over {nsets} clone sets ({nsets * set_bytes >> 20} MiB, "
@@ -488,7 +522,8 @@ def run_ours(args):
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "rmsnorm_bwd (persistent kernel + fixed-order column sum, one call)",
+            "kernel": ("rmsnorm_add_bwd" if residual else "rmsnorm_bwd")
+            + " (persistent kernel + fixed-order column sum, one call)",
             "achieved": round(bwd_gbs, 1),
             "peak": peak,
             "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
@@ -509,7 +544,7 @@ def run_ours(args):
                     "bwd_kernel_hash": libbuild.kernel_source_hash(),
                     "version": pkg.rmsnorm_version()},
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not residual:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if dist is not None:
         dist.destroy_process_group()
@@ -565,29 +600,37 @@ def run_small_m(pkg, torch, steps: int = 200):
     return out
 
 
-def run_e2e(pkg, torch, wl, base, code, stream, steps, logical):
+def run_e2e(pkg, torch, wl, base, code, stream, steps, logical, residual=False):
     """Same work through the C ABI with the inputs in pinned host memory: each
-    step copies x, w, dy to the device, runs forward and backward, and copies
-    y, rstd, dx, dw back."""
+    step copies x, w, dy (and the residual and dres) to the device, runs
+    forward and backward, and copies y, rstd, dx, dw (and h) back."""
     M, N, eps = wl.M, wl.N, wl.eps
-    hx = base["x"].cpu().pin_memory()
-    hw = base["w"].cpu().pin_memory()
-    hdy = base["dy"].cpu().pin_memory()
-    dx_in, dw_in, ddy_in = torch.empty_like(base["x"]), torch.empty_like(base["w"]), \
-        torch.empty_like(base["dy"])
+    names = ["x", "w", "dy"] + (["res", "dres"] if residual else [])
+    host = {k: base[k].cpu().pin_memory() for k in names}
+    dev = {k: torch.empty_like(base[k]) for k in names}
     y, dx = torch.empty_like(base["x"]), torch.empty_like(base["x"])
+    h = torch.empty_like(base["x"]) if residual else None
     rstd = torch.empty(M, dtype=torch.float32, device=base["x"].device)
     dw = torch.empty(N, dtype=torch.float32, device=base["x"].device)
+    hx = host["x"]
     hy, hdx = torch.empty_like(hx).pin_memory(), torch.empty_like(hx).pin_memory()
+    hh = torch.empty_like(hx).pin_memory() if residual else None
     hr = torch.empty(M, dtype=torch.float32).pin_memory()
     hdw = torch.empty(N, dtype=torch.float32).pin_memory()
 
     def step():
-        dx_in.copy_(hx, non_blocking=True)
-        dw_in.copy_(hw, non_blocking=True)
-        ddy_in.copy_(hdy, non_blocking=True)
-        pkg.check(pkg.rmsnorm_fwd(dx_in, dw_in, y, rstd, M, N, eps, code, stream))
-        pkg.check(pkg.rmsnorm_bwd(dx_in, dw_in, ddy_in, rstd, dx, dw, M, N, code, stream))
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        if residual:
+            pkg.check(pkg.rmsnorm_add_fwd(dev["x"], dev["res"], dev["w"], h, y, rstd, M, N, eps,
+                                          code, stream))
+            pkg.check(pkg.rmsnorm_add_bwd(h, dev["w"], dev["dy"], rstd, dev["dres"], dx, dw, M,
+                                          N, code, stream))
+            hh.copy_(h, non_blocking=True)
+        else:
+            pkg.check(pkg.rmsnorm_fwd(dev["x"], dev["w"], y, rstd, M, N, eps, code, stream))
+            pkg.check(pkg.rmsnorm_bwd(dev["x"], dev["w"], dev["dy"], rstd, dx, dw, M, N, code,
+                                      stream))
         hy.copy_(y, non_blocking=True)
         hr.copy_(rstd, non_blocking=True)
         hdx.copy_(dx, non_blocking=True)
@@ -603,9 +646,10 @@ def run_e2e(pkg, torch, wl, base, code, stream, steps, logical):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = event_ms(e0, e1) / steps
-    elem = hx.element_size()
-    h2d = (hx.numel() + hdy.numel()) * elem + hw.numel() * hw.element_size()
-    d2h = (hy.numel() + hdx.numel()) * elem + hr.numel() * 4 + hdw.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hr, hdw))
+    if residual:
+        d2h += hh.numel() * hh.element_size()
     return {"value": round(logical / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "step_ms": round(ms, 4), "steps": steps}

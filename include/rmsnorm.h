@@ -39,7 +39,7 @@
  *     N * element size a multiple of 16 take the vectorised kernels; any
  *     other aligned input takes a scalar kernel that gives the same results
  *     within rounding. A failed launch returns RMSNORM_ERR_CUDA.
- *   - No output may alias an input.
+ *   - No output may alias an input, except where an entry point says so.
  *   - Results are deterministic: the same inputs, shapes, dtype, device
  *     model and pointer-alignment class give bitwise-identical outputs,
  *     dw included (fixed reduction trees, no floating-point atomics).
@@ -121,6 +121,36 @@ int rmsnorm_bwd_ws(const void *x, const void *w, const void *dy,
                    cudaStream_t stream);
 
 /*
+ * Residual add fused into the forward: h = x + residual, rounded once into
+ * the activation type and written to h [M,N]; then y [M,N] and rstd [M] as
+ * rmsnorm_fwd computes them from that stored h (so the result equals adding
+ * in the activation type and calling rmsnorm_fwd on the sum). Reads x,
+ * residual (both [M,N], activation type) and w; h may be the residual or
+ * the x buffer (the sum is written in place). One kernel launch. Source:
+ * "Profiling, GPU utilisation and writing a fused kernel", Problem 15 (the
+ * kernel takes a residual tensor, writes the sum back and normalises it;
+ * the text calls this fusion the bigger win in a real model). Arguments and
+ * errors as rmsnorm_fwd; residual and h follow x's rules.
+ */
+int rmsnorm_add_fwd(const void *x, const void *residual, const void *w,
+                    void *h, void *y, float *rstd, int64_t M, int64_t N,
+                    float eps, int dtype, cudaStream_t stream);
+
+/*
+ * Backward of rmsnorm_add_fwd. Reads h (the sum the forward wrote), w, dy,
+ * rstd and, unless NULL, dres [M,N] (activation type): the gradient that
+ * reaches h from its other uses, e.g. the next residual add. Writes
+ * dx = (the norm's input gradient at h) + dres, which is the gradient of
+ * both x and residual, since h = x + residual; and dw (fp32) as rmsnorm_bwd
+ * does for input h. dx may be the dres buffer (accumulated in place). With
+ * dres NULL this is rmsnorm_bwd on h. Workspace, arguments and errors as
+ * rmsnorm_bwd; dres follows dy's rules.
+ */
+int rmsnorm_add_bwd(const void *h, const void *w, const void *dy,
+                    const float *rstd, const void *dres, void *dx, float *dw,
+                    int64_t M, int64_t N, int dtype, cudaStream_t stream);
+
+/*
  * Size of the fixed scratch array used by rmsnorm_bwd_noalloc (16 MiB per
  * device that loads the library, held until the process exits).
  */
@@ -151,6 +181,29 @@ int rmsnorm_bwd_ws(const void *x, const void *w, const void *dy,
 int rmsnorm_bwd_noalloc(const void *x, const void *w, const void *dy,
                         const float *rstd, void *dx, float *dw,
                         int64_t M, int64_t N, int dtype, cudaStream_t stream);
+
+/*
+ * The naive backward, kept as an ablation to measure what the persistent
+ * rmsnorm_bwd saves on the same GPU. Structure of "RMSNorm backward (almost)
+ * without the column reduction", section "The naive kernel": three kernels
+ * -- one block per row (one 16-byte vector per thread) recomputes rstd from
+ * x and eps, writes dx and an M x N intermediate of per-element weight
+ * gradient contributions dy*x*rstd rounded into the activation type; a
+ * column pass sums contiguous row chunks into 64 fp32 partial rows; the
+ * fixed-order column sum gives dw. About five passes over the tensor instead
+ * of three, and dw carries one rounding per contribution into the
+ * activation type (less accurate than rmsnorm_bwd's).
+ * Reads x, w, dy [M,N]; writes dx [M,N] and dw [N] (fp32); eps as in
+ * rmsnorm_fwd (no rstd input). Workspace (M*N elements plus 64*N floats)
+ * from the stream-ordered allocator (RMSNORM_ERR_NOMEM if that fails).
+ * Vector rows only: 16-byte aligned pointers, N * element size a multiple
+ * of 16 and at most 16 KiB (one block of at most 1024 threads per row), and
+ * M < 2^31; other shapes return RMSNORM_ERR_UNSUPPORTED. Other arguments and
+ * errors as rmsnorm_bwd; M == 0 sets dw to zero.
+ */
+int rmsnorm_bwd_naive(const void *x, const void *w, const void *dy,
+                      void *dx, float *dw, int64_t M, int64_t N, float eps,
+                      int dtype, cudaStream_t stream);
 
 /*
  * Device-side status. Every wait inside the kernels (on a bulk copy landing
@@ -212,8 +265,9 @@ typedef enum {
 } rmsnorm_variant_t;
 
 typedef enum {
-    RMSNORM_PASS_FWD = 0,
-    RMSNORM_PASS_BWD = 1
+    RMSNORM_PASS_FWD = 0,     /* rmsnorm_fwd and rmsnorm_add_fwd */
+    RMSNORM_PASS_BWD = 1,     /* rmsnorm_bwd, and rmsnorm_add_bwd without dres */
+    RMSNORM_PASS_BWD_RES = 2  /* rmsnorm_add_bwd with dres */
 } rmsnorm_pass_t;
 
 typedef struct {
@@ -235,8 +289,8 @@ typedef struct {
 } rmsnorm_plan_t;
 
 /*
- * Describe, without launching anything, what rmsnorm_fwd (pass 0) or
- * rmsnorm_bwd (pass 1) would run for this shape with 16-byte aligned
+ * Describe, without launching anything, what the pass named by `pass`
+ * (rmsnorm_pass_t) would run for this shape with 16-byte aligned
  * pointers. With device >= 0 the grid and workspace are filled in from
  * that device's properties (needs a GPU); with device < 0 only the
  * width-dependent choices are made (host only). Returns a status code.

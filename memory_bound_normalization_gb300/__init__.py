@@ -23,6 +23,7 @@ from ._lib import (  # noqa: F401
     F32,
     OK,
     PASS_BWD,
+    PASS_BWD_RES,
     PASS_FWD,
     PROBE_2R1W,
     PROBE_COPY,
@@ -34,7 +35,10 @@ from ._lib import (  # noqa: F401
     library_path,
     load_library,
     NOALLOC_SCRATCH_BYTES,
+    rmsnorm_add_bwd,
+    rmsnorm_add_fwd,
     rmsnorm_bwd,
+    rmsnorm_bwd_naive,
     rmsnorm_bwd_noalloc,
     rmsnorm_bwd_workspace_size,
     rmsnorm_bwd_ws,
@@ -91,4 +95,33 @@ def backward(x, w, dy, rstd, stream=None):
     dw = torch.empty((N,), dtype=torch.float32, device=x.device)
     check(rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, dtype_code(x.dtype, w.dtype), stream),
           "rmsnorm_bwd")
+    return dx, dw
+
+
+def add_forward(x, residual, w, eps: float = 1e-6, stream=None, inplace: bool = False):
+    """h, y, rstd = (x + residual, RMSNorm(x + residual), rstd); with
+    inplace=True the sum is written into `residual` and returned as h."""
+    import torch
+
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    h = residual if inplace else torch.empty_like(x)
+    y = torch.empty_like(x)
+    rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    check(rmsnorm_add_fwd(x, residual, w, h, y, rstd, M, N, eps, dtype_code(x.dtype, w.dtype),
+                          stream), "rmsnorm_add_fwd")
+    return h, y, rstd
+
+
+def add_backward(h, w, dy, rstd, dres=None, stream=None):
+    """dx, dw of the residual add + RMSNorm: dx (the gradient of x and of the
+    residual) = RMSNorm's input gradient at h plus dres."""
+    import torch
+
+    N = h.shape[-1]
+    M = h.numel() // N if N else 0
+    dx = torch.empty_like(h)
+    dw = torch.empty((N,), dtype=torch.float32, device=h.device)
+    check(rmsnorm_add_bwd(h, w, dy, rstd, dres, dx, dw, M, N, dtype_code(h.dtype, w.dtype),
+                          stream), "rmsnorm_add_bwd")
     return dx, dw

@@ -33,6 +33,7 @@ ERR_DEVICE_TIMEOUT = 6
 
 PASS_FWD = 0
 PASS_BWD = 1
+PASS_BWD_RES = 2  # rmsnorm_add_bwd with dres
 
 PROBE_COPY = 0
 PROBE_WRITE = 1
@@ -48,7 +49,10 @@ EXPORTS = (
     "rmsnorm_bwd",
     "rmsnorm_bwd_workspace_size",
     "rmsnorm_bwd_ws",
+    "rmsnorm_add_fwd",
+    "rmsnorm_add_bwd",
     "rmsnorm_bwd_noalloc",
+    "rmsnorm_bwd_naive",
     "rmsnorm_get_last_device_error",
     "rmsnorm_status_string",
     "rmsnorm_set_wait_limit_ns",
@@ -118,7 +122,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.rmsnorm_bwd_workspace_size.argtypes = [i64, i64, i, i]
         lib.rmsnorm_bwd_workspace_size.restype = sz
         lib.rmsnorm_bwd_ws.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i, vp, sz, vp]
+        lib.rmsnorm_add_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f, i, vp]
+        lib.rmsnorm_add_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i, vp]
         lib.rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i, vp]
+        lib.rmsnorm_bwd_naive.argtypes = [vp, vp, vp, vp, vp, i64, i64, f, i, vp]
         lib.rmsnorm_get_last_device_error.argtypes = [vp]
         lib.rmsnorm_status_string.argtypes = [i]
         lib.rmsnorm_status_string.restype = ctypes.c_char_p
@@ -130,7 +137,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.rmsnorm_plan.argtypes = [i64, i64, i, i, i, ctypes.POINTER(Plan)]
         lib.rmsnorm_version.argtypes = []
         lib.rmsnorm_version.restype = ctypes.c_char_p
-        for name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_ws", "rmsnorm_bwd_noalloc",
+        for name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_ws", "rmsnorm_add_fwd",
+                     "rmsnorm_add_bwd", "rmsnorm_bwd_noalloc", "rmsnorm_bwd_naive",
                      "rmsnorm_get_last_device_error",
                      "rmsnorm_probe", "rmsnorm_plan"):
             getattr(lib, name).restype = ctypes.c_int
@@ -176,6 +184,18 @@ def rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M: int, N: int, dtype: int, workspace
                                          _stream(stream))
 
 
+def rmsnorm_add_fwd(x, residual, w, h, y, rstd, M: int, N: int, eps: float, dtype: int,
+                    stream=None) -> int:
+    return load_library().rmsnorm_add_fwd(_ptr(x), _ptr(residual), _ptr(w), _ptr(h), _ptr(y),
+                                          _ptr(rstd), M, N, eps, dtype, _stream(stream))
+
+
+def rmsnorm_add_bwd(h, w, dy, rstd, dres, dx, dw, M: int, N: int, dtype: int,
+                    stream=None) -> int:
+    return load_library().rmsnorm_add_bwd(_ptr(h), _ptr(w), _ptr(dy), _ptr(rstd), _ptr(dres),
+                                          _ptr(dx), _ptr(dw), M, N, dtype, _stream(stream))
+
+
 def rmsnorm_bwd_noalloc(x, w, dy, rstd, dx, dw, M: int, N: int, dtype: int, stream=None) -> int:
     """rmsnorm_bwd without any device allocation (fixed in-library scratch),
     for callers that cannot allocate; see include/rmsnorm.h."""
@@ -184,6 +204,13 @@ def rmsnorm_bwd_noalloc(x, w, dy, rstd, dx, dw, M: int, N: int, dtype: int, stre
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def rmsnorm_bwd_naive(x, w, dy, dx, dw, M: int, N: int, eps: float, dtype: int,
+                      stream=None) -> int:
+    """The naive three-kernel backward (an ablation); see include/rmsnorm.h."""
+    return load_library().rmsnorm_bwd_naive(_ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw), M, N,
+                                            eps, dtype, _stream(stream))
 
 
 def rmsnorm_get_last_device_error(stream=None) -> int:

@@ -22,7 +22,8 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "librmsnorm.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_f32.cu", "bwd_bf16.cu", "bwd_f16.cu", "probe.cu",
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_f32.cu", "bwd_bf16.cu", "bwd_f16.cu",
+           "bwd_res_f32.cu", "bwd_res_bf16.cu", "bwd_res_f16.cu", "naive.cu", "probe.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -57,7 +58,8 @@ def source_hash() -> str:
 
 
 BWD_KERNEL_FILES = ("bwd.cu", "bwd_kernels.cuh", "bwd_f32.cu", "bwd_bf16.cu", "bwd_f16.cu",
-                    "common.cuh", "kernels.h")
+                    "bwd_res_f32.cu", "bwd_res_bf16.cu", "bwd_res_f16.cu", "common.cuh",
+                    "kernels.h")
 
 
 def kernel_source_hash(names=BWD_KERNEL_FILES) -> str:

@@ -55,7 +55,7 @@ int current_device(const DeviceInfo** out) {
 // clearing dw (M == 0).
 int bwd_prepare(const void* x, const void* w, const void* dy, const float* rstd, void* dx,
                 float* dw, int64_t M, int64_t N, int dtype, const DeviceInfo** dev,
-                rmsnorm_plan_t* plan) {
+                rmsnorm_plan_t* plan, const void* dres = nullptr) {
     int st = shape_status(M, N, dtype);
     if (st != RMSNORM_OK) return st;
     if (M == 0) {
@@ -66,19 +66,19 @@ int bwd_prepare(const void* x, const void* w, const void* dy, const float* rstd,
     if (!x || !w || !dy || !rstd || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
     const int sz = dtype_size(dtype), wsz = weight_size(dtype);
     if (!aligned(x, sz) || !aligned(w, wsz) || !aligned(dy, sz) || !aligned(dx, sz) ||
-        !aligned(rstd, 4) || !aligned(dw, 4))
+        !aligned(rstd, 4) || !aligned(dw, 4) || (dres && !aligned(dres, sz)))
         return RMSNORM_ERR_MISALIGNED;
     const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(dy, 16) && aligned(dx, 16) &&
-                     (N * sz) % 16 == 0 && (N * wsz) % 16 == 0;
+                     (!dres || aligned(dres, 16)) && (N * sz) % 16 == 0 && (N * wsz) % 16 == 0;
     bwd_choose(N, dtype, vec, plan);
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
-    return cuda_status(bwd_finish_plan(**dev, dtype, M, N, plan));
+    return cuda_status(bwd_finish_plan(**dev, dtype, M, N, plan, dres != nullptr));
 }
 
 int bwd_run(const void* x, const void* w, const void* dy, const float* rstd, void* dx, float* dw,
             int64_t M, int64_t N, int dtype, const DeviceInfo& dev, const rmsnorm_plan_t& plan,
-            void* workspace, cudaStream_t stream) {
+            void* workspace, cudaStream_t stream, const void* dres = nullptr) {
     BwdArgs a{};
     a.x = x;
     a.w = w;
@@ -92,7 +92,64 @@ int bwd_run(const void* x, const void* w, const void* dy, const float* rstd, voi
     a.status = dev.status_word;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.drop_unit = plan.variant != RMSNORM_VARIANT_SCALAR ? g_drop_unit.exchange(-1) : -1;
+    a.dres = dres;
     return cuda_status(bwd_launch(plan, dtype, a, stream));
+}
+
+// Forward checks, plan and launch shared by rmsnorm_fwd and rmsnorm_add_fwd
+// (res and h are both NULL for the plain forward).
+int fwd_run(const void* x, const void* res, const void* w, void* h, void* y, float* rstd,
+            int64_t M, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    int st = shape_status(M, N, dtype);
+    if (st != RMSNORM_OK) return st;
+    if (!(eps >= 0.f)) return RMSNORM_ERR_INVALID_ARG;  // negative or NaN
+    if (M == 0) return RMSNORM_OK;
+    const bool add = res != nullptr || h != nullptr;
+    if (!x || !w || !y || !rstd || (add && (!res || !h))) return RMSNORM_ERR_INVALID_ARG;
+    const int sz = dtype_size(dtype), wsz = weight_size(dtype);
+    if (!aligned(x, sz) || !aligned(w, wsz) || !aligned(y, sz) || !aligned(rstd, 4) ||
+        (add && (!aligned(res, sz) || !aligned(h, sz))))
+        return RMSNORM_ERR_MISALIGNED;
+    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(y, 16) && (N * sz) % 16 == 0 &&
+                     (N * wsz) % 16 == 0 && (!add || (aligned(res, 16) && aligned(h, 16)));
+    rmsnorm_plan_t plan;
+    fwd_choose(N, dtype, vec, &plan);
+    const DeviceInfo* dev = nullptr;
+    st = current_device(&dev);
+    if (st != RMSNORM_OK) return st;
+    st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan));
+    if (st != RMSNORM_OK) return st;
+    if (static_cast<int64_t>(plan.grid) <= 0 ||
+        ((plan.variant == RMSNORM_VARIANT_ROWGROUP || plan.variant == RMSNORM_VARIANT_CTA_ROW ||
+          plan.variant == RMSNORM_VARIANT_CLUSTER_ROW) &&
+         cdiv(M, plan.variant == RMSNORM_VARIANT_ROWGROUP ? plan.rows_per_unit : 1) * plan.cluster >
+             INT32_MAX))
+        return RMSNORM_ERR_UNSUPPORTED;
+    FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps, dev->status_word, g_wait_limit_ns.load(),
+              res, h};
+    return cuda_status(fwd_launch(plan, dtype, a, stream));
+}
+
+// rmsnorm_bwd and rmsnorm_add_bwd: workspace from the stream-ordered pool.
+int bwd_alloc_run(const void* x, const void* w, const void* dy, const float* rstd,
+                  const void* dres, void* dx, float* dw, int64_t M, int64_t N, int dtype,
+                  cudaStream_t stream) {
+    const DeviceInfo* dev = nullptr;
+    rmsnorm_plan_t plan;
+    int st = bwd_prepare(x, w, dy, rstd, dx, dw, M, N, dtype, &dev, &plan, dres);
+    if (st != RMSNORM_OK) return st;
+    if (M == 0) {
+        if (dw == nullptr) return RMSNORM_OK;
+        return cuda_status(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream));
+    }
+    void* ws = nullptr;
+    if (cuda_status(cudaMallocAsync(&ws, static_cast<size_t>(plan.workspace_bytes), stream)) !=
+        RMSNORM_OK)
+        return RMSNORM_ERR_NOMEM;
+    st = bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, ws, stream, dres);
+    const int freed = cuda_status(cudaFreeAsync(ws, stream));
+    if (st == RMSNORM_OK) st = freed;
+    return st;
 }
 
 }  // namespace
@@ -130,31 +187,14 @@ extern "C" {
 
 int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
                 float eps, int dtype, cudaStream_t stream) {
-    int st = shape_status(M, N, dtype);
-    if (st != RMSNORM_OK) return st;
-    if (!(eps >= 0.f)) return RMSNORM_ERR_INVALID_ARG;  // negative or NaN
-    if (M == 0) return RMSNORM_OK;
-    if (!x || !w || !y || !rstd) return RMSNORM_ERR_INVALID_ARG;
-    const int sz = dtype_size(dtype), wsz = weight_size(dtype);
-    if (!aligned(x, sz) || !aligned(w, wsz) || !aligned(y, sz) || !aligned(rstd, 4))
-        return RMSNORM_ERR_MISALIGNED;
-    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(y, 16) && (N * sz) % 16 == 0 &&
-                     (N * wsz) % 16 == 0;
-    rmsnorm_plan_t plan;
-    fwd_choose(N, dtype, vec, &plan);
-    const DeviceInfo* dev = nullptr;
-    st = current_device(&dev);
-    if (st != RMSNORM_OK) return st;
-    st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan));
-    if (st != RMSNORM_OK) return st;
-    if (static_cast<int64_t>(plan.grid) <= 0 ||
-        ((plan.variant == RMSNORM_VARIANT_ROWGROUP || plan.variant == RMSNORM_VARIANT_CTA_ROW ||
-          plan.variant == RMSNORM_VARIANT_CLUSTER_ROW) &&
-         cdiv(M, plan.variant == RMSNORM_VARIANT_ROWGROUP ? plan.rows_per_unit : 1) * plan.cluster >
-             INT32_MAX))
-        return RMSNORM_ERR_UNSUPPORTED;
-    FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps, dev->status_word, g_wait_limit_ns.load()};
-    return cuda_status(fwd_launch(plan, dtype, a, stream));
+    return fwd_run(x, nullptr, w, nullptr, y, rstd, M, N, eps, dtype, stream);
+}
+
+int rmsnorm_add_fwd(const void* x, const void* residual, const void* w, void* h, void* y,
+                    float* rstd, int64_t M, int64_t N, float eps, int dtype,
+                    cudaStream_t stream) {
+    if (M > 0 && (residual == nullptr || h == nullptr)) return RMSNORM_ERR_INVALID_ARG;
+    return fwd_run(x, residual, w, h, y, rstd, M, N, eps, dtype, stream);
 }
 
 size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype, int device) {
@@ -193,19 +233,40 @@ int rmsnorm_bwd_ws(const void* x, const void* w, const void* dy, const float* rs
 
 int rmsnorm_bwd(const void* x, const void* w, const void* dy, const float* rstd, void* dx,
                 float* dw, int64_t M, int64_t N, int dtype, cudaStream_t stream) {
-    const DeviceInfo* dev = nullptr;
-    rmsnorm_plan_t plan;
-    int st = bwd_prepare(x, w, dy, rstd, dx, dw, M, N, dtype, &dev, &plan);
+    return bwd_alloc_run(x, w, dy, rstd, nullptr, dx, dw, M, N, dtype, stream);
+}
+
+int rmsnorm_add_bwd(const void* h, const void* w, const void* dy, const float* rstd,
+                    const void* dres, void* dx, float* dw, int64_t M, int64_t N, int dtype,
+                    cudaStream_t stream) {
+    return bwd_alloc_run(h, w, dy, rstd, dres, dx, dw, M, N, dtype, stream);
+}
+
+int rmsnorm_bwd_naive(const void* x, const void* w, const void* dy, void* dx, float* dw,
+                      int64_t M, int64_t N, float eps, int dtype, cudaStream_t stream) {
+    int st = shape_status(M, N, dtype);
     if (st != RMSNORM_OK) return st;
+    if (!(eps >= 0.f)) return RMSNORM_ERR_INVALID_ARG;
+    if (dw != nullptr && !aligned(dw, 4)) return RMSNORM_ERR_MISALIGNED;
     if (M == 0) {
         if (dw == nullptr) return RMSNORM_OK;
         return cuda_status(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream));
     }
+    if (!x || !w || !dy || !dx || !dw) return RMSNORM_ERR_INVALID_ARG;
+    const int sz = dtype_size(dtype), wsz = weight_size(dtype);
+    if (!aligned(x, sz) || !aligned(w, wsz) || !aligned(dy, sz) || !aligned(dx, sz))
+        return RMSNORM_ERR_MISALIGNED;
+    const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(dy, 16) && aligned(dx, 16) &&
+                     (N * sz) % 16 == 0 && (N * wsz) % 16 == 0;
+    if (!vec || N / dtype_vec(dtype) > kNaiveMaxVectors || M > INT32_MAX)
+        return RMSNORM_ERR_UNSUPPORTED;
+    const DeviceInfo* dev = nullptr;
+    st = current_device(&dev);
+    if (st != RMSNORM_OK) return st;
     void* ws = nullptr;
-    if (cuda_status(cudaMallocAsync(&ws, static_cast<size_t>(plan.workspace_bytes), stream)) !=
-        RMSNORM_OK)
+    if (cuda_status(cudaMallocAsync(&ws, naive_workspace_bytes(M, N, dtype), stream)) != RMSNORM_OK)
         return RMSNORM_ERR_NOMEM;
-    st = bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, ws, stream);
+    st = cuda_status(naive_launch(dtype, x, w, dy, dx, dw, M, static_cast<int>(N), eps, ws, stream));
     const int freed = cuda_status(cudaFreeAsync(ws, stream));
     if (st == RMSNORM_OK) st = freed;
     return st;
@@ -263,7 +324,8 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     if (out == nullptr) return RMSNORM_ERR_INVALID_ARG;
     int st = shape_status(M, N, dtype);
     if (st != RMSNORM_OK) return st;
-    if (pass != RMSNORM_PASS_FWD && pass != RMSNORM_PASS_BWD) return RMSNORM_ERR_INVALID_ARG;
+    if (pass != RMSNORM_PASS_FWD && pass != RMSNORM_PASS_BWD && pass != RMSNORM_PASS_BWD_RES)
+        return RMSNORM_ERR_INVALID_ARG;
     if (M == 0) {
         *out = rmsnorm_plan_t{};
         return RMSNORM_OK;
@@ -277,7 +339,8 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     const DeviceInfo* dev = device_info(device);
     if (!dev) return RMSNORM_ERR_CUDA;
     cudaError_t e = pass == RMSNORM_PASS_FWD ? fwd_finish_plan(*dev, dtype, M, out)
-                                             : bwd_finish_plan(*dev, dtype, M, N, out);
+                                             : bwd_finish_plan(*dev, dtype, M, N, out,
+                                                               pass == RMSNORM_PASS_BWD_RES);
     return cuda_status(e);
 }
 

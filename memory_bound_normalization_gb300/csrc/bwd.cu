@@ -78,8 +78,18 @@ __global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ 
     }
 }
 // ------------------------------------------------------------ host side
-const void* main_kernel_for(int dtype, const rmsnorm_plan_t& p) {
+const void* main_kernel_for(int dtype, const rmsnorm_plan_t& p, bool res) {
     const bool pipe = tuning().pipelined;
+    if (res) {
+        switch (dtype) {
+            case RMSNORM_F32: return bwd_res_kernel_f32(p, pipe);
+            case RMSNORM_BF16: return bwd_res_kernel_bf16(p, pipe);
+            case RMSNORM_F16: return bwd_res_kernel_f16(p, pipe);
+            case RMSNORM_BF16_W_F32: return bwd_res_kernel_bf16_w_f32(p, pipe);
+            case RMSNORM_F16_W_F32: return bwd_res_kernel_f16_w_f32(p, pipe);
+            default: return nullptr;
+        }
+    }
     switch (dtype) {
         case RMSNORM_F32: return bwd_main_kernel_f32(p, pipe);
         case RMSNORM_BF16: return bwd_main_kernel_bf16(p, pipe);
@@ -242,9 +252,9 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
 }
 
 cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
-                            rmsnorm_plan_t* p) {
+                            rmsnorm_plan_t* p, bool res) {
     if (p->smem_bytes > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
-    const void* fn = main_kernel_for(dtype, *p);
+    const void* fn = main_kernel_for(dtype, *p, res);
     if (fn == nullptr) return cudaErrorInvalidValue;
     int units = 0;
     cudaError_t err = resident_units(dev, fn, p->threads, p->smem_bytes, p->cluster, &units);
@@ -259,9 +269,14 @@ cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t
     return cudaSuccess;
 }
 
+cudaError_t colsum_launch(const float* partial, float* dw, int P, int N, cudaStream_t s) {
+    colsum_kernel<<<static_cast<unsigned>(cdiv(N, 32)), dim3(32, 32), 0, s>>>(partial, dw, P, N);
+    return cudaGetLastError();
+}
+
 cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cudaStream_t s) {
     if (p.grid <= 0) return cudaSuccess;
-    const void* fn = main_kernel_for(dtype, p);
+    const void* fn = main_kernel_for(dtype, p, a.dres != nullptr);
     if (fn == nullptr) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));

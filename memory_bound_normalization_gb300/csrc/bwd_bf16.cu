@@ -4,11 +4,11 @@
 namespace rmsn {
 
 const void* bwd_main_kernel_bf16(const rmsnorm_plan_t& p, bool pipelined) {
-    return main_kernel<__nv_bfloat16, __nv_bfloat16>(p, pipelined);
+    return main_kernel<__nv_bfloat16, __nv_bfloat16, false>(p, pipelined);
 }
 
 const void* bwd_main_kernel_bf16_w_f32(const rmsnorm_plan_t& p, bool pipelined) {
-    return main_kernel<__nv_bfloat16, float>(p, pipelined);
+    return main_kernel<__nv_bfloat16, float, false>(p, pipelined);
 }
 
 }  // namespace rmsn

@@ -4,11 +4,11 @@
 namespace rmsn {
 
 const void* bwd_main_kernel_f16(const rmsnorm_plan_t& p, bool pipelined) {
-    return main_kernel<__half, __half>(p, pipelined);
+    return main_kernel<__half, __half, false>(p, pipelined);
 }
 
 const void* bwd_main_kernel_f16_w_f32(const rmsnorm_plan_t& p, bool pipelined) {
-    return main_kernel<__half, float>(p, pipelined);
+    return main_kernel<__half, float, false>(p, pipelined);
 }
 
 }  // namespace rmsn

@@ -4,7 +4,7 @@
 namespace rmsn {
 
 const void* bwd_main_kernel_f32(const rmsnorm_plan_t& p, bool pipelined) {
-    return main_kernel<float, float>(p, pipelined);
+    return main_kernel<float, float, false>(p, pipelined);
 }
 
 }  // namespace rmsn

@@ -27,6 +27,14 @@
 //
 // Types: T is the activation type (x, dy, dx), TW the weight type (T, or
 // fp32 with 16-bit activations). rstd, the dw partial rows and dw are fp32.
+//
+// RES (residual path): x is the stored sum h = x + res of the forward, and
+// dx = rstd*(g - xhat*c) + dres, where dres is the gradient reaching h from
+// its other uses; that dx is the gradient of both summands ("Profiling, GPU
+// utilisation and writing a fused kernel", Problem 15, the residual step).
+// dres is read in pass 2 with coherent loads (dx may be the dres buffer);
+// the thread that issues a row's bulk copies also asks L2 to prefetch that
+// row's dres, so those loads hit L2.
 #pragma once
 
 #include "common.cuh"
@@ -59,14 +67,20 @@ __host__ __device__ inline int bwd_row_smem_bytes(int groups, int stages, int un
     return groups * bwd_row_group_stride(stages, unit);
 }
 
-// Main (row) kernel of a backward plan for each element-type code. Each is
-// defined in its own translation unit, so the instantiations compile in
+// Main (row) kernel of a backward plan for each element-type code, without
+// (bwd_main_kernel_*) and with (bwd_res_kernel_*) the residual gradient. Each
+// is defined in its own translation unit, so the instantiations compile in
 // parallel; nullptr when the plan names no instantiated kernel.
 const void* bwd_main_kernel_f32(const rmsnorm_plan_t& p, bool pipelined);
 const void* bwd_main_kernel_bf16(const rmsnorm_plan_t& p, bool pipelined);
 const void* bwd_main_kernel_bf16_w_f32(const rmsnorm_plan_t& p, bool pipelined);
 const void* bwd_main_kernel_f16(const rmsnorm_plan_t& p, bool pipelined);
 const void* bwd_main_kernel_f16_w_f32(const rmsnorm_plan_t& p, bool pipelined);
+const void* bwd_res_kernel_f32(const rmsnorm_plan_t& p, bool pipelined);
+const void* bwd_res_kernel_bf16(const rmsnorm_plan_t& p, bool pipelined);
+const void* bwd_res_kernel_bf16_w_f32(const rmsnorm_plan_t& p, bool pipelined);
+const void* bwd_res_kernel_f16(const rmsnorm_plan_t& p, bool pipelined);
+const void* bwd_res_kernel_f16_w_f32(const rmsnorm_plan_t& p, bool pipelined);
 
 namespace {
 
@@ -88,7 +102,7 @@ __device__ __forceinline__ void wait_for_prerequisite_grid() {
 // P*groups: it owns rows v, v + P*groups, ..., has its own bulk-copy ring and
 // named barrier, and keeps its dw contribution in registers. At the end the
 // groups' dw are added in group order, so every block writes one partial row.
-template <typename T, typename TW, int V>
+template <typename T, typename TW, int V, bool RES>
 __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int groups) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
@@ -123,6 +137,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     const T* DY = static_cast<const T*>(a.dy);
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
+    const T* DRES = static_cast<const T*>(a.dres);
     const int bar_id = 1 + g;  // named barrier of this group (0 is __syncthreads)
 
     // rows of this group: vid, vid + nvirt, ...
@@ -150,6 +165,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
+        if constexpr (RES) bulk_prefetch_l2(DRES + off, bytes);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
@@ -244,7 +260,9 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         for (int j = 0; j < V; ++j) {
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
-            float2 fx[PR], fd[PR], fw[PR], o[PR];
+            float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
+            if constexpr (RES)
+                P::unpack2(ld_global_16_coherent(DRES + (dxr - DX) + static_cast<int64_t>(vbeg + k) * VEC), fr);
             P::unpack2(ld_shared_16(xs + k * 16), fx);
             P::unpack2(ld_shared_16(ds + k * 16), fd);
             weights(j, k, fw);
@@ -252,7 +270,10 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             for (int e = 0; e < PR; ++e) {
                 const float2 xh = __fmul2_rn(fx[e], r2);
                 const float2 gg = __fmul2_rn(fd[e], fw[e]);
-                o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
+                if constexpr (RES)
+                    o[e] = __ffma2_rn(r2, __ffma2_rn(xh, nc2, gg), fr[e]);
+                else
+                    o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
                 acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
             }
             st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(o));
@@ -326,7 +347,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
 // peer sends row r+1 only after receiving row r-1, which needs this block's
 // send of row r-1, made before this block reads the slots of row r-2; so a
 // writer is at most three rows ahead of a reader.
-template <typename T, typename TW, int V, bool PIPE>
+template <typename T, typename TW, int V, bool PIPE, bool RES>
 __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, int /*groups*/) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
@@ -360,6 +381,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     const T* DY = static_cast<const T*>(a.dy);
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
+    const T* DRES = static_cast<const T*>(a.dres);
 
     // rows of this cluster: cid, cid+ncl, ...
     const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
@@ -387,6 +409,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
+        if constexpr (RES) bulk_prefetch_l2(DRES + off, bytes);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
@@ -496,7 +519,9 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         for (int j = 0; j < V; ++j) {
             const int k = j * nthr + tid;
             if (k >= vcnt) continue;
-            float2 fx[PR], fd[PR], fw[PR], o[PR];
+            float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
+            if constexpr (RES)
+                P::unpack2(ld_global_16_coherent(DRES + (dxr - DX) + static_cast<int64_t>(vbeg + k) * VEC), fr);
             P::unpack2(ld_shared_16(xs + k * 16), fx);
             P::unpack2(ld_shared_16(ds + k * 16), fd);
             weights(j, k, fw);
@@ -504,7 +529,10 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
             for (int e = 0; e < PR; ++e) {
                 const float2 xh = __fmul2_rn(fx[e], r2);
                 const float2 gg = __fmul2_rn(fd[e], fw[e]);
-                o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
+                if constexpr (RES)
+                    o[e] = __ffma2_rn(r2, __ffma2_rn(xh, nc2, gg), fr[e]);
+                else
+                    o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
                 acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
             }
             st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(o));
@@ -581,7 +609,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
 // ---------------------------------------------------------- short rows
 // A unit is a tile of RT = (threads/G)*R consecutive rows, moved by one bulk
 // copy per tensor. Group g (G lanes) handles tile rows r*groups + g.
-template <typename T, typename TW, int G, int V, int R>
+template <typename T, typename TW, int G, int V, int R, bool RES>
 __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages, int /*groups*/) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
@@ -607,6 +635,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     const T* DY = static_cast<const T*>(a.dy);
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
+    const T* DRES = static_cast<const T*>(a.dres);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
@@ -626,6 +655,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         const int64_t off = tile * RT * N;
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
+        if constexpr (RES) bulk_prefetch_l2(DRES + off, bytes);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
@@ -722,7 +752,9 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                 const int k = j * G + lane;
                 if (k >= nvec) continue;
                 const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
-                float2 fx[PR], fd[PR], fw[PR], o[PR];
+                float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
+                if constexpr (RES)
+                    P::unpack2(ld_global_16_coherent(DRES + row * N + static_cast<int64_t>(k) * VEC), fr);
                 P::unpack2(ld_shared_16(sx + s * unit + off), fx);
                 P::unpack2(ld_shared_16(sdy + s * unit + off), fd);
                 WP::unpack2(wv[j], fw);
@@ -730,7 +762,10 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                 for (int e = 0; e < PR; ++e) {
                     const float2 xh = __fmul2_rn(fx[e], r2);
                     const float2 g = __fmul2_rn(fd[e], fw[e]);
-                    o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, g));
+                    if constexpr (RES)
+                        o[e] = __ffma2_rn(r2, __ffma2_rn(xh, nc2, g), fr[e]);
+                    else
+                        o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, g));
                     acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
                 }
                 st_global_16(DX + row * N + static_cast<int64_t>(k) * VEC, P::pack2(o));
@@ -768,7 +803,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
 // ------------------------------------------------------------------ scalar
 // Any alignment, any N. Persistent: block b owns rows b, b+P, ... and its
 // partial row, which thread t updates at columns t, t+blockDim, ... only.
-template <typename T, typename TW>
+template <typename T, typename TW, bool RES>
 __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages*/, int /*groups*/) {
     using P = Pack<T>;
     __shared__ float red[2][32];
@@ -778,6 +813,7 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
     const T* DY = static_cast<const T*>(a.dy);
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
+    const T* DRES = static_cast<const T*>(a.dres);
     float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
     for (int col = threadIdx.x; col < N; col += blockDim.x) prow[col] = 0.f;
     int it = 0;
@@ -799,55 +835,58 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
             const float d = to_f32(dyr[col]);
             const float xh = to_f32(xr[col]) * r;
             const float g = d * to_f32(W[col]);
-            dxr[col] = P::from_float(r * (g - xh * c));
+            if constexpr (RES)
+                dxr[col] = P::from_float(fmaf(r, g - xh * c, to_f32(DRES[row * N + col])));
+            else
+                dxr[col] = P::from_float(r * (g - xh * c));
             prow[col] = fmaf(d, xh, prow[col]);
         }
     }
 }
 
 // ------------------------------------------------------ kernel selection
-template <typename T, typename TW>
+template <typename T, typename TW, bool RES>
 const void* row_kernel(int V) {
     switch (V) {
-        case 1: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 1>);
-        case 2: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 2>);
-        case 4: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 4>);
-        case 8: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 8>);
+        case 1: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 1, RES>);
+        case 2: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 2, RES>);
+        case 4: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 4, RES>);
+        case 8: return reinterpret_cast<const void*>(&bwd_row_kernel<T, TW, 8, RES>);
         default: return nullptr;
     }
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool RES>
 const void* wide_kernel(int V, bool pipelined) {
-    if (V == 4) return pipelined ? reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 4, true>)
-                                 : reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 4, false>);
-    if (V == 8) return pipelined ? reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 8, true>)
-                                 : reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 8, false>);
+    if (V == 4) return pipelined ? reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 4, true, RES>)
+                                 : reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 4, false, RES>);
+    if (V == 8) return pipelined ? reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 8, true, RES>)
+                                 : reinterpret_cast<const void*>(&bwd_wide_kernel<T, TW, 8, false, RES>);
     return nullptr;
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool RES>
 const void* rowgroup_kernel(int G, int V) {
-    if (G == 4 && V == 1) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 4, 1, 4>);
-    if (G == 4 && V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 4, 2, 2>);
-    if (G == 8 && V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 8, 2, 2>);
-    if (G == 8 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 8, 4, 1>);
-    if (G == 16 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 16, 4, 1>);
-    if (G == 32 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 32, 4, 1>);
-    if (G == 32 && V == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 32, 8, 1>);
+    if (G == 4 && V == 1) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 4, 1, 4, RES>);
+    if (G == 4 && V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 4, 2, 2, RES>);
+    if (G == 8 && V == 2) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 8, 2, 2, RES>);
+    if (G == 8 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 8, 4, 1, RES>);
+    if (G == 16 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 16, 4, 1, RES>);
+    if (G == 32 && V == 4) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 32, 4, 1, RES>);
+    if (G == 32 && V == 8) return reinterpret_cast<const void*>(&bwd_rowgroup_kernel<T, TW, 32, 8, 1, RES>);
     return nullptr;
 }
 
-template <typename T, typename TW>
+template <typename T, typename TW, bool RES>
 const void* main_kernel(const rmsnorm_plan_t& p, bool pipelined) {
     switch (p.variant) {
-        case RMSNORM_VARIANT_ROWGROUP: return rowgroup_kernel<T, TW>(p.threads_per_row, p.vectors_per_thread);
+        case RMSNORM_VARIANT_ROWGROUP: return rowgroup_kernel<T, TW, RES>(p.threads_per_row, p.vectors_per_thread);
         case RMSNORM_VARIANT_CTA_ROW:
         case RMSNORM_VARIANT_CLUSTER_ROW:
             // single blocks: the grouped kernel; clusters: the pipelined one
-            return p.cluster == 1 ? row_kernel<T, TW>(p.vectors_per_thread)
-                                  : wide_kernel<T, TW>(p.vectors_per_thread, pipelined);
-        case RMSNORM_VARIANT_SCALAR: return reinterpret_cast<const void*>(&bwd_scalar_kernel<T, TW>);
+            return p.cluster == 1 ? row_kernel<T, TW, RES>(p.vectors_per_thread)
+                                  : wide_kernel<T, TW, RES>(p.vectors_per_thread, pipelined);
+        case RMSNORM_VARIANT_SCALAR: return reinterpret_cast<const void*>(&bwd_scalar_kernel<T, TW, RES>);
         default: return nullptr;
     }
 }

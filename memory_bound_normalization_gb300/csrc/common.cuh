@@ -159,6 +159,21 @@ struct WPack {
 
 __device__ __forceinline__ float2 f2_splat(float v) { return make_float2(v, v); }
 
+// a + b element by element, each sum computed in fp32 and rounded once into
+// T (for 16-bit T the fp32 sum of two T values is exact unless the two
+// exponents are far apart, and then the smaller one is below half an ulp of
+// the larger, so the result is the correctly rounded sum either way).
+template <typename T>
+__device__ __forceinline__ uint4 add_vec(const uint4& a, const uint4& b) {
+    using P = Pack<T>;
+    float2 fa[P::PAIRS], fb[P::PAIRS];
+    P::unpack2(a, fa);
+    P::unpack2(b, fb);
+#pragma unroll
+    for (int e = 0; e < P::PAIRS; ++e) fa[e] = __fadd2_rn(fa[e], fb[e]);
+    return P::pack2(fa);
+}
+
 // ------------------------------------------------------------ global memory
 __device__ __forceinline__ uint4 ld_global_16(const void* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
@@ -173,6 +188,16 @@ __device__ __forceinline__ uint4 ld_global_16_stream(const void* p) {
 }
 __device__ __forceinline__ void st_global_16(void* p, const uint4& v) {
     *reinterpret_cast<uint4*>(p) = v;
+}
+// Coherent streaming read (no read-only path) of data that may share memory
+// with one of the kernel's outputs. It is not ordered against other memory
+// accesses: the caller reads each element before any thread writes it.
+__device__ __forceinline__ uint4 ld_global_16_coherent(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 // L2 eviction-priority policies (createpolicy): evict_last keeps lines that
@@ -192,6 +217,16 @@ __device__ __forceinline__ uint4 ld_global_16_hint(const void* p, uint64_t pol) 
     asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p), "l"(pol));
+    return v;
+}
+// Coherent read with an L2 policy, ordered after this thread's earlier
+// memory accesses (it reads back what the same thread stored).
+__device__ __forceinline__ uint4 ld_global_16_coherent_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol)
+                 : "memory");
     return v;
 }
 __device__ __forceinline__ void st_global_16_hint(void* p, const uint4& v, uint64_t pol) {
@@ -278,6 +313,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gm
             smem_u32(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+// Asks L2 to fetch [src, src+bytes) ahead of use (16-byte aligned, a
+// multiple of 16 bytes); completes on its own, nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes)
+                 : "memory");
 }
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (bulk copy) accesses to the same buffers.

@@ -15,6 +15,13 @@
 //     of the row, the row sum exchanged through distributed shared memory.
 // Any input that is not 16-byte aligned, or whose row is not a whole number
 // of 16-byte vectors, takes the scalar kernel.
+//
+// With ADD every kernel first forms h = x + res, rounded once into T, stores
+// h and normalises it ("Profiling, GPU utilisation and writing a fused
+// kernel", Problem 15: the kernel takes a residual, writes the sum back and
+// normalises the sum). h may share memory with x or res: each element of h
+// is written by the thread that read it, and h is read back only through
+// coherent loads.
 #include <algorithm>
 #include <cstdlib>
 #include <string>
@@ -28,12 +35,12 @@ namespace {
 // ---------------------------------------------------------------- short rows
 // Block = threads/G groups; group g handles rows tile + r*groups + g for
 // r < R, so at each r the block touches consecutive rows.
-template <typename T, typename TW, int G, int V, int R>
-__global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__ x,
-                                                           const TW* __restrict__ w,
+template <typename T, typename TW, int G, int V, int R, bool ADD>
+__global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW* __restrict__ w,
                                                            T* __restrict__ y,
                                                            float* __restrict__ rstd, int64_t M,
-                                                           int N, float eps) {
+                                                           int N, float eps, const T* res,
+                                                           T* hout) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
     const int nvec = N / VEC;
@@ -52,6 +59,21 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
             xv[r][j] = (row < M && k < nvec)
                            ? ld_global_16_stream(x + row * N + static_cast<int64_t>(k) * VEC)
                            : make_uint4(0, 0, 0, 0);
+        }
+    }
+    if constexpr (ADD) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = tile + static_cast<int64_t>(r) * groups + group;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int k = j * G + lane;
+                if (row < M && k < nvec) {
+                    const int64_t off = row * N + static_cast<int64_t>(k) * VEC;
+                    xv[r][j] = add_vec<T>(xv[r][j], ld_global_16_stream(res + off));
+                    st_global_16(hout + off, xv[r][j]);
+                }
+            }
         }
     }
     using WP = WPack<T, TW>;
@@ -116,12 +138,11 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* __restrict__
 template <typename T, typename TW>
 constexpr int row_kernel_max_threads() { return std::is_same<T, TW>::value ? 1024 : 512; }
 
-template <typename T, typename TW, int V>
-__global__ void __launch_bounds__(row_kernel_max_threads<T, TW>()) fwd_row_kernel(const T* __restrict__ x,
-                                                       const TW* __restrict__ w,
-                                                       T* __restrict__ y, float* __restrict__ rstd,
-                                                       int64_t M, int N, float eps, int* status,
-                                                       uint64_t wait_limit_ns) {
+template <typename T, typename TW, int V, bool ADD>
+__global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
+    fwd_row_kernel(const T* x, const TW* __restrict__ w, T* __restrict__ y,
+                   float* __restrict__ rstd, int64_t M, int N, float eps, int* status,
+                   uint64_t wait_limit_ns, const T* res, T* hout) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC;
     __shared__ float red[32];
@@ -152,6 +173,17 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>()) fwd_row_kerne
         xv[j] = ok ? ld_global_16_stream(xr + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
         if (ok) WP::load(w, k, wv[j]);
         else WP::zero(wv[j]);
+    }
+    if constexpr (ADD) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = base + j * nthr + threadIdx.x;
+            if (k < nvec) {
+                const int64_t off = row * N + static_cast<int64_t>(k) * VEC;
+                xv[j] = add_vec<T>(xv[j], ld_global_16_stream(res + off));
+                st_global_16(hout + off, xv[j]);
+            }
+        }
     }
     constexpr int PR = P::PAIRS;
     float2 ss2 = make_float2(0.f, 0.f);
@@ -205,11 +237,11 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>()) fwd_row_kerne
 // reads x back from L2 (evict_first: last use), scales and stores y. HBM reads
 // x once; with one or two blocks per SM the rows in flight take a few tens
 // of MB of L2, far below its size.
-template <typename T, typename TW, int U>
-__global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
-                                                       const TW* __restrict__ w,
+template <typename T, typename TW, int U, bool ADD>
+__global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __restrict__ w,
                                                        T* __restrict__ y, float* __restrict__ rstd,
-                                                       int64_t M, int N, float eps) {
+                                                       int64_t M, int N, float eps, const T* res,
+                                                       T* hout) {
     using P = Pack<T>;
     using WP = WPack<T, TW>;
     constexpr int VEC = P::VEC;
@@ -231,6 +263,18 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
                 const int k = base + u * nthr + tid;
                 v[u] = k < nvec ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, keep)
                                 : make_uint4(0, 0, 0, 0);
+            }
+            if constexpr (ADD) {
+                // h = x + res goes to L2 (evict_last) for pass 2 and on to HBM
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = base + u * nthr + tid;
+                    if (k < nvec) {
+                        const int64_t off = row * N + static_cast<int64_t>(k) * VEC;
+                        v[u] = add_vec<T>(v[u], ld_global_16_stream(res + off));
+                        st_global_16_hint(hout + off, v[u], keep);
+                    }
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -254,8 +298,12 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
             for (int u = 0; u < U; ++u) {
                 const int k = base + u * nthr + tid;
                 const bool ok = k < nvec;
-                v[u] = ok ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, last)
-                          : make_uint4(0, 0, 0, 0);
+                if constexpr (ADD)  // h was written by this kernel: coherent loads
+                    v[u] = ok ? ld_global_16_coherent_hint(hout + row * N + static_cast<int64_t>(k) * VEC, last)
+                              : make_uint4(0, 0, 0, 0);
+                else
+                    v[u] = ok ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, last)
+                              : make_uint4(0, 0, 0, 0);
                 if (ok) WP::load(w, k, wv[u]);
                 else WP::zero(wv[u]);
             }
@@ -278,12 +326,12 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* __restrict__ x,
 // -------------------------------------------------------------------- scalar
 // Any alignment, any N: one block per row (grid-strided over rows), two
 // passes over the row with scalar loads.
-template <typename T, typename TW>
-__global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x,
-                                                         const TW* __restrict__ w,
+template <typename T, typename TW, bool ADD>
+__global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* x, const TW* __restrict__ w,
                                                          T* __restrict__ y,
                                                          float* __restrict__ rstd, int64_t M,
-                                                         int N, float eps) {
+                                                         int N, float eps, const T* res,
+                                                         T* hout) {
     using P = Pack<T>;
     __shared__ float red[2][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -292,7 +340,12 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x
         const T* xr = x + row * N;
         float ss = 0.f;
         for (int j = threadIdx.x; j < N; j += blockDim.x) {
-            const float v = to_f32(xr[j]);
+            float v = to_f32(xr[j]);
+            if constexpr (ADD) {
+                const T hv = P::from_float(v + to_f32(res[row * N + j]));
+                hout[row * N + j] = hv;
+                v = to_f32(hv);
+            }
             ss = fmaf(v, v, ss);
         }
         ss = group_allreduce<32>(ss);
@@ -302,17 +355,21 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* __restrict__ x
         total = group_allreduce<32>(total);
         const float rs = rsqrtf(total / static_cast<float>(N) + eps);
         T* yr = y + row * N;
+        // with ADD, h is read back from the elements this thread stored
+        const T* src = ADD ? hout + row * N : xr;
         for (int j = threadIdx.x; j < N; j += blockDim.x)
-            yr[j] = P::from_float(to_f32(xr[j]) * rs * to_f32(w[j]));
+            yr[j] = P::from_float(to_f32(src[j]) * rs * to_f32(w[j]));
         if (threadIdx.x == 0) rstd[row] = rs;
     }
 }
 
 template <typename T, typename TW, int G, int V, int R>
 cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
-    fwd_rowgroup_kernel<T, TW, G, V, R><<<p.grid, p.threads, 0, s>>>(
-        static_cast<const T*>(a.x), static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M,
-        a.N, a.eps);
+    auto fn = a.res != nullptr ? fwd_rowgroup_kernel<T, TW, G, V, R, true>
+                               : fwd_rowgroup_kernel<T, TW, G, V, R, false>;
+    fn<<<p.grid, p.threads, 0, s>>>(static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
+                                    static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                                    static_cast<const T*>(a.res), static_cast<T*>(a.h));
     return cudaGetLastError();
 }
 
@@ -345,9 +402,10 @@ cudaError_t launch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, fwd_row_kernel<T, TW, V>, static_cast<const T*>(a.x),
-                              static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
-                              a.eps, a.status, a.wait_limit_ns);
+    auto fn = a.res != nullptr ? fwd_row_kernel<T, TW, V, true> : fwd_row_kernel<T, TW, V, false>;
+    return cudaLaunchKernelEx(&cfg, fn, static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
+                              static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps, a.status,
+                              a.wait_limit_ns, static_cast<const T*>(a.res), static_cast<T*>(a.h));
 }
 
 template <typename T, typename TW>
@@ -358,9 +416,10 @@ cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t
 template <typename T, typename TW>
 cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     if (p.variant == RMSNORM_VARIANT_TWO_PASS) {
-        fwd_wide_kernel<T, TW, 4><<<p.grid, p.threads, 0, s>>>(
-            static_cast<const T*>(a.x), static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd,
-            a.M, a.N, a.eps);
+        auto fn = a.res != nullptr ? fwd_wide_kernel<T, TW, 4, true> : fwd_wide_kernel<T, TW, 4, false>;
+        fn<<<p.grid, p.threads, 0, s>>>(static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
+                                        static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                                        static_cast<const T*>(a.res), static_cast<T*>(a.h));
         return cudaGetLastError();
     }
     switch (p.variant) {
@@ -368,10 +427,13 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
         case RMSNORM_VARIANT_CTA_ROW:
         case RMSNORM_VARIANT_CLUSTER_ROW: return dispatch_row<T, TW>(p, a, s);
         case RMSNORM_VARIANT_SCALAR:
-            fwd_scalar_kernel<T, TW><<<p.grid, p.threads, 0, s>>>(
-                static_cast<const T*>(a.x), static_cast<const TW*>(a.w), static_cast<T*>(a.y),
-                a.rstd, a.M, a.N, a.eps);
+        {
+            auto fn = a.res != nullptr ? fwd_scalar_kernel<T, TW, true> : fwd_scalar_kernel<T, TW, false>;
+            fn<<<p.grid, p.threads, 0, s>>>(static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
+                                            static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                                            static_cast<const T*>(a.res), static_cast<T*>(a.h));
             return cudaGetLastError();
+        }
         default: return cudaErrorInvalidValue;
     }
 }

@@ -30,6 +30,8 @@ struct FwdArgs {
     float eps;
     int* status;             // device status word (bounded waits)
     uint64_t wait_limit_ns;
+    const void* res;         // residual added to x first (nullptr: plain forward)
+    void* h;                 // x + res as stored (written when res is set)
 };
 
 struct BwdArgs {
@@ -45,6 +47,7 @@ struct BwdArgs {
     int* status;
     uint64_t wait_limit_ns;
     int64_t drop_unit;  // failure-injection hook, -1 = off
+    const void* dres;   // gradient added to dx (residual path), nullptr = none
 };
 
 constexpr int kMaxCluster = 8;
@@ -56,11 +59,24 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);
 
 // Device-dependent completion of a plan (grid size, shared-memory opt-in).
 cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p);
+// `res`: the plan is for the backward with a residual gradient (its kernels
+// differ, and so may the number of resident blocks).
 cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
-                            rmsnorm_plan_t* p);
+                            rmsnorm_plan_t* p, bool res = false);
 
 cudaError_t fwd_launch(const rmsnorm_plan_t& p, int dtype, const FwdArgs& a, cudaStream_t s);
 cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cudaStream_t s);
+
+// The naive three-kernel backward (naive.cu), an ablation: workspace bytes
+// (the M x N intermediate, then the fp32 partial rows) and the launch chain.
+size_t naive_contrib_bytes(int64_t M, int64_t N, int elem);
+size_t naive_workspace_bytes(int64_t M, int64_t N, int dtype);
+constexpr int kNaiveMaxVectors = 1024;  // one 16-byte vector per thread of one block
+cudaError_t naive_launch(int dtype, const void* x, const void* w, const void* dy, void* dx,
+                         float* dw, int64_t M, int N, float eps, void* workspace, cudaStream_t s);
+// Fixed-order column sum of P fp32 partial rows into dw (bwd.cu), launched
+// in plain stream order.
+cudaError_t colsum_launch(const float* partial, float* dw, int P, int N, cudaStream_t s);
 
 cudaError_t probe_launch(int kind, void* dst, const void* a, const void* b, size_t bytes,
                          int grid, cudaStream_t s);

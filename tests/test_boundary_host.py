@@ -99,6 +99,30 @@ def test_argument_checks_need_no_device(lib):
         assert pkg.rmsnorm_bwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, code, 0) == \
             pkg.ERR_INVALID_ARG
 
+    # residual add: the same checks, plus the residual, h and dres
+    afwd, abwd = pkg.rmsnorm_add_fwd, pkg.rmsnorm_add_bwd
+    assert afwd(FAKE, None, FAKE, None, FAKE, FAKE, 0, 64, 1e-6, B, 0) == pkg.OK
+    assert afwd(FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert afwd(FAKE, FAKE, FAKE, None, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert afwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, 5, 0) == pkg.ERR_INVALID_ARG
+    assert afwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, -1.0, B, 0) == pkg.ERR_INVALID_ARG
+    assert afwd(FAKE, FAKE + 1, FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_MISALIGNED
+    assert afwd(FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 4, 64, 1e-6, F, 0) == pkg.ERR_MISALIGNED
+    assert abwd(FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 0, 64, B, 0) == pkg.OK
+    assert abwd(FAKE, FAKE, FAKE, FAKE, FAKE + 1, FAKE, FAKE, 4, 64, B, 0) == pkg.ERR_MISALIGNED
+    assert abwd(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 64, B, 0) == pkg.ERR_INVALID_ARG
+
+    # the naive backward: vector rows of at most 1024 vectors only
+    nv = pkg.rmsnorm_bwd_naive
+    assert nv(FAKE, FAKE, FAKE, FAKE, None, 0, 64, 1e-6, B, 0) == pkg.OK
+    assert nv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, -1.0, B, 0) == pkg.ERR_INVALID_ARG
+    assert nv(FAKE, FAKE, None, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_INVALID_ARG
+    assert nv(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_UNSUPPORTED
+    assert nv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 8200, 1e-6, B, 0) == pkg.ERR_UNSUPPORTED
+    assert nv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 4100, 1e-6, F, 0) == pkg.ERR_UNSUPPORTED
+    assert nv(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 13, 1e-6, B, 0) == pkg.ERR_UNSUPPORTED
+    assert nv(FAKE + 1, FAKE, FAKE, FAKE, FAKE, 4, 64, 1e-6, B, 0) == pkg.ERR_MISALIGNED
+
     probe = pkg.rmsnorm_probe
     assert probe(7, FAKE, FAKE, FAKE, 1024, 1, 0) == pkg.ERR_INVALID_ARG
     assert probe(pkg.PROBE_COPY, FAKE, FAKE, None, 1000, 1, 0) == pkg.ERR_INVALID_ARG
@@ -130,7 +154,7 @@ def test_width_ladder(lib, N, dtype):
     vec = 4 if dtype == pkg.F32 else 8  # elements per 16-byte activation vector
     mixed = dtype in (pkg.BF16_W_F32, pkg.F16_W_F32)
     vector_ok = (N * (16 // vec)) % 16 == 0
-    for pass_ in (pkg.PASS_FWD, pkg.PASS_BWD):
+    for pass_ in (pkg.PASS_FWD, pkg.PASS_BWD, pkg.PASS_BWD_RES):
         p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
         assert p.grid == 0  # no device queried
         assert p.threads % 32 == 0 and 32 <= p.threads <= 1024
@@ -158,8 +182,8 @@ def test_width_ladder(lib, N, dtype):
         else:
             # the backward's vector kernels cover every row up to 256 KiB;
             # wider rows outgrow shared memory
-            assert name == "scalar" and pass_ == pkg.PASS_BWD and N * (16 // vec) > 256 * 1024
-        if pass_ == pkg.PASS_BWD and name != "scalar":
+            assert name == "scalar" and pass_ != pkg.PASS_FWD and N * (16 // vec) > 256 * 1024
+        if pass_ != pkg.PASS_FWD and name != "scalar":
             assert 3 <= p.stages <= 6
             if name == "rowgroup":
                 unit = p.rows_per_unit * N * (16 // vec)
