@@ -58,9 +58,11 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    p.add_argument("--op", choices=["norm", "residual"], default="norm",
+    p.add_argument("--op", choices=["norm", "residual", "naive"], default="norm",
                    help="norm: rmsnorm_fwd + rmsnorm_bwd; residual: rmsnorm_add_fwd + "
-                        "rmsnorm_add_bwd with dres (residual and dres drawn like x and dy)")
+                        "rmsnorm_add_bwd with dres (residual and dres drawn like x and dy); "
+                        "naive: rmsnorm_fwd + the naive three-kernel rmsnorm_bwd_naive "
+                        "(ablation)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle budget for the cpu_baseline sample")
@@ -234,7 +236,7 @@ def run_probes(pkg, torch, nbytes: int, samples: int = 10):
     return res
 
 
-def validate(torch, x, w, dy, eps, y, rstd, dx, dw, dres=None):
+def validate(torch, x, w, dy, eps, y, rstd, dx, dw, dres=None, dw_tol=1e-3):
     """Compare against a float32 PyTorch reference on the GPU (the check
     happens before timing; the tests' rule for each dtype, with the fp32
     margins widened tenfold for a reference that is itself fp32)."""
@@ -263,7 +265,7 @@ def validate(torch, x, w, dy, eps, y, rstd, dx, dw, dres=None):
     dwr = w32.grad
     errs["dw"] = {"rel_l2": float(((dw - dwr).norm() / dwr.norm()).item())}
     ok = errs["y"]["bad"] == 0 and errs["dx"]["bad"] == 0 and errs["rstd"]["max_rel_err"] < 1e-4 \
-        and errs["dw"]["rel_l2"] < 1e-3
+        and errs["dw"]["rel_l2"] < dw_tol
     return ok, errs
 
 
@@ -328,6 +330,7 @@ def run_ours(args):
     wl = synth.WORKLOADS[args.workload]
     M, N, eps = wl.M, wl.N, wl.eps
     residual = args.op == "residual"
+    naive = args.op == "naive"
     code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
     elem = torch.empty(0, dtype=wl.dtype).element_size()
     w_elem = torch.empty(0, dtype=wl.weight_dtype).element_size()
@@ -384,6 +387,9 @@ def run_ours(args):
         if residual:
             return pkg.rmsnorm_add_bwd(o["h"], s["w"], s["dy"], o["rstd"], s["dres"], o["dx"],
                                        o["dw"], M, N, code, stream)
+        if naive:
+            return pkg.rmsnorm_bwd_naive(s["x"], s["w"], s["dy"], o["dx"], o["dw"], M, N, eps,
+                                         code, stream)
         return pkg.rmsnorm_bwd(s["x"], s["w"], s["dy"], o["rstd"], o["dx"], o["dw"], M, N, code,
                                stream)
 
@@ -404,7 +410,10 @@ def run_ours(args):
                 xin = h_ref
             ok, errs_i = validate(torch, xin, sets[i]["w"], sets[i]["dy"], eps,
                                   outs[i]["y"], outs[i]["rstd"], outs[i]["dx"], outs[i]["dw"],
-                                  sets[i]["dres"] if residual else None)
+                                  sets[i]["dres"] if residual else None,
+                                  # the naive chain rounds every dw term to the
+                                  # activation type (about 1e-3 relative in bf16)
+                                  dw_tol=5e-3 if naive else 1e-3)
             if not ok:
                 raise SystemExit(f"validation failed before timing: {json.dumps(errs_i)}")
             errs = errs if errs is not None else errs_i
@@ -473,7 +482,7 @@ def run_ours(args):
 
     # end to end through pinned host buffers
     e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes,
-                  residual)
+                  args.op)
     if dist is not None:
         e2e["step_ms"] = slowest_rank(dist, [e2e["step_ms"]], base["x"].device)[0]
         e2e["value"] = round(replica_throughput(world, fwd_bytes + bwd_bytes, e2e["step_ms"]), 2)
@@ -501,7 +510,9 @@ def run_ours(args):
         "dtype": wl.dtype_name,
         "data": "synthetic",
         "config": {
-            "workload": wl.name, "op": "residual add + rmsnorm" if residual else "rmsnorm",
+            "workload": wl.name,
+            "op": {"norm": "rmsnorm", "residual": "residual add + rmsnorm",
+                   "naive": "rmsnorm, naive three-kernel backward (ablation)"}[args.op],
             "M": M, "N": N, "eps": eps, "io_dtype": wl.dtype_name,
             "accumulate": "f32", "rstd_dw_dtype": "f32", "about": wl.about,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -522,7 +533,8 @@ def run_ours(args):
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": ("rmsnorm_add_bwd" if residual else "rmsnorm_bwd")
+            "kernel": "rmsnorm_bwd_naive (row kernel + two column sums, one call)" if naive
+            else ("rmsnorm_add_bwd" if residual else "rmsnorm_bwd")
             + " (persistent kernel + fixed-order column sum, one call)",
             "achieved": round(bwd_gbs, 1),
             "peak": peak,
@@ -538,13 +550,13 @@ def run_ours(args):
         "clocks": clock_info,
         "e2e": e2e,
         "small_m": small_m,
-        "gpu_launches": 3 * K,
+        "gpu_launches": (4 if naive else 3) * K,  # ours only: fwd, main bwd, column sum(s)
         "validation": errs,
         "library": {"path": pkg.library_path(), "source_hash": libbuild.source_hash(),
                     "bwd_kernel_hash": libbuild.kernel_source_hash(),
                     "version": pkg.rmsnorm_version()},
     }
-    if rank == 0 and not args.no_cpu_baseline and not residual:
+    if rank == 0 and not args.no_cpu_baseline and args.op == "norm":
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if dist is not None:
         dist.destroy_process_group()
@@ -600,11 +612,12 @@ def run_small_m(pkg, torch, steps: int = 200):
     return out
 
 
-def run_e2e(pkg, torch, wl, base, code, stream, steps, logical, residual=False):
+def run_e2e(pkg, torch, wl, base, code, stream, steps, logical, op="norm"):
     """Same work through the C ABI with the inputs in pinned host memory: each
     step copies x, w, dy (and the residual and dres) to the device, runs
     forward and backward, and copies y, rstd, dx, dw (and h) back."""
     M, N, eps = wl.M, wl.N, wl.eps
+    residual = op == "residual"
     names = ["x", "w", "dy"] + (["res", "dres"] if residual else [])
     host = {k: base[k].cpu().pin_memory() for k in names}
     dev = {k: torch.empty_like(base[k]) for k in names}
@@ -627,6 +640,10 @@ def run_e2e(pkg, torch, wl, base, code, stream, steps, logical, residual=False):
             pkg.check(pkg.rmsnorm_add_bwd(h, dev["w"], dev["dy"], rstd, dev["dres"], dx, dw, M,
                                           N, code, stream))
             hh.copy_(h, non_blocking=True)
+        elif op == "naive":
+            pkg.check(pkg.rmsnorm_fwd(dev["x"], dev["w"], y, rstd, M, N, eps, code, stream))
+            pkg.check(pkg.rmsnorm_bwd_naive(dev["x"], dev["w"], dev["dy"], dx, dw, M, N, eps, code,
+                                            stream))
         else:
             pkg.check(pkg.rmsnorm_fwd(dev["x"], dev["w"], y, rstd, M, N, eps, code, stream))
             pkg.check(pkg.rmsnorm_bwd(dev["x"], dev["w"], dev["dy"], rstd, dx, dw, M, N, code,
