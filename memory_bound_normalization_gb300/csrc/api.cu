@@ -70,7 +70,7 @@ int bwd_prepare(const void* x, const void* w, const void* dy, const float* rstd,
         return RMSNORM_ERR_MISALIGNED;
     const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(dy, 16) && aligned(dx, 16) &&
                      (!dres || aligned(dres, 16)) && (N * sz) % 16 == 0 && (N * wsz) % 16 == 0;
-    bwd_choose(N, dtype, vec, plan);
+    bwd_choose(N, dtype, vec, plan, dres != nullptr);
     st = current_device(dev);
     if (st != RMSNORM_OK) return st;
     return cuda_status(bwd_finish_plan(**dev, dtype, M, N, plan, dres != nullptr));
@@ -334,7 +334,7 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     if (pass == RMSNORM_PASS_FWD)
         fwd_choose(N, dtype, vec, out);
     else
-        bwd_choose(N, dtype, vec, out);
+        bwd_choose(N, dtype, vec, out, pass == RMSNORM_PASS_BWD_RES);
     if (device < 0) return RMSNORM_OK;
     const DeviceInfo* dev = device_info(device);
     if (!dev) return RMSNORM_ERR_CUDA;

@@ -176,7 +176,10 @@ cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, i
 
 }  // namespace
 
-void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
+// With res (the residual backward) the rings carry dres as a third tensor:
+// stages may drop to two before a row group or a ring is given up, and wide
+// rows may take a larger cluster. Plans without res are unchanged by it.
+void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool res) {
     *p = rmsnorm_plan_t{};
     p->cluster = 1;
     p->row_groups = 1;
@@ -184,6 +187,8 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     const int sz = dtype_size(dtype);
     const int64_t nvec = N / dtype_vec(dtype);
     const BwdTuning& tu = tuning();
+    const int nt = res ? 3 : 2;          // tensors in a ring stage
+    const int min_stages = res ? 2 : 3;
     GroupShape g;
     if (vector_ok && bwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
@@ -192,8 +197,9 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         p->vectors_per_thread = g.V;
         p->rows_per_unit = (g.threads / g.G) * g.R;
         const int unit = static_cast<int>(p->rows_per_unit * N * sz);
-        p->stages = tu.stages > 0 ? tu.stages : std::max(3, std::min(6, kStageBudget / (2 * unit)));
-        p->smem_bytes = bwd_smem_bytes(p->stages, unit);
+        p->stages = tu.stages > 0 ? tu.stages
+                                  : std::max(min_stages, std::min(6, kStageBudget / (nt * unit)));
+        p->smem_bytes = bwd_smem_bytes(p->stages, unit, nt);
         return;
     }
     if (vector_ok) {
@@ -205,10 +211,17 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         if (tg <= 512) {
             const int unit = tu.vectors * tg * 16;
             int stages = tu.stages > 0 ? tu.stages
-                                       : std::max(3, std::min(6, tu.smem_multi / (groups * 2 * unit)));
-            while (groups > 1 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --groups;
-            while (stages > 3 && bwd_row_smem_bytes(groups, stages, unit) > kSmemMax) --stages;
-            if (bwd_row_smem_bytes(groups, stages, unit) <= kSmemMax) {
+                                       : std::max(min_stages,
+                                                  std::min(6, tu.smem_multi / (groups * nt * unit)));
+            auto bytes = [&] { return bwd_row_smem_bytes(groups, stages, unit, nt); };
+            if (res) {
+                while (stages > min_stages && bytes() > kSmemMax) --stages;
+                while (groups > 1 && bytes() > kSmemMax) --groups;
+            } else {
+                while (groups > 1 && bytes() > kSmemMax) --groups;
+                while (stages > min_stages && bytes() > kSmemMax) --stages;
+            }
+            if (bytes() <= kSmemMax) {
                 p->variant = RMSNORM_VARIANT_CTA_ROW;
                 p->row_groups = groups;
                 p->vectors_per_thread = tu.vectors;
@@ -216,31 +229,35 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
                 p->threads_per_row = tg;
                 p->rows_per_unit = groups;
                 p->stages = stages;
-                p->smem_bytes = bwd_row_smem_bytes(groups, stages, unit);
+                p->smem_bytes = bytes();
                 return;
             }
         }
-        // wider rows: split over a cluster, one pipelined row per block
+        // wider rows: split over a cluster, one row at a time per block
         int c = 1;
         while (2 * cdiv(nvec, c) * 16 > tu.slice && c < kMaxCluster) c *= 2;
-        const int64_t slots = cdiv(nvec, c);
-        int v = 4;
-        while (cdiv(slots, v) > 512 && v < 8) v *= 2;
-        const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
-        const int unit = v * t * 16;
-        int stages = tu.stages > 0 ? tu.stages : std::max(3, std::min(6, tu.smem_multi / (2 * unit)));
-        while (stages > 3 && bwd_wide_smem_bytes(stages, unit) > kSmemMax) --stages;
-        if (t <= 512 && bwd_wide_smem_bytes(stages, unit) <= kSmemMax) {
-            p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
-            p->cluster = c;
-            p->row_groups = 1;
-            p->vectors_per_thread = v;
-            p->threads = t;
-            p->threads_per_row = t * c;
-            p->rows_per_unit = 1;
-            p->stages = stages;
-            p->smem_bytes = bwd_wide_smem_bytes(stages, unit);
-            return;
+        for (;; c *= 2) {
+            const int64_t slots = cdiv(nvec, c);
+            int v = 4;
+            while (cdiv(slots, v) > 512 && v < 8) v *= 2;
+            const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
+            const int unit = v * t * 16;
+            int stages = tu.stages > 0 ? tu.stages
+                                       : std::max(min_stages, std::min(6, tu.smem_multi / (nt * unit)));
+            while (stages > min_stages && bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
+            if (t <= 512 && bwd_wide_smem_bytes(stages, unit, nt) <= kSmemMax) {
+                p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
+                p->cluster = c;
+                p->row_groups = 1;
+                p->vectors_per_thread = v;
+                p->threads = t;
+                p->threads_per_row = t * c;
+                p->rows_per_unit = 1;
+                p->stages = stages;
+                p->smem_bytes = bwd_wide_smem_bytes(stages, unit, nt);
+                return;
+            }
+            if (!res || c >= kMaxCluster) break;
         }
     }
     p->variant = RMSNORM_VARIANT_SCALAR;

@@ -32,9 +32,9 @@
 // dx = rstd*(g - xhat*c) + dres, where dres is the gradient reaching h from
 // its other uses; that dx is the gradient of both summands ("Profiling, GPU
 // utilisation and writing a fused kernel", Problem 15, the residual step).
-// dres is read in pass 2 with coherent loads (dx may be the dres buffer);
-// the thread that issues a row's bulk copies also asks L2 to prefetch that
-// row's dres, so those loads hit L2.
+// dres travels through the bulk-copy ring as a third tensor beside x and dy,
+// so pass 2 reads it from shared memory; the copy of a row lands before that
+// row's dx is written, so dx may be the dres buffer.
 #pragma once
 
 #include "common.cuh"
@@ -42,29 +42,32 @@
 
 namespace rmsn {
 
+// The rings hold nt tensors per stage: x and dy, plus dres on the residual
+// path (nt = 3).
+//
 // Shared memory of the short-row kernel: [S][unit] x | [S][unit] dy |
-// mbarrier[S] | 66 floats of reduction slots | failure flag.
-__host__ __device__ inline int bwd_smem_bytes(int stages, int unit) {
-    return 2 * stages * unit + stages * 8 + 64 * 4 + 2 * 4 + 16;
+// ([S][unit] dres) | mbarrier[S] | 66 floats of reduction slots | failure flag.
+__host__ __device__ inline int bwd_smem_bytes(int stages, int unit, int nt = 2) {
+    return nt * stages * unit + stages * 8 + 64 * 4 + 2 * 4 + 16;
 }
 
 // Shared memory of the grouped row kernel, per group: [S][unit] x |
-// [S][unit] dy | mbarrier[S] | reduction slots [2][32] | failure flag, padded
-// to a multiple of 128 bytes so that every group's ring starts 16-byte aligned
-// (bulk copies and 16-byte shared loads need it).
-__host__ __device__ inline int bwd_row_group_stride(int stages, int unit) {
-    return (2 * stages * unit + stages * 8 + 64 * 4 + 16 + 127) / 128 * 128;
+// [S][unit] dy | ([S][unit] dres) | mbarrier[S] | reduction slots [2][32] |
+// failure flag, padded to a multiple of 128 bytes so that every group's ring
+// starts 16-byte aligned (bulk copies and 16-byte shared loads need it).
+__host__ __device__ inline int bwd_row_group_stride(int stages, int unit, int nt = 2) {
+    return (nt * stages * unit + stages * 8 + 64 * 4 + 16 + 127) / 128 * 128;
 }
 
 // Shared memory of the wide-row kernel: [S][unit] x | [S][unit] dy |
-// mbarrier[S] (copies) | mbarrier[4] (cluster exchange) | reduction slots
-// [2][32] | exchange slots [4][kMaxClusterSize] | failure flag.
+// ([S][unit] dres) | mbarrier[S] (copies) | mbarrier[4] (cluster exchange) |
+// reduction slots [2][32] | exchange slots [4][kMaxClusterSize] | failure flag.
 constexpr int kMaxClusterSize = 16;
-__host__ __device__ inline int bwd_wide_smem_bytes(int stages, int unit) {
-    return 2 * stages * unit + stages * 8 + 4 * 8 + 64 * 4 + 4 * kMaxClusterSize * 4 + 16;
+__host__ __device__ inline int bwd_wide_smem_bytes(int stages, int unit, int nt = 2) {
+    return nt * stages * unit + stages * 8 + 4 * 8 + 64 * 4 + 4 * kMaxClusterSize * 4 + 16;
 }
-__host__ __device__ inline int bwd_row_smem_bytes(int groups, int stages, int unit) {
-    return groups * bwd_row_group_stride(stages, unit);
+__host__ __device__ inline int bwd_row_smem_bytes(int groups, int stages, int unit, int nt = 2) {
+    return groups * bwd_row_group_stride(stages, unit, nt);
 }
 
 // Main (row) kernel of a backward plan for each element-type code, without
@@ -125,11 +128,13 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     const int S = stages;
     const int unit = slots * 16;
 
-    const int gstride = bwd_row_group_stride(S, unit);
+    constexpr int NT = RES ? 3 : 2;  // tensors in the ring
+    const int gstride = bwd_row_group_stride(S, unit, NT);
     unsigned char* gbase = smem + g * gstride;
     unsigned char* sx = gbase;
     unsigned char* sdy = gbase + S * unit;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + 2 * S * unit);
+    unsigned char* sdr = gbase + 2 * S * unit;  // dres (RES only)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(gbase + NT * S * unit);
     float* red = reinterpret_cast<float*>(bar + S);
     volatile int* fail = reinterpret_cast<volatile int*>(red + 64);
 
@@ -160,12 +165,12 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             mbar_arrive(&bar[s]);
             return;
         }
-        mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+        mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         if (row == a.drop_unit) return;  // failure injection: this wait runs out
         const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
-        if constexpr (RES) bulk_prefetch_l2(DRES + off, bytes);
+        if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
@@ -261,8 +266,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
             float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
-            if constexpr (RES)
-                P::unpack2(ld_global_16_coherent(DRES + (dxr - DX) + static_cast<int64_t>(vbeg + k) * VEC), fr);
+            if constexpr (RES) P::unpack2(ld_shared_16(sdr + s * unit + k * 16), fr);
             P::unpack2(ld_shared_16(xs + k * 16), fx);
             P::unpack2(ld_shared_16(ds + k * 16), fd);
             weights(j, k, fw);
@@ -369,9 +373,11 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     const int S = stages;
     const int unit = slots * 16;
 
+    constexpr int NT = RES ? 3 : 2;  // tensors in the ring
     unsigned char* sx = smem;
     unsigned char* sdy = smem + S * unit;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * S * unit);
+    unsigned char* sdr = smem + 2 * S * unit;  // dres (RES only)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + NT * S * unit);
     uint64_t* xbar = bar + S;                          // [4]
     float* red = reinterpret_cast<float*>(xbar + 4);  // [2][32]
     float* xslot = red + 64;                           // [4][kMaxClusterSize]
@@ -404,12 +410,12 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
             mbar_arrive(&bar[s]);
             return;
         }
-        mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+        mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         if (row == a.drop_unit) return;  // failure injection: this wait runs out
         const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
-        if constexpr (RES) bulk_prefetch_l2(DRES + off, bytes);
+        if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
@@ -520,8 +526,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
             const int k = j * nthr + tid;
             if (k >= vcnt) continue;
             float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
-            if constexpr (RES)
-                P::unpack2(ld_global_16_coherent(DRES + (dxr - DX) + static_cast<int64_t>(vbeg + k) * VEC), fr);
+            if constexpr (RES) P::unpack2(ld_shared_16(sdr + s * unit + k * 16), fr);
             P::unpack2(ld_shared_16(xs + k * 16), fx);
             P::unpack2(ld_shared_16(ds + k * 16), fd);
             weights(j, k, fw);
@@ -626,9 +631,11 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     const int S = stages;
     const int unit = RT * N * static_cast<int>(sizeof(T));
 
+    constexpr int NT = RES ? 3 : 2;  // tensors in the ring
     unsigned char* sx = smem;
     unsigned char* sdy = smem + S * unit;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * S * unit);
+    unsigned char* sdr = smem + 2 * S * unit;  // dres (RES only)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + NT * S * unit);
     volatile int* fail = reinterpret_cast<volatile int*>(reinterpret_cast<float*>(bar + S) + 66);
 
     const T* X = static_cast<const T*>(a.x);
@@ -650,12 +657,12 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         const int64_t tile = b + t * nb;
         const int64_t rows = min(static_cast<int64_t>(RT), a.M - tile * RT);
         const uint32_t bytes = static_cast<uint32_t>(rows * N * static_cast<int64_t>(sizeof(T)));
-        mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+        mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         if (tile == a.drop_unit) return;  // failure injection
         const int64_t off = tile * RT * N;
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
-        if constexpr (RES) bulk_prefetch_l2(DRES + off, bytes);
+        if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
         pending |= 1u << s;
         pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
     };
@@ -753,8 +760,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                 if (k >= nvec) continue;
                 const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
                 float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
-                if constexpr (RES)
-                    P::unpack2(ld_global_16_coherent(DRES + row * N + static_cast<int64_t>(k) * VEC), fr);
+                if constexpr (RES) P::unpack2(ld_shared_16(sdr + s * unit + off), fr);
                 P::unpack2(ld_shared_16(sx + s * unit + off), fx);
                 P::unpack2(ld_shared_16(sdy + s * unit + off), fd);
                 WP::unpack2(wv[j], fw);

@@ -55,7 +55,8 @@ constexpr int kMaxCluster = 8;
 // Width-dependent choices (host only, no device queries). `vector_ok` says
 // whether the pointers and N allow 16-byte vector access.
 void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);
-void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);
+// `res`: plan the residual backward (dres rides in the rings as well).
+void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool res = false);
 
 // Device-dependent completion of a plan (grid size, shared-memory opt-in).
 cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p);

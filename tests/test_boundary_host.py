@@ -184,12 +184,14 @@ def test_width_ladder(lib, N, dtype):
             # wider rows outgrow shared memory
             assert name == "scalar" and pass_ != pkg.PASS_FWD and N * (16 // vec) > 256 * 1024
         if pass_ != pkg.PASS_FWD and name != "scalar":
-            assert 3 <= p.stages <= 6
+            # the residual backward's rings carry dres too and may be 2 deep
+            res = pass_ == pkg.PASS_BWD_RES
+            assert (2 if res else 3) <= p.stages <= 6
             if name == "rowgroup":
                 unit = p.rows_per_unit * N * (16 // vec)
             else:
                 unit = p.vectors_per_thread * (p.threads // p.row_groups) * 16 * p.row_groups
-            assert p.smem_bytes >= 2 * p.stages * unit
+            assert p.smem_bytes >= (3 if res else 2) * p.stages * unit
 
 
 def test_plan_rejects_bad_arguments(lib):
