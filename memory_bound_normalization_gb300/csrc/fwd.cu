@@ -62,6 +62,20 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
         }
     }
     if constexpr (ADD) {
+        // every residual load is issued before the first add, so they are in
+        // flight together (the loads cannot be moved past the stores of h)
+        uint4 rv[R][V];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int64_t row = tile + static_cast<int64_t>(r) * groups + group;
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                const int k = j * G + lane;
+                rv[r][j] = (row < M && k < nvec)
+                               ? ld_global_16_stream(res + row * N + static_cast<int64_t>(k) * VEC)
+                               : make_uint4(0, 0, 0, 0);
+            }
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const int64_t row = tile + static_cast<int64_t>(r) * groups + group;
@@ -69,9 +83,8 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
             for (int j = 0; j < V; ++j) {
                 const int k = j * G + lane;
                 if (row < M && k < nvec) {
-                    const int64_t off = row * N + static_cast<int64_t>(k) * VEC;
-                    xv[r][j] = add_vec<T>(xv[r][j], ld_global_16_stream(res + off));
-                    st_global_16(hout + off, xv[r][j]);
+                    xv[r][j] = add_vec<T>(xv[r][j], rv[r][j]);
+                    st_global_16(hout + row * N + static_cast<int64_t>(k) * VEC, xv[r][j]);
                 }
             }
         }
@@ -175,13 +188,20 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
         else WP::zero(wv[j]);
     }
     if constexpr (ADD) {
+        // all residual loads first, then the adds and the stores of h
+        uint4 rv[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = base + j * nthr + threadIdx.x;
+            rv[j] = k < nvec ? ld_global_16_stream(res + row * N + static_cast<int64_t>(k) * VEC)
+                             : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = base + j * nthr + threadIdx.x;
             if (k < nvec) {
-                const int64_t off = row * N + static_cast<int64_t>(k) * VEC;
-                xv[j] = add_vec<T>(xv[j], ld_global_16_stream(res + off));
-                st_global_16(hout + off, xv[j]);
+                xv[j] = add_vec<T>(xv[j], rv[j]);
+                st_global_16(hout + row * N + static_cast<int64_t>(k) * VEC, xv[j]);
             }
         }
     }
@@ -265,14 +285,21 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
                                 : make_uint4(0, 0, 0, 0);
             }
             if constexpr (ADD) {
-                // h = x + res goes to L2 (evict_last) for pass 2 and on to HBM
+                // h = x + res goes to L2 (evict_last) for pass 2 and on to
+                // HBM; all residual loads are issued before the first store
+                uint4 rv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = base + u * nthr + tid;
+                    rv[u] = k < nvec ? ld_global_16_stream(res + row * N + static_cast<int64_t>(k) * VEC)
+                                     : make_uint4(0, 0, 0, 0);
+                }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int k = base + u * nthr + tid;
                     if (k < nvec) {
-                        const int64_t off = row * N + static_cast<int64_t>(k) * VEC;
-                        v[u] = add_vec<T>(v[u], ld_global_16_stream(res + off));
-                        st_global_16_hint(hout + off, v[u], keep);
+                        v[u] = add_vec<T>(v[u], rv[u]);
+                        st_global_16_hint(hout + row * N + static_cast<int64_t>(k) * VEC, v[u], keep);
                     }
                 }
             }
