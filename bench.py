@@ -67,6 +67,10 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle budget for the cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the width sweep (every bf16 and fp32 sweep cell, validated and "
+                        "timed like the main workload with --sweep-steps steps)")
+    p.add_argument("--sweep-steps", type=int, default=30)
     p.add_argument("--no-small-m", action="store_true",
                    help="skip the small-M eager vs CUDA-graph latency table")
     p.add_argument("--profile", action="store_true",
@@ -312,40 +316,17 @@ def cpu_baseline(wl, budget_s: float):
 
 # ------------------------------------------------------------------ our arm
 
-def run_ours(args):
-    import torch
-
-    import memory_bound_normalization_gb300 as pkg
-    from memory_bound_normalization_gb300 import build as libbuild
-    from memory_bound_normalization_gb300 import synth
-
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-
-    pkg.load_library()  # raises if librmsnorm.so is missing
-    wl = synth.WORKLOADS[args.workload]
+def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_first=True,
+              sample_clocks=False, dist=None):
+    """Validates (unless check_first is False) and times `steps` forward +
+    backward calls of one workload: inputs rotated over clone sets covering
+    >= 3x L2, a clean cold L2 before every call, CUDA events on the calling
+    stream around each call; the backward is re-run once at the end and must
+    give the same dw bits."""
     M, N, eps = wl.M, wl.N, wl.eps
-    residual = args.op == "residual"
-    naive = args.op == "naive"
-    code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
+    residual = op == "residual"
+    naive = op == "naive"
     elem = torch.empty(0, dtype=wl.dtype).element_size()
-    w_elem = torch.empty(0, dtype=wl.weight_dtype).element_size()
-    fwd_bytes, bwd_bytes = synth.logical_bytes(M, N, elem, w_elem)
-    if residual:
-        # the residual is read and h written in the forward; dres is read in
-        # the backward
-        fwd_bytes += 2 * M * N * elem
-        bwd_bytes += M * N * elem
-    props = torch.cuda.get_device_properties(local)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-
-    peak, peak_src = read_peaks()
-    probes_open = None if args.profile else run_probes(pkg, torch, 1 << 30)
-
     # inputs, rotated over clone sets covering >= 3x L2
     base = synth.make_inputs(wl, device=f"cuda:{local}")
     if residual:
@@ -395,7 +376,7 @@ def run_ours(args):
 
     # validate every clone set before timing
     errs = None
-    if not args.profile:
+    if check_first:
         for i in range(nsets):
             pkg.check(fwd(i), "rmsnorm_fwd")
             pkg.check(bwd(i), "rmsnorm_bwd")
@@ -419,7 +400,7 @@ def run_ours(args):
             errs = errs if errs is not None else errs_i
     dw0 = None
 
-    for k in range(args.warmup):
+    for k in range(warmup):
         i = k % nsets
         flush()
         pkg.check(fwd(i))
@@ -427,15 +408,17 @@ def run_ours(args):
         pkg.check(bwd(i))
     torch.cuda.synchronize()
 
-    K = args.steps
+    K = steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     region0, region1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    clocks.start()
+    clocks = ClockSampler(local) if sample_clocks else None
+    if clocks is not None:
+        clocks.start()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.mark_start()
+    if clocks is not None:
+        clocks.mark_start()
     region0.record(stream)
     for k in range(K):
         i = k % nsets
@@ -450,10 +433,11 @@ def run_ours(args):
         e[3].record(stream)
     region1.record(stream)
     torch.cuda.synchronize()
-    clocks.mark_end()
+    if clocks is not None:
+        clocks.mark_end()
     if dist is not None:
         dist.barrier()
-    clock_info = clocks.stop()
+    clock_info = clocks.stop() if clocks is not None else None
     st = pkg.rmsnorm_get_last_device_error(stream)
     pkg.check(st, "device status after timing")
     if dw0 is None:
@@ -469,6 +453,53 @@ def run_ours(args):
     bwd_mean = sum(bwd_ms) / K
     step_ms = fwd_mean + bwd_mean
     region_ms = event_ms(region0, region1)
+    return {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_mean": fwd_mean, "bwd_mean": bwd_mean,
+            "step_ms": step_ms, "region_ms": region_ms, "nsets": nsets, "set_bytes": set_bytes,
+            "errs": errs, "base": base, "clock_info": clock_info}
+
+
+def run_ours(args):
+    import torch
+
+    import memory_bound_normalization_gb300 as pkg
+    from memory_bound_normalization_gb300 import build as libbuild
+    from memory_bound_normalization_gb300 import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    pkg.load_library()  # raises if librmsnorm.so is missing
+    wl = synth.WORKLOADS[args.workload]
+    M, N, eps = wl.M, wl.N, wl.eps
+    residual = args.op == "residual"
+    naive = args.op == "naive"
+    code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
+    elem = torch.empty(0, dtype=wl.dtype).element_size()
+    w_elem = torch.empty(0, dtype=wl.weight_dtype).element_size()
+    fwd_bytes, bwd_bytes = synth.logical_bytes(M, N, elem, w_elem)
+    if residual:
+        # the residual is read and h written in the forward; dres is read in
+        # the backward
+        fwd_bytes += 2 * M * N * elem
+        bwd_bytes += M * N * elem
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+
+    peak, peak_src = read_peaks()
+    probes_open = None if args.profile else run_probes(pkg, torch, 1 << 30)
+
+    cell = time_cell(pkg, torch, synth, wl, args.op, code, args.steps, args.warmup, local, l2,
+                     check_first=not args.profile, sample_clocks=True, dist=dist)
+    fwd_ms, bwd_ms = cell["fwd_ms"], cell["bwd_ms"]
+    fwd_mean, bwd_mean, step_ms = cell["fwd_mean"], cell["bwd_mean"], cell["step_ms"]
+    region_ms, nsets, set_bytes = cell["region_ms"], cell["nsets"], cell["set_bytes"]
+    errs, base, clock_info = cell["errs"], cell["base"], cell["clock_info"]
+    K = args.steps
+    stream = torch.cuda.current_stream()
     step_ms, fwd_mean, bwd_mean = slowest_rank(dist, [step_ms, fwd_mean, bwd_mean],
                                                base["x"].device)
 
@@ -556,11 +587,34 @@ def run_ours(args):
                     "bwd_kernel_hash": libbuild.kernel_source_hash(),
                     "version": pkg.rmsnorm_version()},
     }
+    if world == 1 and args.op == "norm" and not args.no_sweep:
+        line["sweep"] = run_sweep(pkg, torch, synth, args, local, l2, peak)
     if rank == 0 and not args.no_cpu_baseline and args.op == "norm":
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if dist is not None:
         dist.destroy_process_group()
     return line if rank == 0 else None
+
+
+def run_sweep(pkg, torch, synth, args, local, l2, peak):
+    """The width sweep (fixed M*N = 2^27, bf16 and fp32): each cell validated
+    against PyTorch, then forward and backward timed after a clean cold L2,
+    as for the main workload. Fractions are of the measured copy bandwidth."""
+    cells = []
+    for dt in (torch.bfloat16, torch.float32):
+        for wl in synth.width_sweep(dt):
+            code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
+            elem = torch.empty(0, dtype=wl.dtype).element_size()
+            fb, bb = synth.logical_bytes(wl.M, wl.N, elem)
+            c = time_cell(pkg, torch, synth, wl, "norm", code, args.sweep_steps, 3, local, l2)
+            fg = fb / (c["fwd_mean"] * 1e-3) / 1e9
+            bg = bb / (c["bwd_mean"] * 1e-3) / 1e9
+            cells.append({"workload": wl.name, "dtype": wl.dtype_name, "M": wl.M, "N": wl.N,
+                          "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
+                          "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
+                          "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1)})
+            del c
+    return {"steps": args.sweep_steps, "peak_gbs": peak, "cells": cells}
 
 
 def run_small_m(pkg, torch, steps: int = 200):
