@@ -18,18 +18,20 @@ namespace {
 constexpr int kStageBudget = 48 * 1024;   // ring bytes aimed at per short-row block
 constexpr int kSliceBudget = 64 * 1024;   // x+dy bytes of one row slice per stage
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory a block may opt into
+constexpr int kMaxRowGroups = 8;          // named barriers 1..8 (0 is __syncthreads)
 
 // Tuning overrides for sweeps (read once; unset = built-in ladder). They
 // change the persistent grid, hence the order of the dw sum: results stay
 // deterministic for a fixed setting.
 struct BwdTuning {
     int vectors = 4;        // 16-byte vectors per thread in a row group
-    int groups = 0;         // row groups per block (0 = up to 4, 512 threads)
+    int groups = 0;         // row groups per block (0 = as many as 512 threads hold)
     int stages = 0;         // ring depth (0 = from the shared-memory budget)
     int smem_multi = 200 * 1024;   // shared memory aimed at, several groups
     int smem_single = 100 * 1024;  // shared memory aimed at, one group
     int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
     bool pipelined = false;        // cluster rows: pass 1 of the next row first
+    bool colsum_vec = false;       // column sum with 16-byte loads (N % 4 == 0)
 };
 
 int env_int(const char* name, int dflt) {
@@ -43,11 +45,12 @@ const BwdTuning& tuning() {
         BwdTuning u;
         u.vectors = env_int("RMSNORM_BWD_VECTORS", u.vectors);
         if (u.vectors != 1 && u.vectors != 2 && u.vectors != 4 && u.vectors != 8) u.vectors = 4;
-        u.groups = std::max(0, std::min(4, env_int("RMSNORM_BWD_GROUPS", 0)));
+        u.groups = std::max(0, std::min(kMaxRowGroups, env_int("RMSNORM_BWD_GROUPS", 0)));
         u.stages = std::max(0, std::min(8, env_int("RMSNORM_BWD_STAGES", 0)));
         u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
         u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
         u.pipelined = env_int("RMSNORM_BWD_PIPE", 0) != 0;
+        u.colsum_vec = env_int("RMSNORM_COLSUM_VEC", 0) != 0;
         return u;
     }();
     return t;
@@ -77,6 +80,49 @@ __global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ 
         dw[col] = t;
     }
 }
+// The same sum with 16-byte loads: thread (x, q) sums partial rows
+// p = q, q+32, ... of columns 4x .. 4x+3 (x = blockIdx.x*32 + threadIdx.x) in
+// ascending p, then the 32 sums of each column are added in q order. A
+// quarter of the blocks and loads of colsum_kernel. Needs N % 4 == 0 (rows
+// of the partial then start 16-byte aligned).
+__global__ void __launch_bounds__(1024) colsum_vec_kernel(const float* __restrict__ partial,
+                                                          float* __restrict__ dw, int P, int N) {
+    __shared__ float4 part[32][33];
+    wait_for_prerequisite_grid();  // partial rows complete and visible
+    const int cx = threadIdx.x, q = threadIdx.y;
+    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * 32 + cx;  // float4 column index
+    const bool ok = c4 < N / 4;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok) {
+#pragma unroll 8
+        for (int p = q; p < P; p += 32) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(partial + static_cast<int64_t>(p) * N) + c4);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+    }
+    part[q][cx] = s;
+    __syncthreads();
+    if (q == 0 && ok) {
+        float4 t = part[0][cx];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) {
+            const float4 v = part[i][cx];
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        float* o = dw + 4 * c4;  // dw is only 4-byte aligned: scalar stores
+        o[0] = t.x;
+        o[1] = t.y;
+        o[2] = t.z;
+        o[3] = t.w;
+    }
+}
+
 // ------------------------------------------------------------ host side
 const void* main_kernel_for(int dtype, const rmsnorm_plan_t& p, bool res) {
     const bool pipe = tuning().pipelined;
@@ -203,10 +249,10 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
         return;
     }
     if (vector_ok) {
-        // rows one block covers with 4 vectors per thread: up to four row
-        // groups per block (one for the widest of them)
+        // rows one block covers with 4 vectors per thread: as many row groups
+        // as 512 threads hold (one for the widest rows, five at 96 threads)
         const int tg = std::max(32, round_up(static_cast<int>(cdiv(nvec, tu.vectors)), 32));
-        int groups = tu.groups > 0 ? tu.groups : std::max(1, std::min(4, 512 / tg));
+        int groups = tu.groups > 0 ? tu.groups : std::max(1, std::min(kMaxRowGroups, 512 / tg));
         while (groups > 1 && groups * tg > 512) --groups;
         if (tg <= 512) {
             const int unit = tu.vectors * tg * 16;
@@ -326,6 +372,10 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cs.attrs = pdl;
     cs.numAttrs = 1;
     const float* part = a.partial;
+    if (tuning().colsum_vec && a.N % 4 == 0) {
+        cs.gridDim = dim3(static_cast<unsigned>(cdiv(a.N / 4, 32)));
+        return cudaLaunchKernelEx(&cs, colsum_vec_kernel, part, a.dw, p.partial_rows, a.N);
+    }
     return cudaLaunchKernelEx(&cs, colsum_kernel, part, a.dw, p.partial_rows, a.N);
 }
 
