@@ -31,7 +31,6 @@ struct BwdTuning {
     int smem_single = 100 * 1024;  // shared memory aimed at, one group
     int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
     bool pipelined = false;        // cluster rows: pass 1 of the next row first
-    bool colsum_vec = false;       // column sum with 16-byte loads (N % 4 == 0)
 };
 
 int env_int(const char* name, int dflt) {
@@ -50,7 +49,6 @@ const BwdTuning& tuning() {
         u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
         u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
         u.pipelined = env_int("RMSNORM_BWD_PIPE", 0) != 0;
-        u.colsum_vec = env_int("RMSNORM_COLSUM_VEC", 0) != 0;
         return u;
     }();
     return t;
@@ -80,49 +78,6 @@ __global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ 
         dw[col] = t;
     }
 }
-// The same sum with 16-byte loads: thread (x, q) sums partial rows
-// p = q, q+32, ... of columns 4x .. 4x+3 (x = blockIdx.x*32 + threadIdx.x) in
-// ascending p, then the 32 sums of each column are added in q order. A
-// quarter of the blocks and loads of colsum_kernel. Needs N % 4 == 0 (rows
-// of the partial then start 16-byte aligned).
-__global__ void __launch_bounds__(1024) colsum_vec_kernel(const float* __restrict__ partial,
-                                                          float* __restrict__ dw, int P, int N) {
-    __shared__ float4 part[32][33];
-    wait_for_prerequisite_grid();  // partial rows complete and visible
-    const int cx = threadIdx.x, q = threadIdx.y;
-    const int64_t c4 = static_cast<int64_t>(blockIdx.x) * 32 + cx;  // float4 column index
-    const bool ok = c4 < N / 4;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok) {
-#pragma unroll 8
-        for (int p = q; p < P; p += 32) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(partial + static_cast<int64_t>(p) * N) + c4);
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
-        }
-    }
-    part[q][cx] = s;
-    __syncthreads();
-    if (q == 0 && ok) {
-        float4 t = part[0][cx];
-#pragma unroll
-        for (int i = 1; i < 32; ++i) {
-            const float4 v = part[i][cx];
-            t.x += v.x;
-            t.y += v.y;
-            t.z += v.z;
-            t.w += v.w;
-        }
-        float* o = dw + 4 * c4;  // dw is only 4-byte aligned: scalar stores
-        o[0] = t.x;
-        o[1] = t.y;
-        o[2] = t.z;
-        o[3] = t.w;
-    }
-}
-
 // ------------------------------------------------------------ host side
 const void* main_kernel_for(int dtype, const rmsnorm_plan_t& p, bool res) {
     const bool pipe = tuning().pipelined;
@@ -372,10 +327,6 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cs.attrs = pdl;
     cs.numAttrs = 1;
     const float* part = a.partial;
-    if (tuning().colsum_vec && a.N % 4 == 0) {
-        cs.gridDim = dim3(static_cast<unsigned>(cdiv(a.N / 4, 32)));
-        return cudaLaunchKernelEx(&cs, colsum_vec_kernel, part, a.dw, p.partial_rows, a.N);
-    }
     return cudaLaunchKernelEx(&cs, colsum_kernel, part, a.dw, p.partial_rows, a.N);
 }
 
