@@ -87,6 +87,20 @@ const void* bwd_res_kernel_f16_w_f32(const rmsnorm_plan_t& p, bool pipelined);
 
 namespace {
 
+// Stage of consecutive rows (or tiles) in an S-stage ring, and the parity of
+// the mbarrier phase that completes it, advanced one row at a time: no
+// division by the run-time S in the loops.
+struct RingPos {
+    int s = 0;
+    uint32_t parity = 0;
+    __device__ __forceinline__ void next(int S) {
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
+    }
+};
+
 __device__ __forceinline__ void group_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -158,8 +172,11 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     // Producer state, meaningful in the group's thread 0 only: stages with a
     // copy in flight and the parity of the phase that copy completes.
     uint32_t pending = 0, pending_parity = 0;
+    RingPos prod;  // ring position of the next row to issue (issued in order)
     auto issue = [&](int64_t t) {
-        const int s = static_cast<int>(t % S);
+        const int s = prod.s;
+        const uint32_t par = prod.parity;
+        prod.next(S);
         const int64_t row = vid + t * nvirt;
         if (bytes == 0) {
             mbar_arrive(&bar[s]);
@@ -172,7 +189,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
         if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
         pending |= 1u << s;
-        pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
+        pending_parity = (pending_parity & ~(1u << s)) | (par << s);
     };
     if (gt == 0)
         for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
@@ -212,10 +229,12 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     float r2 = nrows > 1 ? __ldg(a.rstd + vid + nvirt) : 0.f;
     bool failed = false;  // a copy wait ran out in this group
 
+    RingPos cons;  // ring position of row t
     for (int64_t t = 0; t < nrows; ++t) {
         const int64_t row = vid + t * nvirt;
-        const int s = static_cast<int>(t % S);
-        const uint32_t parity = static_cast<uint32_t>((t / S) & 1);
+        const int s = cons.s;
+        const uint32_t parity = cons.parity;
+        cons.next(S);
         const float r = r1;
         r1 = r2;
         if (t + 2 < nrows) r2 = __ldg(a.rstd + row + 2 * nvirt);
@@ -403,8 +422,11 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     if (csize > 1) cluster_sync_all();
 
     uint32_t pending = 0, pending_parity = 0;  // producer state (thread 0)
+    RingPos prod;  // ring position of the next row to issue (issued in order)
     auto issue = [&](int64_t t) {
-        const int s = static_cast<int>(t % S);
+        const int s = prod.s;
+        const uint32_t par = prod.parity;
+        prod.next(S);
         const int64_t row = cid + t * ncl;
         if (bytes == 0) {
             mbar_arrive(&bar[s]);
@@ -417,7 +439,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
         if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
         pending |= 1u << s;
-        pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
+        pending_parity = (pending_parity & ~(1u << s)) | (par << s);
     };
     if (tid == 0)
         for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
@@ -455,10 +477,13 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     bool xfailed = false;  // an exchange wait ran out in this thread
 
     // pass 1 of row t: wait for its copy, partial dot, warp sums to red[t&1]
+    RingPos pos1, pos2;  // ring positions of the rows of pass 1 and pass 2 (each in order)
     auto pass1 = [&](int64_t t) {
-        const int s = static_cast<int>(t % S);
+        const int s = pos1.s;
+        const uint32_t parity = pos1.parity;
+        pos1.next(S);
         if (!failed) {
-            if (mbar_wait_bounded(&bar[s], static_cast<uint32_t>((t / S) & 1), a.wait_limit_ns)) {
+            if (mbar_wait_bounded(&bar[s], parity, a.wait_limit_ns)) {
                 if (tid == 0) pending &= ~(1u << s);
             } else {
                 *fail = 1;
@@ -515,7 +540,8 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     };
     // pass 2 of row t: dx = r*(g - xhat*c), dw += dy*xhat
     auto pass2 = [&](int64_t t, float r, float tot) {
-        const int s = static_cast<int>(t % S);
+        const int s = pos2.s;
+        pos2.next(S);
         const unsigned char* xs = sx + s * unit;
         const unsigned char* ds = sdy + s * unit;
         const float c = r * (tot / static_cast<float>(N));
@@ -652,8 +678,11 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     __syncthreads();
 
     uint32_t pending = 0, pending_parity = 0;
+    RingPos prod;  // ring position of the next tile to issue (issued in order)
     auto issue = [&](int64_t t) {
-        const int s = static_cast<int>(t % S);
+        const int s = prod.s;
+        const uint32_t par = prod.parity;
+        prod.next(S);
         const int64_t tile = b + t * nb;
         const int64_t rows = min(static_cast<int64_t>(RT), a.M - tile * RT);
         const uint32_t bytes = static_cast<uint32_t>(rows * N * static_cast<int64_t>(sizeof(T)));
@@ -664,7 +693,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
         if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
         pending |= 1u << s;
-        pending_parity = (pending_parity & ~(1u << s)) | (static_cast<uint32_t>((t / S) & 1) << s);
+        pending_parity = (pending_parity & ~(1u << s)) | (par << s);
     };
     if (tid == 0)
         for (int64_t t = 0; t < S && t < count; ++t) issue(t);
@@ -696,10 +725,12 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     load_rstd(0, rnext);
     bool failed = false;
 
+    RingPos cons;  // ring position of tile t
     for (int64_t t = 0; t < count; ++t) {
         const int64_t tile = b + t * nb;
-        const int s = static_cast<int>(t % S);
-        const uint32_t parity = static_cast<uint32_t>((t / S) & 1);
+        const int s = cons.s;
+        const uint32_t parity = cons.parity;
+        cons.next(S);
         float rcur[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) rcur[r] = rnext[r];
