@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     const int64_t vid = cid * groups + g;       // virtual block of this group
     const int64_t nvirt = ncl * groups;
     const int N = a.N;
+    const float inv_n = 1.f / static_cast<float>(N);  // mean = sum * inv_n, one multiply a row
     const int nvec = N / VEC;
     const int slots = V * TG;
     const int vbeg = 0;
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             issue(t - 1 + S);
         }
         // mean_j(g * xhat) = rstd * mean_j(g * x)
-        const float c = r * (tot / static_cast<float>(N));
+        const float c = r * (tot * inv_n);
         const float2 r2 = f2_splat(r), nc2 = f2_splat(-c);
         T* dxr = DX + row * N;
         // pass 2: dx = r*(g - xhat*c) and dw += dy*xhat, re-reading the row
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     const int64_t cid = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
     const int64_t ncl = csize > 1 ? static_cast<int64_t>(cluster_count()) : gridDim.x;
     const int N = a.N;
+    const float inv_n = 1.f / static_cast<float>(N);  // mean = sum * inv_n, one multiply a row
     const int nvec = N / VEC;
     const int slots = V * nthr;
     const int vbeg = static_cast<int>(crank) * slots;
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         pos2.next(S);
         const unsigned char* xs = sx + s * unit;
         const unsigned char* ds = sdy + s * unit;
-        const float c = r * (tot / static_cast<float>(N));
+        const float c = r * (tot * inv_n);
         const float2 r2 = f2_splat(r), nc2 = f2_splat(-c);
         T* dxr = DX + (cid + t * ncl) * N;
 #pragma unroll
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     const int lane = tid % G, group = tid / G, groups = blockDim.x / G;
     const int RT = groups * R;
     const int N = a.N;
+    const float inv_n = 1.f / static_cast<float>(N);  // mean = sum * inv_n, one multiply a row
     const int nvec = N / VEC;
     const int64_t ntiles = (a.M + RT - 1) / RT;
     const int64_t b = blockIdx.x, nb = gridDim.x;
@@ -783,7 +786,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
             const int64_t row = tile * RT + lr;
             if (row >= a.M) continue;
             const float rs = rcur[r];
-            const float c = rs * (dot[r] / static_cast<float>(N));
+            const float c = rs * (dot[r] * inv_n);
             const float2 r2 = f2_splat(rs), nc2 = f2_splat(-c);
 #pragma unroll
             for (int j = 0; j < V; ++j) {
@@ -845,6 +848,7 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
     using P = Pack<T>;
     __shared__ float red[2][32];
     const int N = a.N;
+    const float inv_n = 1.f / static_cast<float>(N);  // mean = sum * inv_n, one multiply a row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const T* X = static_cast<const T*>(a.x);
     const T* DY = static_cast<const T*>(a.dy);
@@ -866,7 +870,7 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
         __syncthreads();
         float tot = lane < nw ? red[it & 1][lane] : 0.f;
         tot = group_allreduce<32>(tot);
-        const float c = r * (tot / static_cast<float>(N));
+        const float c = r * (tot * inv_n);
         T* dxr = DX + row * N;
         for (int col = threadIdx.x; col < N; col += blockDim.x) {
             const float d = to_f32(dyr[col]);

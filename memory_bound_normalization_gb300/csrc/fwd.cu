@@ -403,13 +403,14 @@ cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStrea
 template <typename T, typename TW>
 cudaError_t dispatch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     const int G = p.threads_per_row, V = p.vectors_per_thread;
-    if (G == 4 && V == 1) return launch_rowgroup<T, TW, 4, 1, 4>(p, a, s);
-    if (G == 4 && V == 2) return launch_rowgroup<T, TW, 4, 2, 4>(p, a, s);
-    if (G == 8 && V == 2) return launch_rowgroup<T, TW, 8, 2, 4>(p, a, s);
-    if (G == 8 && V == 4) return launch_rowgroup<T, TW, 8, 4, 2>(p, a, s);
-    if (G == 16 && V == 4) return launch_rowgroup<T, TW, 16, 4, 2>(p, a, s);
-    if (G == 32 && V == 4) return launch_rowgroup<T, TW, 32, 4, 1>(p, a, s);
-    if (G == 32 && V == 8) return launch_rowgroup<T, TW, 32, 8, 1>(p, a, s);
+    const int R = p.rows_per_unit / (p.threads / G);
+    if (G == 4 && V == 1 && R == 4) return launch_rowgroup<T, TW, 4, 1, 4>(p, a, s);
+    if (G == 4 && V == 2 && R == 2) return launch_rowgroup<T, TW, 4, 2, 2>(p, a, s);
+    if (G == 8 && V == 2 && R == 2) return launch_rowgroup<T, TW, 8, 2, 2>(p, a, s);
+    if (G == 8 && V == 4 && R == 1) return launch_rowgroup<T, TW, 8, 4, 1>(p, a, s);
+    if (G == 16 && V == 4 && R == 1) return launch_rowgroup<T, TW, 16, 4, 1>(p, a, s);
+    if (G == 32 && V == 4 && R == 1) return launch_rowgroup<T, TW, 32, 4, 1>(p, a, s);
+    if (G == 32 && V == 8 && R == 1) return launch_rowgroup<T, TW, 32, 8, 1>(p, a, s);
     return cudaErrorInvalidValue;
 }
 
