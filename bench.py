@@ -58,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--shape", default=None,
+                   help="M,N,dtype (bf16|f16|f32): an ad-hoc workload drawn like the width "
+                        "sweep's, in place of --workload")
     p.add_argument("--op", choices=["norm", "residual", "naive"], default="norm",
                    help="norm: rmsnorm_fwd + rmsnorm_bwd; residual: rmsnorm_add_fwd + "
                         "rmsnorm_add_bwd with dres (residual and dres drawn like x and dy); "
@@ -314,6 +317,19 @@ def cpu_baseline(wl, budget_s: float):
                       f"one host thread, {passes} pass(es), {total:.1f} s"}
 
 
+def pick_workload(synth, args):
+    """--shape M,N,dtype (x, dy ~ N(0,1), w = 1 + 0.1 N(0,1), eps 1e-5, fixed
+    seeds), else the named workload."""
+    if not args.shape:
+        return synth.WORKLOADS[args.workload]
+    import torch
+
+    m, n, dt = args.shape.split(",")
+    dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dt]
+    return synth.Workload(f"shape_{m}x{n}_{dt}", int(m), int(n), dtype, 1e-5, 51, 52, 53,
+                          about="ad-hoc shape")
+
+
 # ------------------------------------------------------------------ our arm
 
 def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_first=True,
@@ -455,7 +471,7 @@ def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_f
     region_ms = event_ms(region0, region1)
     return {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_mean": fwd_mean, "bwd_mean": bwd_mean,
             "step_ms": step_ms, "region_ms": region_ms, "nsets": nsets, "set_bytes": set_bytes,
-            "errs": errs, "base": base, "clock_info": clock_info}
+            "errs": errs, "base": base, "clock_info": clock_info, "dw0": outs[0]["dw"]}
 
 
 def run_ours(args):
@@ -473,7 +489,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
 
     pkg.load_library()  # raises if librmsnorm.so is missing
-    wl = synth.WORKLOADS[args.workload]
+    wl = pick_workload(synth, args)
     M, N, eps = wl.M, wl.N, wl.eps
     residual = args.op == "residual"
     naive = args.op == "naive"
@@ -513,7 +529,7 @@ def run_ours(args):
 
     # end to end through pinned host buffers
     e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes,
-                  args.op)
+                  args.op, ref_dw=cell["dw0"])
     if dist is not None:
         e2e["step_ms"] = slowest_rank(dist, [e2e["step_ms"]], base["x"].device)[0]
         e2e["value"] = round(replica_throughput(world, fwd_bytes + bwd_bytes, e2e["step_ms"]), 2)
@@ -666,64 +682,88 @@ def run_small_m(pkg, torch, steps: int = 200):
     return out
 
 
-def run_e2e(pkg, torch, wl, base, code, stream, steps, logical, op="norm"):
-    """Same work through the C ABI with the inputs in pinned host memory: each
-    step copies x, w, dy (and the residual and dres) to the device, runs
-    forward and backward, and copies y, rstd, dx, dw (and h) back."""
+def run_e2e(pkg, torch, wl, base, code, stream, steps, logical, op="norm", ref_dw=None):
+    """Same work through the C ABI with the inputs in pinned host memory:
+    every step copies x, w, dy (and the residual and dres) to the device,
+    runs forward and backward, and copies y, rstd, dx, dw (and h) back.
+    Steps are independent batches, so they are pipelined over two device
+    buffer slots: the inputs of a step go in on one copy stream while the
+    previous step's results come out on another and the GPU computes in
+    between, using both directions of the host link at once. The timed
+    region runs from the first input copy to the last result copy."""
     M, N, eps = wl.M, wl.N, wl.eps
     residual = op == "residual"
     names = ["x", "w", "dy"] + (["res", "dres"] if residual else [])
+    outn = ["y", "rstd", "dx", "dw"] + (["h"] if residual else [])
     host = {k: base[k].cpu().pin_memory() for k in names}
-    dev = {k: torch.empty_like(base[k]) for k in names}
-    y, dx = torch.empty_like(base["x"]), torch.empty_like(base["x"])
-    h = torch.empty_like(base["x"]) if residual else None
-    rstd = torch.empty(M, dtype=torch.float32, device=base["x"].device)
-    dw = torch.empty(N, dtype=torch.float32, device=base["x"].device)
-    hx = host["x"]
-    hy, hdx = torch.empty_like(hx).pin_memory(), torch.empty_like(hx).pin_memory()
-    hh = torch.empty_like(hx).pin_memory() if residual else None
-    hr = torch.empty(M, dtype=torch.float32).pin_memory()
-    hdw = torch.empty(N, dtype=torch.float32).pin_memory()
+    dev_in = [{k: torch.empty_like(base[k]) for k in names} for _ in range(2)]
+    x0 = base["x"]
 
-    def step():
-        for k in names:
-            dev[k].copy_(host[k], non_blocking=True)
+    def outs():
+        o = {"y": torch.empty_like(x0), "dx": torch.empty_like(x0),
+             "rstd": torch.empty(M, dtype=torch.float32, device=x0.device),
+             "dw": torch.empty(N, dtype=torch.float32, device=x0.device)}
         if residual:
-            pkg.check(pkg.rmsnorm_add_fwd(dev["x"], dev["res"], dev["w"], h, y, rstd, M, N, eps,
-                                          code, stream))
-            pkg.check(pkg.rmsnorm_add_bwd(h, dev["w"], dev["dy"], rstd, dev["dres"], dx, dw, M,
-                                          N, code, stream))
-            hh.copy_(h, non_blocking=True)
-        elif op == "naive":
-            pkg.check(pkg.rmsnorm_fwd(dev["x"], dev["w"], y, rstd, M, N, eps, code, stream))
-            pkg.check(pkg.rmsnorm_bwd_naive(dev["x"], dev["w"], dev["dy"], dx, dw, M, N, eps, code,
-                                            stream))
-        else:
-            pkg.check(pkg.rmsnorm_fwd(dev["x"], dev["w"], y, rstd, M, N, eps, code, stream))
-            pkg.check(pkg.rmsnorm_bwd(dev["x"], dev["w"], dev["dy"], rstd, dx, dw, M, N, code,
-                                      stream))
-        hy.copy_(y, non_blocking=True)
-        hr.copy_(rstd, non_blocking=True)
-        hdx.copy_(dx, non_blocking=True)
-        hdw.copy_(dw, non_blocking=True)
+            o["h"] = torch.empty_like(x0)
+        return o
 
-    for _ in range(3):
-        step()
+    dev_out = [outs(), outs()]
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in dev_out[0].items()}
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    cmp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+
+    def compute(d, o):
+        if residual:
+            pkg.check(pkg.rmsnorm_add_fwd(d["x"], d["res"], d["w"], o["h"], o["y"], o["rstd"], M,
+                                          N, eps, code, stream))
+            pkg.check(pkg.rmsnorm_add_bwd(o["h"], d["w"], d["dy"], o["rstd"], d["dres"], o["dx"],
+                                          o["dw"], M, N, code, stream))
+        elif op == "naive":
+            pkg.check(pkg.rmsnorm_fwd(d["x"], d["w"], o["y"], o["rstd"], M, N, eps, code, stream))
+            pkg.check(pkg.rmsnorm_bwd_naive(d["x"], d["w"], d["dy"], o["dx"], o["dw"], M, N, eps,
+                                            code, stream))
+        else:
+            pkg.check(pkg.rmsnorm_fwd(d["x"], d["w"], o["y"], o["rstd"], M, N, eps, code, stream))
+            pkg.check(pkg.rmsnorm_bwd(d["x"], d["w"], d["dy"], o["rstd"], o["dx"], o["dw"], M, N,
+                                      code, stream))
+
+    def step(k):
+        b = k % 2
+        s_in.wait_event(cmp_done[b])  # the compute that read this input slot is done
+        with torch.cuda.stream(s_in):
+            for n in names:
+                dev_in[b][n].copy_(host[n], non_blocking=True)
+        in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        stream.wait_event(out_done[b])  # the copy-out of this output slot is done
+        compute(dev_in[b], dev_out[b])
+        cmp_done[b].record(stream)
+        s_out.wait_event(cmp_done[b])
+        with torch.cuda.stream(s_out):
+            for n in outn:
+                host_out[n].copy_(dev_out[b][n], non_blocking=True)
+        out_done[b].record(s_out)
+
+    for k in range(3):
+        step(k)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    for k in range(steps):
+        step(k)
+    e1.record(s_out)  # every step's copy-out is ordered before it on s_out
     torch.cuda.synchronize()
     ms = event_ms(e0, e1) / steps
+    if ref_dw is not None and not torch.equal(host_out["dw"], ref_dw.cpu()):
+        raise SystemExit("end-to-end dw differs from the device-resident run on the same inputs")
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hr, hdw))
-    if residual:
-        d2h += hh.numel() * hh.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     return {"value": round(logical / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "step_ms": round(ms, 4), "steps": steps}
+            "step_ms": round(ms, 4), "steps": steps,
+            "pipeline": "two buffer slots; copies in and out on their own streams"}
 
 
 # ------------------------------------------------------------ reference arm
@@ -740,7 +780,7 @@ def run_reference(args):
     from memory_bound_normalization_gb300 import synth
 
     oracle.build()
-    wl = synth.WORKLOADS[args.workload]
+    wl = pick_workload(synth, args)
     elem = torch.empty(0, dtype=wl.dtype).element_size()
     w_elem = torch.empty(0, dtype=wl.weight_dtype).element_size()
     rows_avail = min(wl.M, 2048)
