@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ 
                                                       float* __restrict__ dw, int P, int N) {
     __shared__ float part[32][33];
     wait_for_prerequisite_grid();  // partial rows complete and visible
+    allow_dependent_launch();
     const int cx = threadIdx.x, q = threadIdx.y;
     const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + cx;
     float s = 0.f;
@@ -301,14 +302,17 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
     cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (p.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     BwdArgs args = a;
     int stages = p.stages, groups = p.row_groups;

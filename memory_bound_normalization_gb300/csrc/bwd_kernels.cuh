@@ -105,13 +105,6 @@ __device__ __forceinline__ void group_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Lets the dependent column-sum grid launch while this grid finishes.
-__device__ __forceinline__ void allow_dependent_launch() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void wait_for_prerequisite_grid() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 // ------------------------------------------------------ row groups per block
 // A block holds `groups` independent row groups of TG = blockDim.x / groups
@@ -169,6 +162,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         fence_mbarrier_init();
     }
     __syncthreads();
+    wait_for_prerequisite_grid();  // no global access before this
 
     // Producer state, meaningful in the group's thread 0 only: stages with a
     // copy in flight and the parity of the phase that copy completes.
@@ -422,6 +416,7 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     __syncthreads();
     // every block's barriers must exist before any peer arrives on them
     if (csize > 1) cluster_sync_all();
+    wait_for_prerequisite_grid();  // no global access before this
 
     uint32_t pending = 0, pending_parity = 0;  // producer state (thread 0)
     RingPos prod;  // ring position of the next row to issue (issued in order)
@@ -679,6 +674,7 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         fence_mbarrier_init();
     }
     __syncthreads();
+    wait_for_prerequisite_grid();  // no global access before this
 
     uint32_t pending = 0, pending_parity = 0;
     RingPos prod;  // ring position of the next tile to issue (issued in order)
@@ -856,6 +852,7 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
     T* DX = static_cast<T*>(a.dx);
     const T* DRES = static_cast<const T*>(a.dres);
     float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
+    wait_for_prerequisite_grid();  // no global access before this
     for (int col = threadIdx.x; col < N; col += blockDim.x) prow[col] = 0.f;
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, ++it) {

@@ -425,6 +425,22 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     }
 }
 
+// ------------------------------------------ programmatic dependent launch
+// Every library kernel is launched with programmatic stream serialization:
+// it may start while the previous kernel of the stream finishes, does only
+// work that touches no global memory (index math, shared-memory and
+// mbarrier set-up), then waits for the prerequisite grid -- its completion
+// and the visibility of its memory -- before the first global load or store.
+// Without a programmatic edge the wait returns at once.
+__device__ __forceinline__ void wait_for_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream launch while this grid finishes; that
+// kernel still waits for this grid's completion before touching memory.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Records the first failure on the device status word.
 __device__ __forceinline__ void report_status(int* status, int code) {
     if (status != nullptr) atomicCAS(status, 0, code);

@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
     const int group = threadIdx.x / G;
     const int groups = blockDim.x / G;
     const int64_t tile = static_cast<int64_t>(blockIdx.x) * groups * R;
+    wait_for_prerequisite_grid();  // no global access before this
 
     uint4 xv[R][V];
 #pragma unroll
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
         }
         if (lane == 0) rstd[row] = rs;
     }
+    allow_dependent_launch();
 }
 
 // ------------------------------------------------------- block/cluster per row
@@ -177,6 +179,7 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
         }
         cluster_arrive_relaxed();  // waited for below, after the loads
     }
+    wait_for_prerequisite_grid();  // no global access before this
     using WP = WPack<T, TW>;
     uint4 xv[V], wv[V][WP::WORDS];
 #pragma unroll
@@ -248,6 +251,7 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
         st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
     }
     if (crank == 0 && threadIdx.x == 0) rstd[row] = rs;
+    allow_dependent_launch();
 }
 
 // ---------------------------------------------------------------- wide rows
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
     const int nvec = N / VEC;
     const uint64_t keep = l2_policy_evict_last();
     const uint64_t last = l2_policy_evict_first();
+    wait_for_prerequisite_grid();  // no global access before this
     int it = 0;
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
         const T* xr = x + row * N;
@@ -348,6 +353,7 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
         }
         if (tid == 0) rstd[row] = rs;
     }
+    allow_dependent_launch();
 }
 
 // -------------------------------------------------------------------- scalar
@@ -362,6 +368,7 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* x, const TW* _
     using P = Pack<T>;
     __shared__ float red[2][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    wait_for_prerequisite_grid();  // no global access before this
     int it = 0;
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
         const T* xr = x + row * N;
@@ -394,10 +401,9 @@ template <typename T, typename TW, int G, int V, int R>
 cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     auto fn = a.res != nullptr ? fwd_rowgroup_kernel<T, TW, G, V, R, true>
                                : fwd_rowgroup_kernel<T, TW, G, V, R, false>;
-    fn<<<p.grid, p.threads, 0, s>>>(static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
-                                    static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
-                                    static_cast<const T*>(a.res), static_cast<T*>(a.h));
-    return cudaGetLastError();
+    return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
+                      static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                      static_cast<const T*>(a.res), static_cast<T*>(a.h));
 }
 
 template <typename T, typename TW>
@@ -416,24 +422,11 @@ cudaError_t dispatch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStr
 
 template <typename T, typename TW, int V>
 cudaError_t launch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(p.threads));
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    if (p.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
     auto fn = a.res != nullptr ? fwd_row_kernel<T, TW, V, true> : fwd_row_kernel<T, TW, V, false>;
-    return cudaLaunchKernelEx(&cfg, fn, static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
-                              static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps, a.status,
-                              a.wait_limit_ns, static_cast<const T*>(a.res), static_cast<T*>(a.h));
+    return launch_pdl(fn, p.grid, p.threads, 0, p.cluster, s, static_cast<const T*>(a.x),
+                      static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                      a.status, a.wait_limit_ns, static_cast<const T*>(a.res),
+                      static_cast<T*>(a.h));
 }
 
 template <typename T, typename TW>
@@ -445,10 +438,9 @@ template <typename T, typename TW>
 cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
     if (p.variant == RMSNORM_VARIANT_TWO_PASS) {
         auto fn = a.res != nullptr ? fwd_wide_kernel<T, TW, 4, true> : fwd_wide_kernel<T, TW, 4, false>;
-        fn<<<p.grid, p.threads, 0, s>>>(static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
-                                        static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
-                                        static_cast<const T*>(a.res), static_cast<T*>(a.h));
-        return cudaGetLastError();
+        return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
+                          static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
+                          a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h));
     }
     switch (p.variant) {
         case RMSNORM_VARIANT_ROWGROUP: return dispatch_rowgroup<T, TW>(p, a, s);
@@ -457,10 +449,9 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
         case RMSNORM_VARIANT_SCALAR:
         {
             auto fn = a.res != nullptr ? fwd_scalar_kernel<T, TW, true> : fwd_scalar_kernel<T, TW, false>;
-            fn<<<p.grid, p.threads, 0, s>>>(static_cast<const T*>(a.x), static_cast<const TW*>(a.w),
-                                            static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
-                                            static_cast<const T*>(a.res), static_cast<T*>(a.h));
-            return cudaGetLastError();
+            return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
+                              static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
+                              a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h));
         }
         default: return cudaErrorInvalidValue;
     }

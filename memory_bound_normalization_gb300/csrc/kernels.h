@@ -52,6 +52,32 @@ struct BwdArgs {
 
 constexpr int kMaxCluster = 8;
 
+// Launches a library kernel with programmatic stream serialization (it may
+// start while the previous kernel of the stream finishes; the kernel waits
+// for it before touching memory) and, for cluster > 1, a cluster shape.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*fn)(KArgs...), int grid, int threads, size_t smem, int cluster,
+                       cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
+}
+
 // Width-dependent choices (host only, no device queries). `vector_ok` says
 // whether the pointers and N allow 16-byte vector access.
 void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);

@@ -72,3 +72,49 @@ def test_graph_replay_matches_eager(M, N, dtype, w_dtype):
         for got, want in zip((y, rstd, dx, dw), ref):
             assert torch.equal(got, want)
     assert pkg.rmsnorm_get_last_device_error() == pkg.OK
+
+
+RES_CASES = [(1, 4096, torch.bfloat16), (256, 1024, torch.bfloat16), (300, 128, torch.float16),
+             (8, 65536, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("M,N,dtype", RES_CASES,
+                         ids=[f"{m}x{n}-{str(d)[6:]}" for m, n, d in RES_CASES])
+def test_graph_replay_residual_in_place(M, N, dtype):
+    """The residual pair captured with the sum written over the residual and
+    dx over dres (as a serving step would) replays like the eager calls."""
+    wl = synth.Workload(f"graphres{M}x{N}", M, N, dtype, 1e-6, 64, 65, 66)
+    a = synth.make_inputs(wl, device=DEV)
+    b = synth.make_inputs(synth.Workload("r", M, N, dtype, 1e-6, 67, 68, 69), device=DEV)
+    x, w, dy = a["x"], a["w"], a["dy"]
+    res0, dres0 = b["x"].clone(), b["dy"].clone()
+    code = pkg.dtype_code(dtype)
+    res, dres = torch.empty_like(res0), torch.empty_like(dres0)
+    y = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=DEV)
+    dw = torch.empty(N, dtype=torch.float32, device=DEV)
+
+    def step(stream):
+        res.copy_(res0)
+        dres.copy_(dres0)
+        pkg.check(pkg.rmsnorm_add_fwd(x, res, w, res, y, rstd, M, N, wl.eps, code, stream))
+        pkg.check(pkg.rmsnorm_add_bwd(res, w, dy, rstd, dres, dres, dw, M, N, code, stream))
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (res, y, rstd, dres, dw)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(torch.cuda.current_stream())
+    for _ in range(3):
+        for t in (y, rstd, dw):
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for got, want in zip((res, y, rstd, dres, dw), ref):
+            assert torch.equal(got, want)
+    assert pkg.rmsnorm_get_last_device_error() == pkg.OK
