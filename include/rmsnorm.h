@@ -260,14 +260,18 @@ typedef enum {
     RMSNORM_VARIANT_CTA_ROW = 2,   /* one thread block per row */
     RMSNORM_VARIANT_CLUSTER_ROW = 3, /* a thread-block cluster per row */
     RMSNORM_VARIANT_SCALAR = 4,    /* unaligned or ragged rows */
-    RMSNORM_VARIANT_TWO_PASS = 5   /* wide rows (forward): a block per row,
+    RMSNORM_VARIANT_TWO_PASS = 5,  /* wide rows (forward): a block per row,
                                       two passes, the second served by L2 */
+    RMSNORM_VARIANT_RING = 6       /* wide rows (forward): persistent blocks
+                                      (or clusters) with a ring of row slices
+                                      moved by bulk copies */
 } rmsnorm_variant_t;
 
 typedef enum {
     RMSNORM_PASS_FWD = 0,     /* rmsnorm_fwd and rmsnorm_add_fwd */
     RMSNORM_PASS_BWD = 1,     /* rmsnorm_bwd, and rmsnorm_add_bwd without dres */
-    RMSNORM_PASS_BWD_RES = 2  /* rmsnorm_add_bwd with dres */
+    RMSNORM_PASS_BWD_RES = 2, /* rmsnorm_add_bwd with dres */
+    RMSNORM_PASS_FWD_ADD = 3  /* rmsnorm_add_fwd */
 } rmsnorm_pass_t;
 
 typedef struct {

@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     PASS_BWD,
     PASS_BWD_RES,
     PASS_FWD,
+    PASS_FWD_ADD,
     PROBE_2R1W,
     PROBE_COPY,
     PROBE_WRITE,

@@ -34,13 +34,14 @@ ERR_DEVICE_TIMEOUT = 6
 PASS_FWD = 0
 PASS_BWD = 1
 PASS_BWD_RES = 2  # rmsnorm_add_bwd with dres
+PASS_FWD_ADD = 3  # rmsnorm_add_fwd
 
 PROBE_COPY = 0
 PROBE_WRITE = 1
 PROBE_2R1W = 2
 
 VARIANTS = {0: "none", 1: "rowgroup", 2: "cta_row", 3: "cluster_row", 4: "scalar",
-            5: "two_pass"}
+            5: "two_pass", 6: "ring"}
 
 # Exported symbols, in header order (tests check the library against this
 # list and the header against the library).

@@ -113,11 +113,11 @@ int fwd_run(const void* x, const void* res, const void* w, void* h, void* y, flo
     const bool vec = aligned(x, 16) && aligned(w, 16) && aligned(y, 16) && (N * sz) % 16 == 0 &&
                      (N * wsz) % 16 == 0 && (!add || (aligned(res, 16) && aligned(h, 16)));
     rmsnorm_plan_t plan;
-    fwd_choose(N, dtype, vec, &plan);
+    fwd_choose(N, dtype, vec, &plan, add);
     const DeviceInfo* dev = nullptr;
     st = current_device(&dev);
     if (st != RMSNORM_OK) return st;
-    st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan));
+    st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan, add));
     if (st != RMSNORM_OK) return st;
     if (static_cast<int64_t>(plan.grid) <= 0 ||
         ((plan.variant == RMSNORM_VARIANT_ROWGROUP || plan.variant == RMSNORM_VARIANT_CTA_ROW ||
@@ -324,21 +324,21 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     if (out == nullptr) return RMSNORM_ERR_INVALID_ARG;
     int st = shape_status(M, N, dtype);
     if (st != RMSNORM_OK) return st;
-    if (pass != RMSNORM_PASS_FWD && pass != RMSNORM_PASS_BWD && pass != RMSNORM_PASS_BWD_RES)
-        return RMSNORM_ERR_INVALID_ARG;
+    if (pass < RMSNORM_PASS_FWD || pass > RMSNORM_PASS_FWD_ADD) return RMSNORM_ERR_INVALID_ARG;
+    const bool fwd = pass == RMSNORM_PASS_FWD || pass == RMSNORM_PASS_FWD_ADD;
     if (M == 0) {
         *out = rmsnorm_plan_t{};
         return RMSNORM_OK;
     }
     const bool vec = (N * dtype_size(dtype)) % 16 == 0;
-    if (pass == RMSNORM_PASS_FWD)
-        fwd_choose(N, dtype, vec, out);
+    if (fwd)
+        fwd_choose(N, dtype, vec, out, pass == RMSNORM_PASS_FWD_ADD);
     else
         bwd_choose(N, dtype, vec, out, pass == RMSNORM_PASS_BWD_RES);
     if (device < 0) return RMSNORM_OK;
     const DeviceInfo* dev = device_info(device);
     if (!dev) return RMSNORM_ERR_CUDA;
-    cudaError_t e = pass == RMSNORM_PASS_FWD ? fwd_finish_plan(*dev, dtype, M, out)
+    cudaError_t e = fwd ? fwd_finish_plan(*dev, dtype, M, out, pass == RMSNORM_PASS_FWD_ADD)
                                              : bwd_finish_plan(*dev, dtype, M, N, out,
                                                                pass == RMSNORM_PASS_BWD_RES);
     return cuda_status(e);

@@ -31,6 +31,7 @@ struct BwdTuning {
     int smem_single = 100 * 1024;  // shared memory aimed at, one group
     int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
     bool pipelined = false;        // cluster rows: pass 1 of the next row first
+    int rowgroup_max_vec = 256;    // widest row (16-byte vectors) for the short-row kernel
 };
 
 int env_int(const char* name, int dflt) {
@@ -49,6 +50,7 @@ const BwdTuning& tuning() {
         u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
         u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
         u.pipelined = env_int("RMSNORM_BWD_PIPE", 0) != 0;
+        u.rowgroup_max_vec = std::max(0, std::min(256, env_int("RMSNORM_BWD_ROWGROUP_MAX_VEC", 256)));
         return u;
     }();
     return t;
@@ -192,7 +194,7 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
     const int nt = res ? 3 : 2;          // tensors in a ring stage
     const int min_stages = res ? 2 : 3;
     GroupShape g;
-    if (vector_ok && bwd_group_shape(nvec, &g)) {
+    if (vector_ok && nvec <= tu.rowgroup_max_vec && bwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
         p->threads = g.threads;
         p->threads_per_row = g.G;

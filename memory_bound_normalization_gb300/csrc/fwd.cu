@@ -24,7 +24,10 @@
 // coherent loads.
 #include <algorithm>
 #include <cstdlib>
+#include <map>
+#include <mutex>
 #include <string>
+#include <tuple>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -356,6 +359,197 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
     allow_dependent_launch();
 }
 
+// ------------------------------------------------- wide rows, persistent ring
+// Shared memory of the ring kernel: [S][unit] x | ([S][unit] residual) |
+// mbarrier[S] (copies) | mbarrier[4] (cluster exchange) | reduction slots
+// [2][32] | exchange slots [4][kMaxCluster] | failure flag.
+__host__ __device__ inline int fwd_ring_smem_bytes(int stages, int unit, int nt) {
+    return nt * stages * unit + stages * 8 + 4 * 8 + 64 * 4 + 4 * kMaxCluster * 4 + 16;
+}
+
+// Rows too wide for one block's registers, persistent: cluster cid (a single
+// block when launched without clusters) walks rows cid, cid + ncl, ...; block
+// rank q of the cluster owns vector slots [q*V*T, (q+1)*V*T) of every row.
+// The slices of the coming rows arrive by 1-D bulk copies into an S-stage
+// shared-memory ring, completion counted on an mbarrier. Per row: the slice
+// moves from shared memory into registers (with ADD, h = x + res is formed
+// and stored there), the sum of squares is reduced over the block, the block
+// barrier frees the stage, which is refilled with row t + S at once, the
+// blocks of a cluster exchange their sums by st.async into a 4-slot ring of
+// exchange slots (as in the wide backward: a block sends row t + 1 only after
+// receiving every sum of row t, so a writer is at most three rows ahead of a
+// reader), and y is scaled from registers. Every wait is bounded.
+template <typename T, typename TW, int V, bool ADD>
+__global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __restrict__ w,
+                                                      T* __restrict__ y, float* __restrict__ rstd,
+                                                      int64_t M, int N, float eps, int stages,
+                                                      int* status, uint64_t wait_limit_ns,
+                                                      const T* res, T* hout) {
+    using P = Pack<T>;
+    using WP = WPack<T, TW>;
+    constexpr int VEC = P::VEC;
+    constexpr int PR = P::PAIRS;
+    constexpr int NT = ADD ? 2 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int nthr = blockDim.x, tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    const uint32_t csize = cluster_size();
+    const uint32_t crank = csize > 1 ? cluster_rank() : 0u;
+    const int64_t cid = csize > 1 ? static_cast<int64_t>(cluster_index()) : blockIdx.x;
+    const int64_t ncl = csize > 1 ? static_cast<int64_t>(cluster_count()) : gridDim.x;
+    const float inv_n = 1.f / static_cast<float>(N);
+    const int nvec = N / VEC;
+    const int slots = V * nthr;
+    const int vbeg = static_cast<int>(crank) * slots;
+    const int vcnt = max(0, min(slots, nvec - vbeg));
+    const uint32_t bytes = static_cast<uint32_t>(vcnt) * 16u;
+    const int S = stages;
+    const int unit = slots * 16;
+
+    unsigned char* sx = smem;
+    unsigned char* sr = smem + S * unit;  // residual (ADD only)
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + NT * S * unit);
+    uint64_t* xbar = bar + S;                          // [4]
+    float* red = reinterpret_cast<float*>(xbar + 4);  // [2][32]
+    float* xslot = red + 64;                           // [4][kMaxCluster]
+    volatile int* fail = reinterpret_cast<volatile int*>(xslot + 4 * kMaxCluster);
+
+    const int64_t nrows = cid < M ? (M - 1 - cid) / ncl + 1 : 0;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+        for (int b = 0; b < 4; ++b) mbar_init(&xbar[b], 1);
+        *fail = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    // every block's barriers must exist before any peer arrives on them
+    if (csize > 1) cluster_sync_all();
+    wait_for_prerequisite_grid();  // no global access before this
+
+    uint32_t pending = 0, pending_parity = 0;  // producer state (thread 0)
+    int ps = 0;
+    uint32_t ppar = 0;  // ring position of the next row to issue (issued in order)
+    auto issue = [&](int64_t t) {
+        const int s = ps;
+        const uint32_t par = ppar;
+        if (++ps == S) {
+            ps = 0;
+            ppar ^= 1u;
+        }
+        if (bytes == 0) {
+            mbar_arrive(&bar[s]);
+            return;
+        }
+        mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
+        const int64_t off = (cid + t * ncl) * N + static_cast<int64_t>(vbeg) * VEC;
+        bulk_copy_g2s(sx + s * unit, x + off, bytes, &bar[s]);
+        if constexpr (ADD) bulk_copy_g2s(sr + s * unit, res + off, bytes, &bar[s]);
+        pending |= 1u << s;
+        pending_parity = (pending_parity & ~(1u << s)) | (par << s);
+    };
+    if (tid == 0)
+        for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
+
+    uint4 wv[V][WP::WORDS];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int k = j * nthr + tid;
+        if (k < vcnt) WP::load(w, vbeg + k, wv[j]);
+        else WP::zero(wv[j]);
+    }
+
+    bool failed = false, xfailed = false;
+    int cs = 0;
+    uint32_t cpar = 0;  // ring position of row t
+    for (int64_t t = 0; t < nrows; ++t) {
+        const int64_t row = cid + t * ncl;
+        const int s = cs;
+        const uint32_t parity = cpar;
+        if (++cs == S) {
+            cs = 0;
+            cpar ^= 1u;
+        }
+        if (!failed) {
+            if (mbar_wait_bounded(&bar[s], parity, wait_limit_ns)) {
+                if (tid == 0) pending &= ~(1u << s);
+            } else {
+                *fail = 1;
+                report_status(status, kStatusTimeout);
+            }
+        }
+        // the slice into registers (h = x + res with ADD, stored to global)
+        uint4 xv[V];
+        float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * nthr + tid;
+            xv[j] = k < vcnt ? ld_shared_16(sx + s * unit + k * 16) : make_uint4(0, 0, 0, 0);
+            if constexpr (ADD) {
+                if (k < vcnt) {
+                    xv[j] = add_vec<T>(xv[j], ld_shared_16(sr + s * unit + k * 16));
+                    st_global_16(hout + row * N + static_cast<int64_t>(vbeg + k) * VEC, xv[j]);
+                }
+            }
+            float2 f[PR];
+            P::unpack2(xv[j], f);
+#pragma unroll
+            for (int e = 0; e < PR; ++e) ss2 = __ffma2_rn(f[e], f[e], ss2);
+        }
+        const float part = group_allreduce<32>(ss2.x + ss2.y);
+        if (lane == 0) red[(t & 1) * 32 + warp] = part;
+        __syncthreads();  // the stage is read; the warp sums of row t are published
+        failed = *fail != 0;
+        if (tid == 0 && !failed && t + S < nrows) {
+            fence_proxy_async_shared();
+            issue(t + S);
+        }
+        float tot = lane < nw ? red[(t & 1) * 32 + lane] : 0.f;
+        tot = group_allreduce<32>(tot);
+        if (csize > 1) {
+            const int b = static_cast<int>(t & 3);
+            // this block expects the C sums of row t as 4*C transaction bytes
+            if (tid == 0) mbar_arrive_expect_tx(&xbar[b], 4u * csize);
+            if (static_cast<uint32_t>(tid) < csize) {
+                const uint32_t q = static_cast<uint32_t>(tid);  // thread q sends to block q
+                st_async_cluster_f32(cluster_map(&xslot[b * kMaxCluster + crank], q), tot,
+                                     cluster_map(&xbar[b], q));
+            }
+            if (!xfailed &&
+                !mbar_wait_cluster_bounded(&xbar[b], static_cast<uint32_t>((t >> 2) & 1), wait_limit_ns)) {
+                xfailed = true;  // later exchanges are not waited for again
+                *fail = 1;
+                report_status(status, kStatusTimeout);
+            }
+            tot = 0.f;
+            for (uint32_t q = 0; q < csize; ++q) tot += xslot[b * kMaxCluster + q];
+        }
+        const float rs = rsqrtf(tot * inv_n + eps);
+        const float2 rs2 = f2_splat(rs);
+        T* yr = y + row * N;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * nthr + tid;
+            if (k >= vcnt) continue;
+            float2 fx[PR], fw[PR], fy[PR];
+            P::unpack2(xv[j], fx);
+            WP::unpack2(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
+            st_global_16(yr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(fy));
+        }
+        if (crank == 0 && tid == 0) rstd[row] = rs;
+    }
+    allow_dependent_launch();
+    // after a failure, let copies already in flight land before going on
+    if (tid == 0 && failed)
+        for (int s = 0; s < S; ++s)
+            if ((pending >> s) & 1u) mbar_wait_bounded(&bar[s], (pending_parity >> s) & 1u, wait_limit_ns);
+    // no block may leave while a peer can still reach its shared memory
+    if (csize > 1) cluster_sync_all();
+}
+
 // -------------------------------------------------------------------- scalar
 // Any alignment, any N: one block per row (grid-strided over rows), two
 // passes over the row with scalar loads.
@@ -435,7 +629,47 @@ cudaError_t dispatch_row(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t
 }
 
 template <typename T, typename TW>
+const void* ring_kernel(int V, bool add) {
+    if (V == 4) return add ? reinterpret_cast<const void*>(&fwd_ring_kernel<T, TW, 4, true>)
+                           : reinterpret_cast<const void*>(&fwd_ring_kernel<T, TW, 4, false>);
+    if (V == 8) return add ? reinterpret_cast<const void*>(&fwd_ring_kernel<T, TW, 8, true>)
+                           : reinterpret_cast<const void*>(&fwd_ring_kernel<T, TW, 8, false>);
+    return nullptr;
+}
+
+const void* ring_kernel_for(int dtype, int V, bool add) {
+    switch (dtype) {
+        case RMSNORM_BF16: return ring_kernel<__nv_bfloat16, __nv_bfloat16>(V, add);
+        case RMSNORM_F16: return ring_kernel<__half, __half>(V, add);
+        case RMSNORM_BF16_W_F32: return ring_kernel<__nv_bfloat16, float>(V, add);
+        case RMSNORM_F16_W_F32: return ring_kernel<__half, float>(V, add);
+        case RMSNORM_F32: return ring_kernel<float, float>(V, add);
+        default: return nullptr;
+    }
+}
+
+template <typename T, typename TW, int V, bool ADD>
+cudaError_t launch_ring(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    return launch_pdl(fwd_ring_kernel<T, TW, V, ADD>, p.grid, p.threads,
+                      static_cast<size_t>(p.smem_bytes), p.cluster, s, static_cast<const T*>(a.x),
+                      static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                      p.stages, a.status, a.wait_limit_ns, static_cast<const T*>(a.res),
+                      static_cast<T*>(a.h));
+}
+
+template <typename T, typename TW>
+cudaError_t dispatch_ring(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    const bool add = a.res != nullptr;
+    if (p.vectors_per_thread == 4)
+        return add ? launch_ring<T, TW, 4, true>(p, a, s) : launch_ring<T, TW, 4, false>(p, a, s);
+    if (p.vectors_per_thread == 8)
+        return add ? launch_ring<T, TW, 8, true>(p, a, s) : launch_ring<T, TW, 8, false>(p, a, s);
+    return cudaErrorInvalidValue;
+}
+
+template <typename T, typename TW>
 cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
+    if (p.variant == RMSNORM_VARIANT_RING) return dispatch_ring<T, TW>(p, a, s);
     if (p.variant == RMSNORM_VARIANT_TWO_PASS) {
         auto fn = a.res != nullptr ? fwd_wide_kernel<T, TW, 4, true> : fwd_wide_kernel<T, TW, 4, false>;
         return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
@@ -457,20 +691,75 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
     }
 }
 
+// Resident blocks (or clusters) of a ring kernel configuration, cached per
+// (device, kernel, shape) so every call sees the same persistent grid; the
+// kernel is opted into the device's largest dynamic shared memory once.
+std::mutex g_ring_mu;
+std::map<std::tuple<int, const void*, int, int, int>, int> g_ring_units;
+std::map<std::pair<int, const void*>, bool> g_ring_optin;
+
+cudaError_t ring_resident_units(const DeviceInfo& dev, const void* fn, int threads, int smem,
+                                int cluster, int* out) {
+    std::lock_guard<std::mutex> lk(g_ring_mu);
+    const auto key = std::make_tuple(dev.device, fn, threads, smem, cluster);
+    auto it = g_ring_units.find(key);
+    if (it != g_ring_units.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    cudaError_t err = cudaSuccess;
+    if (!g_ring_optin[std::make_pair(dev.device, fn)]) {
+        cudaFuncAttributes fa;
+        err = cudaFuncGetAttributes(&fa, fn);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       dev.max_smem_optin - static_cast<int>(fa.sharedSizeBytes));
+        if (err != cudaSuccess) return err;
+        g_ring_optin[std::make_pair(dev.device, fn)] = true;
+    }
+    int units = 0;
+    if (cluster <= 1) {
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
+        units = per_sm * dev.sm_count;
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(cluster * dev.sm_count));
+        cfg.blockDim = dim3(static_cast<unsigned>(threads));
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaOccupancyMaxActiveClusters(&units, fn, &cfg);
+    }
+    if (err != cudaSuccess) return err;
+    if (units < 1) return cudaErrorInvalidConfiguration;
+    g_ring_units[key] = units;
+    *out = units;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 // Mid rows: a block holds the row in registers (4 vectors per thread). Wider
-// rows: a cluster of up to 8 blocks holding the row in registers, or the
-// two-pass kernel. RMSNORM_FWD_WIDE (cluster | two_pass),
-// RMSNORM_FWD_ROW_THREADS and RMSNORM_FWD_CLUSTER_THREADS override the
-// choices below for sweeps.
-// Measured on GB300 over the width sweep: bf16 rows do best in one block of
-// up to 512 threads and, wider, in the two-pass kernel (fp16 rows, the same
-// bytes per element, follow bf16); fp32 rows do best in
-// blocks of at most 256 threads, split over a cluster once the row needs
-// more (up to 8 blocks of up to 512 threads), then in the two-pass kernel.
+// rows: the persistent ring kernel, a cluster of up to 8 blocks holding the
+// row in registers, or the two-pass kernel. RMSNORM_FWD_WIDE (cluster |
+// two_pass | ring), RMSNORM_FWD_ROW_THREADS and RMSNORM_FWD_CLUSTER_THREADS
+// override the choices below for sweeps.
+// Measured on GB300: bf16 rows do best in one block of up to 512 threads and,
+// wider, in the ring kernel (N = 32768: 94% against 91% two-pass; N = 65536:
+// 92% against 86%); fp16 rows, the same bytes per element, follow bf16. fp32
+// rows do best in blocks of at most 256 threads, then in clusters of 2, then
+// in the ring kernel (N = 16384: 96% against 90% for a cluster of 4; N =
+// 65536: 96% against 72% for a cluster of 8); with the residual, fp32 rows
+// stay in clusters, and every row the ring cannot hold takes the two-pass
+// kernel.
 struct FwdTuning {
-    int wide = -1;             // -1: per dtype; 0: two passes; 1: clusters
+    int wide = -1;             // -1: per dtype; 0: two passes; 1: clusters; 2: ring
     int row_threads = 0;       // largest block holding a row (0: per dtype)
     int cluster_threads = 256; // block size aimed at in a cluster
 };
@@ -481,6 +770,7 @@ const FwdTuning& fwd_tuning() {
         const char* wide = getenv("RMSNORM_FWD_WIDE");
         if (wide != nullptr && std::string(wide) == "cluster") u.wide = 1;
         if (wide != nullptr && std::string(wide) == "two_pass") u.wide = 0;
+        if (wide != nullptr && std::string(wide) == "ring") u.wide = 2;
         const char* rt = getenv("RMSNORM_FWD_ROW_THREADS");
         if (rt && *rt) u.row_threads = std::max(64, std::min(1024, atoi(rt) / 32 * 32));
         const char* ct = getenv("RMSNORM_FWD_CLUSTER_THREADS");
@@ -490,7 +780,37 @@ const FwdTuning& fwd_tuning() {
     return t;
 }
 
-void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
+// The persistent ring kernel for a row of nvec vectors: the smallest cluster
+// (1, 2, 4, then 8 blocks) whose blocks hold a slice of at most 4096 vectors
+// (512 threads x 8; 2048 for 16-bit elements) with room for at least three ring stages in about
+// 200 KB of shared memory. nt tensors ride in the ring (2 with the residual).
+bool fwd_ring_plan(int64_t nvec, int nt, int elem, rmsnorm_plan_t* p) {
+    constexpr int kRingBudget = 200 * 1024, kSmemMax = 227 * 1024;
+    // 8 vectors a thread only for 32-bit elements: with 16-bit ones the
+    // unpacked pairs of 8 vectors spill
+    const int max_slots = elem == 4 ? 4096 : 2048;
+    for (int c = 1; c <= kMaxCluster; c *= 2) {
+        const int64_t slots = cdiv(nvec, c);
+        if (slots > max_slots) continue;
+        const int v = slots <= 2048 ? 4 : 8;
+        const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
+        const int unit = v * t * 16;
+        int stages = std::min(6, kRingBudget / (nt * unit));
+        while (stages > 3 && fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
+        if (stages < 3 || fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) continue;
+        p->variant = RMSNORM_VARIANT_RING;
+        p->cluster = c;
+        p->vectors_per_thread = v;
+        p->threads = t;
+        p->threads_per_row = t * c;
+        p->stages = stages;
+        p->smem_bytes = fwd_ring_smem_bytes(stages, unit, nt);
+        return true;
+    }
+    return false;
+}
+
+void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool add) {
     *p = rmsnorm_plan_t{};
     p->stages = 0;
     p->cluster = 1;
@@ -518,10 +838,19 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
         p->threads_per_row = p->threads;
         return;
     }
+    const bool ladder = tu.wide < 0;  // no override
+    // 16-bit rows too wide for one block (and any such row under
+    // RMSNORM_FWD_WIDE=ring): the persistent ring kernel
+    if (vector_ok && (tu.wide == 2 || (ladder && half)) &&
+        fwd_ring_plan(nvec, add ? 2 : 1, dtype_size(dtype), p))
+        return;
     if (vector_ok && clusters) {
         int c = 1, v = 4;
         while (cdiv(nvec, c) > static_cast<int64_t>(tu.cluster_threads) * v && c < kMaxCluster) c *= 2;
         if (cdiv(nvec, c) <= 512 * v) {
+            // fp32 rows that need four or more blocks: the ring kernel
+            // (measured faster there, though not with the residual)
+            if (ladder && !add && c >= 4 && fwd_ring_plan(nvec, 1, dtype_size(dtype), p)) return;
             const int64_t slots = cdiv(nvec, c);
             p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
             p->cluster = c;
@@ -547,8 +876,18 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p) {
     p->vectors_per_thread = 0;
 }
 
-cudaError_t fwd_finish_plan(const DeviceInfo& dev, int, int64_t M, rmsnorm_plan_t* p) {
+cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p,
+                            bool add) {
     switch (p->variant) {
+        case RMSNORM_VARIANT_RING: {
+            const void* fn = ring_kernel_for(dtype, p->vectors_per_thread, add);
+            if (fn == nullptr) return cudaErrorInvalidValue;
+            int units = 0;
+            cudaError_t e = ring_resident_units(dev, fn, p->threads, p->smem_bytes, p->cluster, &units);
+            if (e != cudaSuccess) return e;
+            p->grid = static_cast<int>(std::min<int64_t>(M, units) * p->cluster);
+            break;
+        }
         case RMSNORM_VARIANT_ROWGROUP:
             p->grid = static_cast<int>(cdiv(M, p->rows_per_unit));
             break;

@@ -80,12 +80,14 @@ cudaError_t launch_pdl(void (*fn)(KArgs...), int grid, int threads, size_t smem,
 
 // Width-dependent choices (host only, no device queries). `vector_ok` says
 // whether the pointers and N allow 16-byte vector access.
-void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p);
+// `add`: plan the residual forward (the ring kernel then carries the residual).
+void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool add = false);
 // `res`: plan the residual backward (dres rides in the rings as well).
 void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool res = false);
 
 // Device-dependent completion of a plan (grid size, shared-memory opt-in).
-cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p);
+cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p,
+                            bool add = false);
 // `res`: the plan is for the backward with a residual gradient (its kernels
 // differ, and so may the number of resident blocks).
 cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,

@@ -154,7 +154,7 @@ def test_width_ladder(lib, N, dtype):
     vec = 4 if dtype == pkg.F32 else 8  # elements per 16-byte activation vector
     mixed = dtype in (pkg.BF16_W_F32, pkg.F16_W_F32)
     vector_ok = (N * (16 // vec)) % 16 == 0
-    for pass_ in (pkg.PASS_FWD, pkg.PASS_BWD, pkg.PASS_BWD_RES):
+    for pass_ in (pkg.PASS_FWD, pkg.PASS_FWD_ADD, pkg.PASS_BWD, pkg.PASS_BWD_RES):
         p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
         assert p.grid == 0  # no device queried
         assert p.threads % 32 == 0 and 32 <= p.threads <= 1024
@@ -178,12 +178,22 @@ def test_width_ladder(lib, N, dtype):
             if mixed and pass_ == pkg.PASS_FWD:
                 assert p.threads <= 512  # the fp32-weight row kernel's launch bound
         elif name == "two_pass":
-            assert pass_ == pkg.PASS_FWD and N > 512 * 4 * vec
+            assert pass_ in (pkg.PASS_FWD, pkg.PASS_FWD_ADD) and N > 512 * 4 * vec
+        elif name == "ring":
+            # persistent forward: a cluster of blocks whose slices cover the row,
+            # at least three stages of the ring (x, and the residual with ADD)
+            assert pass_ in (pkg.PASS_FWD, pkg.PASS_FWD_ADD)
+            assert p.vectors_per_thread in (4, 8) and p.threads <= 512
+            assert p.threads * p.vectors_per_thread * p.cluster * vec >= N
+            assert 3 <= p.stages <= 6
+            nt = 2 if pass_ == pkg.PASS_FWD_ADD else 1
+            assert p.smem_bytes >= nt * p.stages * p.vectors_per_thread * p.threads * 16
         else:
             # the backward's vector kernels cover every row up to 256 KiB;
             # wider rows outgrow shared memory
-            assert name == "scalar" and pass_ != pkg.PASS_FWD and N * (16 // vec) > 256 * 1024
-        if pass_ != pkg.PASS_FWD and name != "scalar":
+            assert name == "scalar" and pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES)
+            assert N * (16 // vec) > 256 * 1024
+        if pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES) and name != "scalar":
             # the residual backward's rings carry dres too and may be 2 deep
             res = pass_ == pkg.PASS_BWD_RES
             assert (2 if res else 3) <= p.stages <= 6
