@@ -59,8 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--shape", default=None,
-                   help="M,N,dtype (bf16|f16|f32): an ad-hoc workload drawn like the width "
-                        "sweep's, in place of --workload")
+                   help="M,N,dtype (bf16|f16|f32, or bf16_wf32|f16_wf32 for an fp32 weight): "
+                        "an ad-hoc workload drawn like the width sweep's, in place of --workload")
     p.add_argument("--op", choices=["norm", "residual", "naive"], default="norm",
                    help="norm: rmsnorm_fwd + rmsnorm_bwd; residual: rmsnorm_add_fwd + "
                         "rmsnorm_add_bwd with dres (residual and dres drawn like x and dy); "
@@ -325,9 +325,10 @@ def pick_workload(synth, args):
     import torch
 
     m, n, dt = args.shape.split(",")
-    dtype = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dt]
-    return synth.Workload(f"shape_{m}x{n}_{dt}", int(m), int(n), dtype, 1e-5, 51, 52, 53,
-                          about="ad-hoc shape")
+    act, _, wt = dt.partition("_w")  # e.g. bf16_wf32: bf16 activations, fp32 weight
+    types = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+    return synth.Workload(f"shape_{m}x{n}_{dt}", int(m), int(n), types[act], 1e-5, 51, 52, 53,
+                          about="ad-hoc shape", w_dtype=types[wt] if wt else None)
 
 
 # ------------------------------------------------------------------ our arm

@@ -750,9 +750,11 @@ cudaError_t ring_resident_units(const DeviceInfo& dev, const void* fn, int threa
 // row in registers, or the two-pass kernel. RMSNORM_FWD_WIDE (cluster |
 // two_pass | ring), RMSNORM_FWD_ROW_THREADS and RMSNORM_FWD_CLUSTER_THREADS
 // override the choices below for sweeps.
-// Measured on GB300: bf16 rows do best in one block of up to 512 threads and,
-// wider, in the ring kernel (N = 32768: 94% against 91% two-pass; N = 65536:
-// 92% against 86%); fp16 rows, the same bytes per element, follow bf16. fp32
+// Measured on GB300: bf16 rows do best in one block of up to 256 threads and,
+// wider, in the ring kernel (N = 12288: 94% against 82% for a block of 384
+// threads; N = 16384: 95% against 92%; N = 32768: 94% against 91% two-pass;
+// N = 65536: 92% against 86%); fp16 rows, the same bytes per element, follow
+// bf16. fp32
 // rows do best in blocks of at most 256 threads, then in clusters of 2, then
 // in the ring kernel (N = 16384: 96% against 90% for a cluster of 4; N =
 // 65536: 96% against 72% for a cluster of 8); with the residual, fp32 rows
@@ -762,6 +764,7 @@ struct FwdTuning {
     int wide = -1;             // -1: per dtype; 0: two passes; 1: clusters; 2: ring
     int row_threads = 0;       // largest block holding a row (0: per dtype)
     int cluster_threads = 256; // block size aimed at in a cluster
+    int ring_min_vec = 0;      // rows of at least this many vectors take the ring (0: ladder)
 };
 
 const FwdTuning& fwd_tuning() {
@@ -775,6 +778,8 @@ const FwdTuning& fwd_tuning() {
         if (rt && *rt) u.row_threads = std::max(64, std::min(1024, atoi(rt) / 32 * 32));
         const char* ct = getenv("RMSNORM_FWD_CLUSTER_THREADS");
         if (ct && *ct) u.cluster_threads = std::max(64, std::min(1024, atoi(ct) / 32 * 32));
+        const char* rm = getenv("RMSNORM_FWD_RING_MIN_VEC");
+        if (rm && *rm) u.ring_min_vec = std::max(0, atoi(rm));
         return u;
     }();
     return t;
@@ -828,6 +833,12 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
     }
     const FwdTuning& tu = fwd_tuning();
     const bool half = dtype_size(dtype) == 2;  // 16-bit activations
+    // the ring kernel from this many vectors on: 16-bit rows wider than 256
+    // threads x 4 vectors (RMSNORM_FWD_RING_MIN_VEC overrides)
+    const int64_t ring_from = tu.ring_min_vec > 0 ? tu.ring_min_vec : (half ? 1025 : INT64_MAX);
+    if (vector_ok && tu.wide < 0 && nvec >= ring_from &&
+        fwd_ring_plan(nvec, add ? 2 : 1, dtype_size(dtype), p))
+        return;
     const bool clusters = tu.wide >= 0 ? tu.wide == 1 : !half;
     const int row_cap = dtype_size(dtype) == weight_size(dtype) ? 1024 : 512;
     const int row_threads = std::min(row_cap, tu.row_threads > 0 ? tu.row_threads : (half ? 512 : 256));
