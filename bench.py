@@ -536,7 +536,8 @@ def run_ours(args):
         e2e["value"] = round(replica_throughput(world, fwd_bytes + bwd_bytes, e2e["step_ms"]), 2)
 
     small_m = None if args.no_small_m else run_small_m(pkg, torch)
-    plan_f = pkg.rmsnorm_plan(M, N, code, pkg.PASS_FWD, local).as_dict()
+    plan_f = pkg.rmsnorm_plan(M, N, code, pkg.PASS_FWD_ADD if residual else pkg.PASS_FWD,
+                              local).as_dict()
     plan_b = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD_RES if residual else pkg.PASS_BWD,
                               local).as_dict()
     value = replica_throughput(world, fwd_bytes + bwd_bytes, step_ms)

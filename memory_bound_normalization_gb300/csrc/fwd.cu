@@ -834,8 +834,14 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
     const FwdTuning& tu = fwd_tuning();
     const bool half = dtype_size(dtype) == 2;  // 16-bit activations
     // the ring kernel from this many vectors on: 16-bit rows wider than 256
-    // threads x 4 vectors (RMSNORM_FWD_RING_MIN_VEC overrides)
-    const int64_t ring_from = tu.ring_min_vec > 0 ? tu.ring_min_vec : (half ? 1025 : INT64_MAX);
+    // threads x 4 vectors, and, with an fp32 weight and no residual, every
+    // row past the short-row kernel (its block per row holds twice the weight
+    // registers: 75-92% against 88-95% in the ring; with the residual the
+    // block per row stays ahead). RMSNORM_FWD_RING_MIN_VEC overrides.
+    const bool wide_weight = weight_size(dtype) > dtype_size(dtype);
+    const int64_t ring_from = tu.ring_min_vec > 0 ? tu.ring_min_vec
+                              : (wide_weight && !add) ? 257
+                              : half ? 1025 : INT64_MAX;
     if (vector_ok && tu.wide < 0 && nvec >= ring_from &&
         fwd_ring_plan(nvec, add ? 2 : 1, dtype_size(dtype), p))
         return;
