@@ -11,8 +11,12 @@
 //     per row shape of "RMSNorm backward (almost) without the column
 //     reduction", section "The forward pass", and the block kernel of the
 //     hello-gpu chapter;
-//   * wide rows: a thread-block cluster per row, each block holding a slice
-//     of the row, the row sum exchanged through distributed shared memory.
+//   * wide rows: a persistent ring kernel (each block's slice of the coming
+//     rows arrives by bulk copies into a shared-memory ring; with a cluster
+//     the row sum is exchanged through distributed shared memory), or a
+//     thread-block cluster per row with the slices in registers, or, for rows
+//     the ring cannot hold, two passes over the row with the second served
+//     by L2.
 // Any input that is not 16-byte aligned, or whose row is not a whole number
 // of 16-byte vectors, takes the scalar kernel.
 //
