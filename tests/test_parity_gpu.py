@@ -248,3 +248,24 @@ def test_full_size_sampled(wl_name):
     rng = np.random.default_rng(12345)
     rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, size=min(M, 4096), replace=False)]))
     check_all(x, w, dy, wl.eps, *out, rows=rows)
+
+
+RING = [(16384, torch.bfloat16, None), (65536, torch.bfloat16, None), (65536, torch.float32, None),
+        (8192, torch.bfloat16, torch.float32), (32768, torch.float16, None)]
+
+
+@pytest.mark.parametrize("N,dtype,w_dtype", RING,
+                         ids=[f"{n}-{str(d)[6:]}" + ("-wf32" if wd else "") for n, d, wd in RING])
+def test_ring_forward_around_its_grid(N, dtype, w_dtype):
+    """The persistent ring forward with M just below, at and above the number
+    of co-resident clusters, and a few rows per cluster: some clusters walk
+    one row more than others. Sampled rows plus the first and last."""
+    code = pkg.dtype_code(dtype, w_dtype)
+    plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_FWD, 0)
+    assert pkg.VARIANTS[plan.variant] == "ring", pkg.VARIANTS[plan.variant]
+    P = plan.grid // plan.cluster
+    for M in sorted({max(1, P - 1), P, P + 1, 3 * P + 2}):
+        inp, eps = inputs(M, N, dtype, seed=M % 3, w_dtype=w_dtype)
+        out = run(inp["x"], inp["w"], inp["dy"], eps)
+        rows = np.unique(np.concatenate([[0, M - 1], np.arange(0, M, max(1, M // 40))]))
+        check_all(inp["x"], inp["w"], inp["dy"], eps, *out, rows=rows)
