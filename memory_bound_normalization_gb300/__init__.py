@@ -4,7 +4,9 @@ The computation lives in the CUDA library ``librmsnorm.so`` (C ABI in
 ``include/rmsnorm.h``); this package is its Python binding. The ``rmsnorm_*``
 functions mirror the C entry points one for one. ``forward`` and ``backward``
 are conveniences that allocate outputs with PyTorch (device memory only) and
-raise ``RMSNormError`` on a non-OK status.
+raise ``RMSNormError`` on a non-OK status; ``add_forward`` and
+``add_backward`` do the same for the residual add. ``autograd`` holds
+differentiable wrappers (``rms_norm``, ``fused_add_rms_norm``, ``RMSNorm``).
 """
 from __future__ import annotations
 
