@@ -311,10 +311,55 @@ def cpu_baseline(wl, budget_s: float):
             break
     fb, bb = synth.logical_bytes(rows, wl.N, elem, w_elem)
     what = "all" if rows == wl.M else f"the first {rows} of"
-    return {"value": round(passes * (fb + bb) / total / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"{what} {wl.M} rows x {wl.N} ({wl.dtype_name}), fwd + dx + dw in fp64 on "
-                      f"one host thread, {passes} pass(es), {total:.1f} s"}
+    out = {"value": round(passes * (fb + bb) / total / 1e9, 4), "unit": "GB/s", "cores": 1,
+           "kind": "oracle",
+           "sample": f"{what} {wl.M} rows x {wl.N} ({wl.dtype_name}), fwd + dx + dw in fp64 on "
+                     f"one host thread, {passes} pass(es), {total:.1f} s"}
+    cores = os.cpu_count() or 1
+    if cores > 1:
+        out["all_cores"] = cpu_baseline_all_cores(oracle, synth, wl, rows, cores, budget_s,
+                                                  elem, w_elem)
+    return out
+
+
+def cpu_baseline_all_cores(oracle, synth, wl, rows_one, cores, budget_s, elem, w_elem):
+    """The same oracle calls on every host core: the rows are cut into one
+    contiguous shard per thread (the oracle's C entry points run without the
+    interpreter lock), each thread computes its shard's y, dx and partial dw,
+    and the partial dw are added in shard order. The sample is about what one
+    thread did alone, times the number of threads, up to all rows."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    rows = int(min(wl.M, max(cores, rows_one * cores)))
+    inp = synth.make_inputs(wl, device="cpu", M=rows)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    cuts = [rows * k // cores for k in range(cores + 1)]
+
+    def shard(k):
+        a, b = cuts[k], cuts[k + 1]
+        if a == b:
+            return None
+        oracle.fwd(x[a:b], w, wl.eps)
+        oracle.bwd_dx(x[a:b], w, dy[a:b], wl.eps)
+        return oracle.bwd_dw(x[a:b], dy[a:b], wl.eps)
+
+    passes, total = 0, 0.0
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        while True:
+            t0 = time.perf_counter()
+            dw = None
+            for part in pool.map(shard, range(cores)):
+                if part is not None:
+                    dw = part if dw is None else dw + part
+            total += time.perf_counter() - t0
+            passes += 1
+            if total >= budget_s or passes >= 64:
+                break
+    fb, bb = synth.logical_bytes(rows, wl.N, elem, w_elem)
+    what = "all" if rows == wl.M else f"the first {rows} of"
+    return {"value": round(passes * (fb + bb) / total / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "sample": f"{what} {wl.M} rows in {cores} row shards, one thread each; "
+                      f"{passes} pass(es), {total:.1f} s"}
 
 
 def pick_workload(synth, args):

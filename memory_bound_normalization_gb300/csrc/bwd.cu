@@ -31,7 +31,9 @@ struct BwdTuning {
     int smem_single = 100 * 1024;  // shared memory aimed at, one group
     int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
     bool pipelined = false;        // cluster rows: pass 1 of the next row first
-    int rowgroup_max_vec = 256;    // widest row (16-byte vectors) for the short-row kernel
+    int cluster = 0;               // blocks a wide row is split over (0 = from the ladder)
+    int rowgroup_max_vec = -1;     // widest row (16-byte vectors) for the short-row kernel
+                                   // (-1 = by type: 256 for fp32 rows, 128 for 16-bit rows)
 };
 
 int env_int(const char* name, int dflt) {
@@ -50,7 +52,8 @@ const BwdTuning& tuning() {
         u.smem_multi = std::max(32 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SMEM", u.smem_multi)));
         u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
         u.pipelined = env_int("RMSNORM_BWD_PIPE", 0) != 0;
-        u.rowgroup_max_vec = std::max(0, std::min(256, env_int("RMSNORM_BWD_ROWGROUP_MAX_VEC", 256)));
+        u.cluster = std::max(0, std::min(kMaxCluster, env_int("RMSNORM_BWD_CLUSTER", 0)));
+        u.rowgroup_max_vec = std::max(-1, std::min(256, env_int("RMSNORM_BWD_ROWGROUP_MAX_VEC", -1)));
         return u;
     }();
     return t;
@@ -193,8 +196,13 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
     const BwdTuning& tu = tuning();
     const int nt = res ? 3 : 2;          // tensors in a ring stage
     const int min_stages = res ? 2 : 3;
+    // 16-bit rows of 129..256 vectors ran 7..15 points of the copy roofline
+    // faster as one row per 64-thread group (8 groups a block) than as one
+    // row per 32-thread group; fp32 rows of 256 vectors ran 1 point slower
+    const int rowgroup_max_vec = tu.rowgroup_max_vec >= 0 ? tu.rowgroup_max_vec
+                                                          : (sz == 4 ? 256 : 128);
     GroupShape g;
-    if (vector_ok && nvec <= tu.rowgroup_max_vec && bwd_group_shape(nvec, &g)) {
+    if (vector_ok && nvec <= rowgroup_max_vec && bwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
         p->threads = g.threads;
         p->threads_per_row = g.G;
@@ -238,29 +246,34 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
             }
         }
         // wider rows: split over a cluster, one row at a time per block
-        int c = 1;
-        while (2 * cdiv(nvec, c) * 16 > tu.slice && c < kMaxCluster) c *= 2;
-        for (;; c *= 2) {
+        auto try_wide = [&](int c, int st_min) {
             const int64_t slots = cdiv(nvec, c);
             int v = 4;
             while (cdiv(slots, v) > 512 && v < 8) v *= 2;
             const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
             const int unit = v * t * 16;
             int stages = tu.stages > 0 ? tu.stages
-                                       : std::max(min_stages, std::min(6, tu.smem_multi / (nt * unit)));
-            while (stages > min_stages && bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
-            if (t <= 512 && bwd_wide_smem_bytes(stages, unit, nt) <= kSmemMax) {
-                p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
-                p->cluster = c;
-                p->row_groups = 1;
-                p->vectors_per_thread = v;
-                p->threads = t;
-                p->threads_per_row = t * c;
-                p->rows_per_unit = 1;
-                p->stages = stages;
-                p->smem_bytes = bwd_wide_smem_bytes(stages, unit, nt);
-                return;
-            }
+                                       : std::max(st_min, std::min(6, tu.smem_multi / (nt * unit)));
+            while (stages > st_min && bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
+            if (t > 512 || bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) return false;
+            p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
+            p->cluster = c;
+            p->row_groups = 1;
+            p->vectors_per_thread = v;
+            p->threads = t;
+            p->threads_per_row = t * c;
+            p->rows_per_unit = 1;
+            p->stages = stages;
+            p->smem_bytes = bwd_wide_smem_bytes(stages, unit, nt);
+            return true;
+        };
+        // a forced cluster size may run a two-deep ring; the ladder's own
+        // sizes keep three stages (two with dres in the ring)
+        if (tu.cluster > 0 && try_wide(tu.cluster, 2)) return;
+        int c = 1;
+        while (2 * cdiv(nvec, c) * 16 > tu.slice && c < kMaxCluster) c *= 2;
+        for (;; c *= 2) {
+            if (try_wide(c, min_stages)) return;
             if (!res || c >= kMaxCluster) break;
         }
     }

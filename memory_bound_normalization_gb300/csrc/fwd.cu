@@ -769,6 +769,7 @@ struct FwdTuning {
     int row_threads = 0;       // largest block holding a row (0: per dtype)
     int cluster_threads = 256; // block size aimed at in a cluster
     int ring_min_vec = 0;      // rows of at least this many vectors take the ring (0: ladder)
+    int rowgroup_max_vec = -1; // widest row (16-byte vectors) for the short-row kernel (-1: 256)
 };
 
 const FwdTuning& fwd_tuning() {
@@ -784,6 +785,8 @@ const FwdTuning& fwd_tuning() {
         if (ct && *ct) u.cluster_threads = std::max(64, std::min(1024, atoi(ct) / 32 * 32));
         const char* rm = getenv("RMSNORM_FWD_RING_MIN_VEC");
         if (rm && *rm) u.ring_min_vec = std::max(0, atoi(rm));
+        const char* gm = getenv("RMSNORM_FWD_ROWGROUP_MAX_VEC");
+        if (gm && *gm) u.rowgroup_max_vec = std::max(0, std::min(256, atoi(gm)));
         return u;
     }();
     return t;
@@ -826,8 +829,10 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
     p->row_groups = 1;
     p->rows_per_unit = 1;
     const int64_t nvec = N / dtype_vec(dtype);
+    const FwdTuning& tu = fwd_tuning();
+    const int64_t rowgroup_max_vec = tu.rowgroup_max_vec >= 0 ? tu.rowgroup_max_vec : 256;
     GroupShape g;
-    if (vector_ok && fwd_group_shape(nvec, &g)) {
+    if (vector_ok && nvec <= rowgroup_max_vec && fwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;
         p->threads = g.threads;
         p->threads_per_row = g.G;
@@ -835,7 +840,6 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
         p->rows_per_unit = (g.threads / g.G) * g.R;
         return;
     }
-    const FwdTuning& tu = fwd_tuning();
     const bool half = dtype_size(dtype) == 2;  // 16-bit activations
     // the ring kernel from this many vectors on: 16-bit rows wider than 256
     // threads x 4 vectors, and, with an fp32 weight and no residual, every

@@ -58,3 +58,15 @@ def test_dist_env_defaults(monkeypatch):
     monkeypatch.setenv("RANK", "3")
     monkeypatch.setenv("LOCAL_RANK", "3")
     assert bench.dist_env() == (3, 8, 3)
+
+
+def test_cpu_baseline_reports_one_thread_and_all_cores():
+    from memory_bound_normalization_gb300 import synth
+
+    wl = synth.WORKLOADS["small_256x1024"]
+    got = bench.cpu_baseline(wl, 0.2)
+    assert got["kind"] == "oracle" and got["cores"] == 1 and got["value"] > 0
+    cores = os.cpu_count() or 1
+    if cores > 1:
+        allc = got["all_cores"]
+        assert allc["cores"] == cores and allc["value"] > 0 and allc["unit"] == got["unit"]

@@ -211,3 +211,16 @@ def test_plan_rejects_bad_arguments(lib):
         pkg.rmsnorm_plan(10, 64, pkg.BF16, 7)
     p = pkg.rmsnorm_plan(0, 64, pkg.BF16, pkg.PASS_BWD)
     assert pkg.VARIANTS[p.variant] == "none"
+
+
+@pytest.mark.parametrize("dtype,N,want", [(pkg.BF16, 1024, "rowgroup"), (pkg.BF16, 1032, "cta_row"),
+                                          (pkg.BF16, 2048, "cta_row"), (pkg.F16, 2048, "cta_row"),
+                                          (pkg.BF16_W_F32, 1536, "cta_row"),
+                                          (pkg.F32, 1024, "rowgroup"), (pkg.F32, 1028, "cta_row")])
+def test_short_row_backward_cutoff(lib, dtype, N, want):
+    """The backward keeps the row-group kernel up to 128 vectors a row for
+    16-bit activations and up to 256 for fp32 (the faster side of each
+    measured pair); both passes of the backward follow the same cutoff."""
+    for pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES):
+        p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
+        assert pkg.VARIANTS[p.variant] == want
