@@ -246,10 +246,10 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
             }
         }
         // wider rows: split over a cluster, one row at a time per block
-        auto try_wide = [&](int c, int st_min) {
+        auto try_wide = [&](int c, int st_min, int max_v = 8) {
             const int64_t slots = cdiv(nvec, c);
             int v = 4;
-            while (cdiv(slots, v) > 512 && v < 8) v *= 2;
+            while (cdiv(slots, v) > 512 && v < max_v) v *= 2;
             const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
             const int unit = v * t * 16;
             int stages = tu.stages > 0 ? tu.stages
@@ -272,6 +272,17 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
         if (tu.cluster > 0 && try_wide(tu.cluster, 2)) return;
         int c = 1;
         while (2 * cdiv(nvec, c) * 16 > tu.slice && c < kMaxCluster) c *= 2;
+        // Clusters of 8 leave SMs idle: 15 fit at once on a 152-SM GB300 (120
+        // SMs), against 28 of 5 (140) and 23 of 6 (138). A row that would take
+        // 8 blocks takes 5 or 6 where 4 vectors a thread and a three-deep ring
+        // fit (fp32 N = 40960: 89% against 63%; N = 49152: 87% against 69%;
+        // bf16 N = 98304: 86% against 70%); an fp32 row also takes 5 blocks of
+        // 8 vectors a thread with a two-deep ring (N = 65536: 89% against 79%),
+        // which 16-bit rows do not (their 8-vector threads ran at 35-50%).
+        if (c == kMaxCluster && !res) {
+            if (try_wide(5, 3, 4) || try_wide(6, 3, 4)) return;
+            if (sz == 4 && try_wide(5, 2)) return;
+        }
         for (;; c *= 2) {
             if (try_wide(c, min_stages)) return;
             if (!res || c >= kMaxCluster) break;

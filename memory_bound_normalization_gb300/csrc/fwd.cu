@@ -769,7 +769,8 @@ struct FwdTuning {
     int row_threads = 0;       // largest block holding a row (0: per dtype)
     int cluster_threads = 256; // block size aimed at in a cluster
     int ring_min_vec = 0;      // rows of at least this many vectors take the ring (0: ladder)
-    int rowgroup_max_vec = -1; // widest row (16-byte vectors) for the short-row kernel (-1: 256)
+    int rowgroup_max_vec = -1; // widest row (16-byte vectors) for the short-row kernel
+                               // (-1: 256, or 128 with the residual)
 };
 
 const FwdTuning& fwd_tuning() {
@@ -830,7 +831,12 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
     p->rows_per_unit = 1;
     const int64_t nvec = N / dtype_vec(dtype);
     const FwdTuning& tu = fwd_tuning();
-    const int64_t rowgroup_max_vec = tu.rowgroup_max_vec >= 0 ? tu.rowgroup_max_vec : 256;
+    // With the residual, a lane of the short-row kernel holds 8 vectors of x
+    // and 8 of the residual at 129..256 vectors a row; a block per row (4
+    // vectors of each a thread) ran 8..20 points of the copy roofline faster
+    // there. Without it the short-row kernel stays ahead.
+    const int64_t rowgroup_max_vec = tu.rowgroup_max_vec >= 0 ? tu.rowgroup_max_vec
+                                     : add ? 128 : 256;
     GroupShape g;
     if (vector_ok && nvec <= rowgroup_max_vec && fwd_group_shape(nvec, &g)) {
         p->variant = RMSNORM_VARIANT_ROWGROUP;

@@ -194,9 +194,11 @@ def test_width_ladder(lib, N, dtype):
             assert name == "scalar" and pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES)
             assert N * (16 // vec) > 256 * 1024
         if pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES) and name != "scalar":
-            # the residual backward's rings carry dres too and may be 2 deep
+            # the residual backward's rings carry dres too and may be 2 deep, as
+            # may an fp32 row over a cluster of 5 blocks of 8 vectors a thread
             res = pass_ == pkg.PASS_BWD_RES
-            assert (2 if res else 3) <= p.stages <= 6
+            two_deep = res or (dtype == pkg.F32 and p.cluster == 5 and p.vectors_per_thread == 8)
+            assert (2 if two_deep else 3) <= p.stages <= 6
             if name == "rowgroup":
                 unit = p.rows_per_unit * N * (16 // vec)
             else:
@@ -224,3 +226,34 @@ def test_short_row_backward_cutoff(lib, dtype, N, want):
     for pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES):
         p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
         assert pkg.VARIANTS[p.variant] == want
+
+
+@pytest.mark.parametrize("dtype,N", [(pkg.BF16, 1032), (pkg.BF16, 2048), (pkg.F16, 1536),
+                                     (pkg.BF16_W_F32, 2048), (pkg.F32, 1024)])
+def test_residual_forward_short_row_cutoff(lib, dtype, N):
+    """Rows of 129..256 vectors: the plain forward keeps the short-row kernel,
+    the residual forward takes a block per row."""
+    plain = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD, -1)
+    add = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD_ADD, -1)
+    assert pkg.VARIANTS[plain.variant] == "rowgroup"
+    assert pkg.VARIANTS[add.variant] == "cta_row" and add.vectors_per_thread == 4
+    vec = 4 if dtype == pkg.F32 else 8
+    assert add.threads * 4 * vec >= N
+
+
+@pytest.mark.parametrize("dtype,N,cluster,vectors,stages", [
+    (pkg.F32, 32768, 4, 4, 3), (pkg.F32, 40960, 5, 4, 3), (pkg.F32, 49152, 6, 4, 3),
+    (pkg.F32, 65536, 5, 8, 2), (pkg.BF16, 65536, 4, 4, 3), (pkg.BF16, 98304, 6, 4, 3),
+    (pkg.BF16, 131072, 8, 4, 3), (pkg.F16, 131072, 8, 4, 3)])
+def test_wide_backward_cluster_sizes(lib, dtype, N, cluster, vectors, stages):
+    """Rows the power-of-two ladder would split over 8 blocks take 5 or 6
+    where 4 vectors a thread and a three-deep ring fit (fp32 also 5 blocks of
+    8 vectors with a two-deep ring); 16-bit rows otherwise keep 8."""
+    p = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_BWD, -1)
+    assert pkg.VARIANTS[p.variant] == "cluster_row"
+    assert (p.cluster, p.vectors_per_thread, p.stages) == (cluster, vectors, stages)
+    vec = 4 if dtype == pkg.F32 else 8
+    assert p.threads * vectors * cluster * vec >= N and p.threads <= 512
+    # the residual backward keeps the power-of-two ladder
+    r = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_BWD_RES, -1)
+    assert r.cluster in (1, 2, 4, 8)

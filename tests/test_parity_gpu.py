@@ -75,7 +75,8 @@ TYPE_IDS = ["bf16", "f32", "f16", "bf16_wf32", "f16_wf32"]
 
 SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (37, 256),
           (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (5, 6144), (4, 8192),
-          (3, 16384), (2, 32768), (2, 65536), (1, 65536), (1000, 40), (777, 96)]
+          (3, 16384), (2, 32768), (3, 40960), (4, 49152), (2, 65536), (1, 65536), (2, 98304),
+          (1000, 40), (777, 96)]
 
 
 @pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
@@ -98,6 +99,23 @@ def test_rows_around_persistent_grid(N, dtype, w_dtype):
     for M in sorted({max(1, (P - 1) * per_unit), P * per_unit, P * per_unit + 1,
                      3 * P * per_unit + per_unit // 2 + 1}):
         inp, eps = inputs(M, N, dtype, seed=M % 7, w_dtype=w_dtype)
+        out = run(inp["x"], inp["w"], inp["dy"], eps)
+        check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
+
+
+@pytest.mark.parametrize("dtype,w_dtype", [(torch.bfloat16, None), (torch.float32, None)],
+                         ids=["bf16", "f32"])
+@pytest.mark.parametrize("N", [40960, 49152, 65536, 98304])
+def test_wide_rows_around_cluster_grid(N, dtype, w_dtype):
+    """Rows split over clusters of 5, 6 or 8 blocks (4 for bf16 at 65536):
+    M just below, at and above the number of co-resident clusters, and a
+    ragged multiple of it."""
+    code = pkg.dtype_code(dtype, w_dtype)
+    plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_BWD, 0)
+    P = plan.partial_rows
+    assert plan.grid == P * plan.cluster
+    for M in sorted({max(1, P - 1), P, P + 1, 2 * P + 3}):
+        inp, eps = inputs(M, N, dtype, seed=M % 5, w_dtype=w_dtype)
         out = run(inp["x"], inp["w"], inp["dy"], eps)
         check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
 

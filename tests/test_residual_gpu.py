@@ -92,7 +92,8 @@ def check_bwd(h, w, dy, dres, eps, dx, dw, rows=None):
 
 
 SHAPES = [(1, 8), (3, 13), (33, 257), (7, 32), (100, 64), (130, 128), (19, 512), (256, 1024),
-          (9, 2880), (6, 4096), (4, 8192), (3, 16384), (2, 65536), (1000, 40)]
+          (40, 1032), (21, 1536), (5, 2048), (9, 2880), (6, 4096), (4, 8192), (3, 16384),
+          (2, 65536), (1000, 40)]
 
 
 @pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
