@@ -442,10 +442,13 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         for (int64_t t = 0; t < S && t < nrows; ++t) issue(t);
 
     // The weights of the thread's slots stay in registers across rows when
-    // they take at most 8 16-byte words; more (an fp32 weight with 8 vectors
-    // a thread) would spill, so those are re-read from cache at each use.
+    // they take at most 8 16-byte words and the thread holds at most 4
+    // vectors of 16-bit elements; otherwise (an fp32 weight with 8 vectors a
+    // thread, or 8 vectors of 16-bit elements, whose 64 dw accumulators
+    // leave no room) they would spill, so they are re-read from cache at
+    // each use.
     using WP = WPack<T, TW>;
-    constexpr bool kWReg = WP::WORDS * V <= 8;
+    constexpr bool kWReg = WP::WORDS * V <= 8 && !(sizeof(T) == 2 && V > 4);
     uint4 wv[kWReg ? V : 1][WP::WORDS];
     if constexpr (kWReg) {
 #pragma unroll

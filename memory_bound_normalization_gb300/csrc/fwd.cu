@@ -769,6 +769,8 @@ struct FwdTuning {
     int row_threads = 0;       // largest block holding a row (0: per dtype)
     int cluster_threads = 256; // block size aimed at in a cluster
     int ring_min_vec = 0;      // rows of at least this many vectors take the ring (0: ladder)
+    int ring_cluster = 0;      // blocks of the ring kernel's cluster (0: ladder)
+    int ring_smem = 200 * 1024;  // shared memory the ring's stages aim at per block
     int rowgroup_max_vec = -1; // widest row (16-byte vectors) for the short-row kernel
                                // (-1: 256, or 128 with the residual)
 };
@@ -786,6 +788,10 @@ const FwdTuning& fwd_tuning() {
         if (ct && *ct) u.cluster_threads = std::max(64, std::min(1024, atoi(ct) / 32 * 32));
         const char* rm = getenv("RMSNORM_FWD_RING_MIN_VEC");
         if (rm && *rm) u.ring_min_vec = std::max(0, atoi(rm));
+        const char* rc = getenv("RMSNORM_FWD_RING_CLUSTER");
+        if (rc && *rc) u.ring_cluster = std::max(0, std::min(kMaxCluster, atoi(rc)));
+        const char* rs = getenv("RMSNORM_FWD_RING_SMEM");
+        if (rs && *rs) u.ring_smem = std::max(16 * 1024, std::min(227 * 1024, atoi(rs)));
         const char* gm = getenv("RMSNORM_FWD_ROWGROUP_MAX_VEC");
         if (gm && *gm) u.rowgroup_max_vec = std::max(0, std::min(256, atoi(gm)));
         return u;
@@ -798,17 +804,18 @@ const FwdTuning& fwd_tuning() {
 // (512 threads x 8; 2048 for 16-bit elements) with room for at least three ring stages in about
 // 200 KB of shared memory. nt tensors ride in the ring (2 with the residual).
 bool fwd_ring_plan(int64_t nvec, int nt, int elem, rmsnorm_plan_t* p) {
-    constexpr int kRingBudget = 200 * 1024, kSmemMax = 227 * 1024;
+    constexpr int kSmemMax = 227 * 1024;
     // 8 vectors a thread only for 32-bit elements: with 16-bit ones the
     // unpacked pairs of 8 vectors spill
     const int max_slots = elem == 4 ? 4096 : 2048;
-    for (int c = 1; c <= kMaxCluster; c *= 2) {
+    const int forced = fwd_tuning().ring_cluster;
+    for (int c = forced > 0 ? forced : 1; c <= kMaxCluster; c = forced > 0 ? kMaxCluster + 1 : c * 2) {
         const int64_t slots = cdiv(nvec, c);
         if (slots > max_slots) continue;
         const int v = slots <= 2048 ? 4 : 8;
         const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
         const int unit = v * t * 16;
-        int stages = std::min(6, kRingBudget / (nt * unit));
+        int stages = std::min(6, fwd_tuning().ring_smem / (nt * unit));
         while (stages > 3 && fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
         if (stages < 3 || fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) continue;
         p->variant = RMSNORM_VARIANT_RING;
