@@ -117,7 +117,7 @@ int fwd_run(const void* x, const void* res, const void* w, void* h, void* y, flo
     const DeviceInfo* dev = nullptr;
     st = current_device(&dev);
     if (st != RMSNORM_OK) return st;
-    st = cuda_status(fwd_finish_plan(*dev, dtype, M, &plan, add));
+    st = cuda_status(fwd_finish_plan(*dev, dtype, M, N, &plan, add));
     if (st != RMSNORM_OK) return st;
     if (static_cast<int64_t>(plan.grid) <= 0 ||
         ((plan.variant == RMSNORM_VARIANT_ROWGROUP || plan.variant == RMSNORM_VARIANT_CTA_ROW ||
@@ -338,7 +338,7 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     if (device < 0) return RMSNORM_OK;
     const DeviceInfo* dev = device_info(device);
     if (!dev) return RMSNORM_ERR_CUDA;
-    cudaError_t e = fwd ? fwd_finish_plan(*dev, dtype, M, out, pass == RMSNORM_PASS_FWD_ADD)
+    cudaError_t e = fwd ? fwd_finish_plan(*dev, dtype, M, N, out, pass == RMSNORM_PASS_FWD_ADD)
                                              : bwd_finish_plan(*dev, dtype, M, N, out,
                                                                pass == RMSNORM_PASS_BWD_RES);
     return cuda_status(e);

@@ -32,6 +32,8 @@ struct BwdTuning {
     int slice = kSliceBudget;      // x+dy bytes of a block's row slice per stage
     bool pipelined = false;        // cluster rows: pass 1 of the next row first
     int cluster = 0;               // blocks a wide row is split over (0 = from the ladder)
+    int wide_select = 2;           // cluster rows shaped on the device: 0 never, 1 without
+                                   // dres, 2 always
     int rowgroup_max_vec = -1;     // widest row (16-byte vectors) for the short-row kernel
                                    // (-1 = by type: 256 for fp32 rows, 128 for 16-bit rows)
 };
@@ -53,6 +55,7 @@ const BwdTuning& tuning() {
         u.slice = std::max(8 * 1024, std::min(kSmemMax, env_int("RMSNORM_BWD_SLICE", u.slice)));
         u.pipelined = env_int("RMSNORM_BWD_PIPE", 0) != 0;
         u.cluster = std::max(0, std::min(kMaxCluster, env_int("RMSNORM_BWD_CLUSTER", 0)));
+        u.wide_select = std::max(0, std::min(2, env_int("RMSNORM_WIDE_SELECT", 2)));
         u.rowgroup_max_vec = std::max(-1, std::min(256, env_int("RMSNORM_BWD_ROWGROUP_MAX_VEC", -1)));
         return u;
     }();
@@ -181,6 +184,33 @@ cudaError_t resident_units(const DeviceInfo& dev, const void* fn, int threads, i
 
 
 
+// A cluster-row plan for rows of nvec 16-byte vectors split over c blocks:
+// 4 vectors a thread, else up to max_v, so that a block has at most 512
+// threads; a ring of `stages` stages (0: as many as `budget` bytes of shared
+// memory hold, at most 6), lowered to st_min while it does not fit. False
+// when the block or its ring cannot fit.
+bool wide_plan(int64_t nvec, int nt, int c, int max_v, int st_min, int stages, int budget,
+               rmsnorm_plan_t* p) {
+    const int64_t slots = cdiv(nvec, c);
+    int v = 4;
+    while (cdiv(slots, v) > 512 && v < max_v) v *= 2;
+    const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
+    const int unit = v * t * 16;
+    if (stages <= 0) stages = std::max(st_min, std::min(6, budget / (nt * unit)));
+    while (stages > st_min && bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
+    if (t > 512 || bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) return false;
+    p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
+    p->cluster = c;
+    p->row_groups = 1;
+    p->vectors_per_thread = v;
+    p->threads = t;
+    p->threads_per_row = t * c;
+    p->rows_per_unit = 1;
+    p->stages = stages;
+    p->smem_bytes = bwd_wide_smem_bytes(stages, unit, nt);
+    return true;
+}
+
 }  // namespace
 
 // With res (the residual backward) the rings carry dres as a third tensor:
@@ -247,25 +277,7 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
         }
         // wider rows: split over a cluster, one row at a time per block
         auto try_wide = [&](int c, int st_min, int max_v = 8) {
-            const int64_t slots = cdiv(nvec, c);
-            int v = 4;
-            while (cdiv(slots, v) > 512 && v < max_v) v *= 2;
-            const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
-            const int unit = v * t * 16;
-            int stages = tu.stages > 0 ? tu.stages
-                                       : std::max(st_min, std::min(6, tu.smem_multi / (nt * unit)));
-            while (stages > st_min && bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
-            if (t > 512 || bwd_wide_smem_bytes(stages, unit, nt) > kSmemMax) return false;
-            p->variant = c > 1 ? RMSNORM_VARIANT_CLUSTER_ROW : RMSNORM_VARIANT_CTA_ROW;
-            p->cluster = c;
-            p->row_groups = 1;
-            p->vectors_per_thread = v;
-            p->threads = t;
-            p->threads_per_row = t * c;
-            p->rows_per_unit = 1;
-            p->stages = stages;
-            p->smem_bytes = bwd_wide_smem_bytes(stages, unit, nt);
-            return true;
+            return wide_plan(nvec, nt, c, max_v, st_min, tu.stages, tu.smem_multi, p);
         };
         // a forced cluster size may run a two-deep ring; the ladder's own
         // sizes keep three stages (two with dres in the ring)
@@ -296,8 +308,82 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
     p->smem_bytes = 0;
 }
 
+namespace {
+
+// Cluster-row plans chosen on a device, per (device, dtype, N).
+std::mutex g_wide_mu;
+std::map<std::tuple<int, int, int64_t, bool>, rmsnorm_plan_t> g_wide;
+
+// A row split over a cluster runs best where the clusters resident at once
+// (rows in flight) times the threads resident with them is largest; ties go
+// to fewer, larger blocks (at N = 65536, 4 blocks of 512 threads against 8 of
+// 256: fp16 81% against 77%, bf16 90% against 89%), then to the deeper ring. How
+// many fit depends on registers, shared memory and the device's GPC layout,
+// so the occupancy API counts them for cluster sizes 2, 4, 5, 6 and 8, four
+// vectors a thread (also eight for fp32 rows) and rings two to six deep
+// (three to six for 16-bit rows without dres, whose two-deep rings never
+// gained there; with dres, a third tensor in the ring, two to six). On
+// GB300 this took fp32 rows of N = 16384..49152 from 83..97% of the copy
+// roofline to 93..101% (blocks of 128..448 threads, two-deep rings, two or
+// more blocks to an SM) and bf16 N = 40960 from 72% to 91%.
+cudaError_t wide_select(const DeviceInfo& dev, int dtype, int64_t N, bool res, rmsnorm_plan_t* p) {
+    const auto key = std::make_tuple(dev.device, dtype, N, res);
+    {
+        std::lock_guard<std::mutex> lk(g_wide_mu);
+        auto it = g_wide.find(key);
+        if (it != g_wide.end()) {
+            *p = it->second;
+            return cudaSuccess;
+        }
+    }
+    const int sz = dtype_size(dtype);
+    const int64_t nvec = N / dtype_vec(dtype);
+    const BwdTuning& tu = tuning();
+    rmsnorm_plan_t best = *p;
+    int64_t best_score[3] = {-1, -1, -1};
+    for (int c : {2, 4, 5, 6, 8}) {
+        for (int max_v : {4, 8}) {
+            if (max_v == 8 && sz != 4) continue;
+            for (int st = (sz == 4 || res) ? 2 : 3; st <= 6; ++st) {
+                rmsnorm_plan_t q = *p;
+                if (!wide_plan(nvec, res ? 3 : 2, c, max_v, st, st, tu.smem_multi, &q)) continue;
+                if (q.cluster != c || q.stages != st || q.smem_bytes > dev.max_smem_optin) continue;
+                const void* fn = main_kernel_for(dtype, q, res);
+                if (fn == nullptr) continue;
+                int units = 0;
+                if (resident_units(dev, fn, q.threads, q.smem_bytes, c, &units) != cudaSuccess) {
+                    cudaGetLastError();  // an occupancy query that fails rules the shape out
+                    continue;
+                }
+                // rows in flight times resident threads, then fewer (larger)
+                // blocks, then the deeper ring
+                const int64_t blocks = static_cast<int64_t>(units) * c;
+                const int64_t score[3] = {units * blocks * q.threads, -blocks, st};
+                if (std::lexicographical_compare(best_score, best_score + 3, score, score + 3)) {
+                    best = q;
+                    std::copy(score, score + 3, best_score);
+                }
+            }
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_wide_mu);
+    g_wide[key] = best;
+    *p = best;
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
                             rmsnorm_plan_t* p, bool res) {
+    const BwdTuning& tu = tuning();
+    const bool wide_overridden = tu.cluster > 0 || tu.stages > 0 || tu.pipelined ||
+                                 tu.smem_multi != 200 * 1024 || tu.slice != kSliceBudget;
+    if (p->variant == RMSNORM_VARIANT_CLUSTER_ROW && !wide_overridden &&
+        tu.wide_select >= (res ? 2 : 1)) {
+        cudaError_t e = wide_select(dev, dtype, N, res, p);
+        if (e != cudaSuccess) return e;
+    }
     if (p->smem_bytes > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     const void* fn = main_kernel_for(dtype, *p, res);
     if (fn == nullptr) return cudaErrorInvalidValue;

@@ -771,6 +771,8 @@ struct FwdTuning {
     int ring_min_vec = 0;      // rows of at least this many vectors take the ring (0: ladder)
     int ring_cluster = 0;      // blocks of the ring kernel's cluster (0: ladder)
     int ring_smem = 200 * 1024;  // shared memory the ring's stages aim at per block
+    int wide_select = 2;       // ring clusters shaped on the device: 0 never, 1 without the
+                               // residual, 2 always
     int rowgroup_max_vec = -1; // widest row (16-byte vectors) for the short-row kernel
                                // (-1: 256, or 128 with the residual)
 };
@@ -792,6 +794,8 @@ const FwdTuning& fwd_tuning() {
         if (rc && *rc) u.ring_cluster = std::max(0, std::min(kMaxCluster, atoi(rc)));
         const char* rs = getenv("RMSNORM_FWD_RING_SMEM");
         if (rs && *rs) u.ring_smem = std::max(16 * 1024, std::min(227 * 1024, atoi(rs)));
+        const char* ws = getenv("RMSNORM_WIDE_SELECT");
+        if (ws && *ws) u.wide_select = std::max(0, std::min(2, atoi(ws)));
         const char* gm = getenv("RMSNORM_FWD_ROWGROUP_MAX_VEC");
         if (gm && *gm) u.rowgroup_max_vec = std::max(0, std::min(256, atoi(gm)));
         return u;
@@ -799,34 +803,41 @@ const FwdTuning& fwd_tuning() {
     return t;
 }
 
+// The ring plan for rows of nvec vectors over c blocks: 4 vectors a thread,
+// or 8 for 32-bit elements where max_v allows it and 4 would need more than
+// 512 threads (with 16-bit elements the unpacked pairs of 8 vectors spill),
+// and as many stages, 3 to 6, as `budget` bytes of shared memory hold.
+bool ring_plan_c(int64_t nvec, int nt, int elem, int c, int max_v, int budget,
+                 rmsnorm_plan_t* p) {
+    constexpr int kSmemMax = 227 * 1024;
+    const int64_t slots = cdiv(nvec, c);
+    if (slots > ((elem == 4 && max_v >= 8) ? 4096 : 2048)) return false;
+    const int v = slots <= 2048 ? 4 : 8;
+    const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
+    const int unit = v * t * 16;
+    int stages = std::min(6, budget / (nt * unit));
+    while (stages > 3 && fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
+    if (stages < 3 || fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) return false;
+    p->variant = RMSNORM_VARIANT_RING;
+    p->cluster = c;
+    p->vectors_per_thread = v;
+    p->threads = t;
+    p->threads_per_row = t * c;
+    p->stages = stages;
+    p->smem_bytes = fwd_ring_smem_bytes(stages, unit, nt);
+    return true;
+}
+
 // The persistent ring kernel for a row of nvec vectors: the smallest cluster
 // (1, 2, 4, then 8 blocks) whose blocks hold a slice of at most 4096 vectors
-// (512 threads x 8; 2048 for 16-bit elements) with room for at least three ring stages in about
-// 200 KB of shared memory. nt tensors ride in the ring (2 with the residual).
+// (512 threads x 8; 2048 for 16-bit elements) with room for at least three
+// ring stages in about 200 KB of shared memory. nt tensors ride in the ring
+// (2 with the residual).
 bool fwd_ring_plan(int64_t nvec, int nt, int elem, rmsnorm_plan_t* p) {
-    constexpr int kSmemMax = 227 * 1024;
-    // 8 vectors a thread only for 32-bit elements: with 16-bit ones the
-    // unpacked pairs of 8 vectors spill
-    const int max_slots = elem == 4 ? 4096 : 2048;
-    const int forced = fwd_tuning().ring_cluster;
-    for (int c = forced > 0 ? forced : 1; c <= kMaxCluster; c = forced > 0 ? kMaxCluster + 1 : c * 2) {
-        const int64_t slots = cdiv(nvec, c);
-        if (slots > max_slots) continue;
-        const int v = slots <= 2048 ? 4 : 8;
-        const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
-        const int unit = v * t * 16;
-        int stages = std::min(6, fwd_tuning().ring_smem / (nt * unit));
-        while (stages > 3 && fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) --stages;
-        if (stages < 3 || fwd_ring_smem_bytes(stages, unit, nt) > kSmemMax) continue;
-        p->variant = RMSNORM_VARIANT_RING;
-        p->cluster = c;
-        p->vectors_per_thread = v;
-        p->threads = t;
-        p->threads_per_row = t * c;
-        p->stages = stages;
-        p->smem_bytes = fwd_ring_smem_bytes(stages, unit, nt);
-        return true;
-    }
+    const FwdTuning& tu = fwd_tuning();
+    if (tu.ring_cluster > 0) return ring_plan_c(nvec, nt, elem, tu.ring_cluster, 8, tu.ring_smem, p);
+    for (int c = 1; c <= kMaxCluster; c *= 2)
+        if (ring_plan_c(nvec, nt, elem, c, 8, tu.ring_smem, p)) return true;
     return false;
 }
 
@@ -914,8 +925,75 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
     p->vectors_per_thread = 0;
 }
 
-cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p,
-                            bool add) {
+namespace {
+
+// Ring plans chosen on a device, per (device, dtype, N).
+std::mutex g_ring_sel_mu;
+std::map<std::tuple<int, int, int64_t, bool>, rmsnorm_plan_t> g_ring_sel;
+
+// A row split over a ring cluster runs best where the clusters resident at
+// once times the threads resident with them is largest; ties go to more
+// resident blocks (two to an SM hide each other's per-row exchanges), then to
+// the deeper ring. The occupancy API counts them for cluster sizes 2, 4, 5, 6
+// and 8, four vectors a thread (also eight for fp32 rows) and stage budgets
+// of 100 and 200 KB (the residual rides in the ring too when there is one).
+// On GB300 this took bf16 N = 40960..57344 from 73..85% of the copy roofline
+// to 94..95% and N = 98304 from 69% to 85% (with the residual: 93% to 100%).
+cudaError_t ring_select(const DeviceInfo& dev, int dtype, int64_t N, bool add, rmsnorm_plan_t* p) {
+    const auto key = std::make_tuple(dev.device, dtype, N, add);
+    {
+        std::lock_guard<std::mutex> lk(g_ring_sel_mu);
+        auto it = g_ring_sel.find(key);
+        if (it != g_ring_sel.end()) {
+            *p = it->second;
+            return cudaSuccess;
+        }
+    }
+    const int elem = dtype_size(dtype);
+    const int64_t nvec = N / dtype_vec(dtype);
+    rmsnorm_plan_t best = *p;
+    int64_t best_score[3] = {-1, -1, -1};
+    for (int c : {2, 4, 5, 6, 8}) {
+        for (int max_v : {4, 8}) {
+            if (max_v == 8 && elem != 4) continue;
+            for (int budget : {100 * 1024, 200 * 1024}) {
+                rmsnorm_plan_t q = *p;
+                if (!ring_plan_c(nvec, add ? 2 : 1, elem, c, max_v, budget, &q)) continue;
+                if (q.smem_bytes > dev.max_smem_optin) continue;
+                const void* fn = ring_kernel_for(dtype, q.vectors_per_thread, add);
+                if (fn == nullptr) continue;
+                int units = 0;
+                if (ring_resident_units(dev, fn, q.threads, q.smem_bytes, c, &units) != cudaSuccess ||
+                    units < 1) {
+                    cudaGetLastError();  // an occupancy query that fails rules the shape out
+                    continue;
+                }
+                // rows in flight times resident threads, then resident blocks
+                const int64_t blocks = static_cast<int64_t>(units) * c;
+                const int64_t score[3] = {units * blocks * q.threads, blocks, q.stages};
+                if (std::lexicographical_compare(best_score, best_score + 3, score, score + 3)) {
+                    best = q;
+                    std::copy(score, score + 3, best_score);
+                }
+            }
+        }
+    }
+    std::lock_guard<std::mutex> lk(g_ring_sel_mu);
+    g_ring_sel[key] = best;
+    *p = best;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
+                            rmsnorm_plan_t* p, bool add) {
+    const FwdTuning& tu = fwd_tuning();
+    if (p->variant == RMSNORM_VARIANT_RING && p->cluster >= 2 && tu.ring_cluster == 0 &&
+        tu.ring_smem == 200 * 1024 && tu.wide_select >= (add ? 2 : 1)) {
+        cudaError_t e = ring_select(dev, dtype, N, add, p);
+        if (e != cudaSuccess) return e;
+    }
     switch (p->variant) {
         case RMSNORM_VARIANT_RING: {
             const void* fn = ring_kernel_for(dtype, p->vectors_per_thread, add);

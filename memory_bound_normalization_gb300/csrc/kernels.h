@@ -86,8 +86,8 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
 void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool res = false);
 
 // Device-dependent completion of a plan (grid size, shared-memory opt-in).
-cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, rmsnorm_plan_t* p,
-                            bool add = false);
+cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
+                            rmsnorm_plan_t* p, bool add = false);
 // `res`: the plan is for the backward with a residual gradient (its kernels
 // differ, and so may the number of resident blocks).
 cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,

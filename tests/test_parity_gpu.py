@@ -75,7 +75,8 @@ TYPE_IDS = ["bf16", "f32", "f16", "bf16_wf32", "f16_wf32"]
 
 SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (37, 256),
           (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (5, 6144), (4, 8192),
-          (3, 16384), (2, 32768), (3, 40960), (4, 49152), (2, 65536), (1, 65536), (2, 98304),
+          (3, 16384), (3, 20480), (5, 24576), (2, 32768), (3, 40960), (4, 49152), (3, 57344),
+          (2, 65536), (1, 65536), (2, 98304),
           (1000, 40), (777, 96)]
 
 
@@ -103,13 +104,40 @@ def test_rows_around_persistent_grid(N, dtype, w_dtype):
         check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
 
 
+@pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
+@pytest.mark.parametrize("N", [16384, 20480, 24576, 32768, 40960, 49152, 57344, 65536, 98304,
+                               131072])
+def test_device_chosen_wide_shapes(N, dtype, w_dtype):
+    """Wide rows take a cluster shape chosen with the occupancy API: every
+    pass's plan covers the row with a legal block, cluster and ring, and
+    asking again gives the same plan (so dw keeps its bits)."""
+    code = pkg.dtype_code(dtype, w_dtype)
+    vec = 4 if dtype == torch.float32 else 8
+    for pass_ in (pkg.PASS_FWD, pkg.PASS_FWD_ADD, pkg.PASS_BWD, pkg.PASS_BWD_RES):
+        p = pkg.rmsnorm_plan(1 << 20, N, code, pass_, 0)
+        q = pkg.rmsnorm_plan(1 << 20, N, code, pass_, 0)
+        fields = ("variant", "cluster", "threads", "vectors_per_thread", "stages", "smem_bytes",
+                  "grid")
+        assert all(getattr(p, f) == getattr(q, f) for f in fields)
+        name = pkg.VARIANTS[p.variant]
+        if name not in ("ring", "cluster_row"):
+            continue
+        assert p.cluster in (1, 2, 4, 5, 6, 8) and 32 <= p.threads <= 512
+        assert p.threads * p.vectors_per_thread * p.cluster * vec >= N
+        assert p.vectors_per_thread in (4, 8)
+        if dtype != torch.float32:
+            assert p.vectors_per_thread == 4
+        assert 2 <= p.stages <= 6 and p.smem_bytes <= 227 * 1024
+        assert p.grid % p.cluster == 0 and p.grid > 0
+
+
 @pytest.mark.parametrize("dtype,w_dtype", [(torch.bfloat16, None), (torch.float32, None)],
                          ids=["bf16", "f32"])
-@pytest.mark.parametrize("N", [40960, 49152, 65536, 98304])
+@pytest.mark.parametrize("N", [24576, 40960, 49152, 65536, 98304])
 def test_wide_rows_around_cluster_grid(N, dtype, w_dtype):
-    """Rows split over clusters of 5, 6 or 8 blocks (4 for bf16 at 65536):
-    M just below, at and above the number of co-resident clusters, and a
-    ragged multiple of it."""
+    """Rows split over a cluster of the shape chosen on the device: M just
+    below, at and above the number of co-resident clusters, and a ragged
+    multiple of it."""
     code = pkg.dtype_code(dtype, w_dtype)
     plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_BWD, 0)
     P = plan.partial_rows
