@@ -127,8 +127,10 @@ def test_device_chosen_wide_shapes(N, dtype, w_dtype):
         assert p.vectors_per_thread in (4, 8)
         if dtype != torch.float32:
             assert p.vectors_per_thread == 4
-        assert 2 <= p.stages <= 6 and p.smem_bytes <= 227 * 1024
+        assert p.smem_bytes <= 227 * 1024
         assert p.grid % p.cluster == 0 and p.grid > 0
+        if name == "ring" or pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES):
+            assert 2 <= p.stages <= 6  # the forward's one-shot cluster kernel has no ring
 
 
 @pytest.mark.parametrize("dtype,w_dtype", [(torch.bfloat16, None), (torch.float32, None)],
