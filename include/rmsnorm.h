@@ -94,6 +94,8 @@ int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
  * The partial rows live in a workspace that this call takes from the
  * stream-ordered allocator (cudaMallocAsync/cudaFreeAsync on `stream`);
  * RMSNORM_ERR_NOMEM if that fails. Use rmsnorm_bwd_ws to pass your own.
+ * When the rows are few enough for one block (or one cluster) to take them
+ * all, its partial row is dw itself: one kernel, no workspace, no allocation.
  */
 int rmsnorm_bwd(const void *x, const void *w, const void *dy,
                 const float *rstd, void *dx, float *dw,
@@ -101,7 +103,9 @@ int rmsnorm_bwd(const void *x, const void *w, const void *dy,
 
 /*
  * Bytes of workspace rmsnorm_bwd_ws needs for this shape on `device`
- * (a CUDA ordinal). Returns 0 when M == 0 or the arguments are invalid.
+ * (a CUDA ordinal). Returns 0 when M == 0, when one block or cluster takes
+ * every row (its partial row is dw itself), or when the arguments are
+ * invalid.
  */
 size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype,
                                   int device);
@@ -111,8 +115,8 @@ size_t rmsnorm_bwd_workspace_size(int64_t M, int64_t N, int dtype,
  * rmsnorm_bwd_workspace_size(M, N, dtype, current device) bytes, 16-byte
  * aligned, not read by the caller until the stream reaches the end of the
  * call, and not shared with another call in flight. A smaller or NULL
- * workspace (with M > 0) returns RMSNORM_ERR_INVALID_ARG; misaligned returns
- * RMSNORM_ERR_MISALIGNED. Allocates nothing.
+ * workspace (with M > 0 and a nonzero need) returns RMSNORM_ERR_INVALID_ARG;
+ * misaligned returns RMSNORM_ERR_MISALIGNED. Allocates nothing.
  */
 int rmsnorm_bwd_ws(const void *x, const void *w, const void *dy,
                    const float *rstd, void *dx, float *dw,

@@ -142,6 +142,8 @@ int bwd_alloc_run(const void* x, const void* w, const void* dy, const float* rst
         if (dw == nullptr) return RMSNORM_OK;
         return cuda_status(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream));
     }
+    if (plan.workspace_bytes == 0)  // one partial row: written straight to dw
+        return bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, nullptr, stream, dres);
     void* ws = nullptr;
     if (cuda_status(cudaMallocAsync(&ws, static_cast<size_t>(plan.workspace_bytes), stream)) !=
         RMSNORM_OK)
@@ -225,7 +227,8 @@ int rmsnorm_bwd_ws(const void* x, const void* w, const void* dy, const float* rs
         if (dw == nullptr) return RMSNORM_OK;
         return cuda_status(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * 4, stream));
     }
-    if (workspace == nullptr || workspace_bytes < static_cast<size_t>(plan.workspace_bytes))
+    if (plan.workspace_bytes > 0 &&
+        (workspace == nullptr || workspace_bytes < static_cast<size_t>(plan.workspace_bytes)))
         return RMSNORM_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return RMSNORM_ERR_MISALIGNED;
     return bwd_run(x, w, dy, rstd, dx, dw, M, N, dtype, *dev, plan, workspace, stream);

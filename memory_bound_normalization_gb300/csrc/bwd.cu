@@ -396,7 +396,8 @@ cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t
     const int64_t n = std::min<int64_t>(units, work);
     p->partial_rows = static_cast<int>(n);
     p->grid = static_cast<int>(n * p->cluster);
-    p->workspace_bytes = (n * N * 4 + 255) / 256 * 256;
+    // one partial row is dw itself: no workspace and no column sum
+    p->workspace_bytes = n == 1 ? 0 : (n * N * 4 + 255) / 256 * 256;
     return cudaSuccess;
 }
 
@@ -427,10 +428,12 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
         cfg.numAttrs = 2;
     }
     BwdArgs args = a;
+    if (p.partial_rows == 1) args.partial = a.dw;  // the one partial row is dw
     int stages = p.stages, groups = p.row_groups;
     void* kargs[3] = {&args, &stages, &groups};
     cudaError_t err = cudaLaunchKernelExC(&cfg, fn, kargs);
     if (err != cudaSuccess) return err;
+    if (p.partial_rows == 1) return cudaSuccess;
     // the column sum may launch early and waits on the grid above
     // (programmatic dependent launch) instead of a full stream boundary
     cudaLaunchConfig_t cs = {};

@@ -258,6 +258,44 @@ def test_workspace_entry_point():
     check_all(x, w, dy, eps, y, rstd, dx, dw)
 
 
+@pytest.mark.parametrize("M,N,dtype", [(1, 4096, torch.bfloat16), (4, 4096, torch.bfloat16),
+                                     (2, 128, torch.bfloat16), (1, 13, torch.bfloat16),
+                                     (1, 65536, torch.float32), (1, 40960, torch.bfloat16)],
+                         ids=["1x4096", "4x4096", "2x128", "1x13", "1x65536f32", "1x40960"])
+def test_single_partial_row_is_dw(M, N, dtype):
+    """Rows few enough for one block (or one cluster) of the persistent
+    backward: its partial row is written to dw directly, with no workspace
+    and no column sum; every entry point agrees bit for bit."""
+    code = pkg.dtype_code(dtype)
+    plan = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD, 0)
+    if plan.partial_rows != 1:
+        # several clusters can be resident; one row per cluster then
+        assert M > 1 and plan.partial_rows == min(M, plan.grid // plan.cluster)
+        pytest.skip("more than one partial row on this device")
+    assert plan.workspace_bytes == 0
+    # the size query covers the scalar plan too, which has one partial row
+    # per row here: none at M = 1
+    assert (pkg.rmsnorm_bwd_workspace_size(M, N, code, 0) == 0) == (M == 1)
+    inp, eps = inputs(M, N, dtype, seed=M)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    y, rstd = pkg.forward(x, w, eps)
+    dx = torch.empty_like(x)
+    dw = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+    pkg.check(pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx, dw, M, N, code, 0, 0))
+    dx2, dw2 = pkg.backward(x, w, dy, rstd)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dx2) and torch.equal(dw.view(torch.int32), dw2.view(torch.int32))
+    check_all(x, w, dy, eps, y, rstd, dx, dw)
+    # the residual backward takes the same path
+    dres = inputs(M, N, dtype, seed=M + 50)[0]["dy"]
+    dxr = torch.empty_like(x)
+    dwr = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+    pkg.check(pkg.rmsnorm_add_bwd(x, w, dy, rstd, dres, dxr, dwr, M, N, code))
+    torch.cuda.synchronize()
+    assert torch.equal(dwr, dw)  # dres does not enter dw
+    check_rows(dxr, oracle.add_bwd_dx(x.cpu(), w.cpu(), dy.cpu(), dres.cpu(), eps), dtype, "dx")
+
+
 @pytest.mark.parametrize("wl_name", ["hidden4096_16384x4096", "qknorm_1048576x128",
                                      "sweep_bf16_N65536", "sweep_f32_N2880",
                                      "hidden4096_16384x4096_f16",
