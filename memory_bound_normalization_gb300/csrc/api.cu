@@ -90,6 +90,7 @@ int bwd_run(const void* x, const void* w, const void* dy, const float* rstd, voi
     a.M = M;
     a.N = static_cast<int>(N);
     a.status = dev.status_word;
+    a.sm_count = dev.sm_count;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.drop_unit = plan.variant != RMSNORM_VARIANT_SCALAR ? g_drop_unit.exchange(-1) : -1;
     a.dres = dres;

@@ -64,11 +64,13 @@ const BwdTuning& tuning() {
 
 // ---------------------------------------------------------- column sum
 // dw[j] = sum over p of partial[p][j] in a fixed tree: thread row q of the
-// block sums p = q, q+32, q+64, ... in ascending order, then the 32 sums are
-// added in q order. Same bits on every run for a given P.
-__global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ partial,
-                                                      float* __restrict__ dw, int P, int N) {
-    __shared__ float part[32][33];
+// block (Q rows of 32 threads, 32 columns) sums p = q, q+Q, q+2Q, ... in
+// ascending order, then the Q sums are added in q order. Same bits on every
+// run for a given P and Q.
+template <int Q>
+__global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict__ partial,
+                                                        float* __restrict__ dw, int P, int N) {
+    __shared__ float part[Q][33];
     wait_for_prerequisite_grid();  // partial rows complete and visible
     allow_dependent_launch();
     const int cx = threadIdx.x, q = threadIdx.y;
@@ -76,16 +78,39 @@ __global__ void __launch_bounds__(1024) colsum_kernel(const float* __restrict__ 
     float s = 0.f;
     if (col < N) {
 #pragma unroll 4
-        for (int p = q; p < P; p += 32) s += partial[static_cast<int64_t>(p) * N + col];
+        for (int p = q; p < P; p += Q) s += partial[static_cast<int64_t>(p) * N + col];
     }
     part[q][cx] = s;
     __syncthreads();
     if (q == 0 && col < N) {
         float t = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) t += part[i][cx];
+        for (int i = 0; i < Q; ++i) t += part[i][cx];
         dw[col] = t;
     }
+}
+
+// The column-sum kernel with q thread rows (a power of two up to 32).
+const void* colsum_kernel_for(int q) {
+    switch (q) {
+        case 1: return reinterpret_cast<const void*>(&colsum_kernel<1>);
+        case 2: return reinterpret_cast<const void*>(&colsum_kernel<2>);
+        case 4: return reinterpret_cast<const void*>(&colsum_kernel<4>);
+        case 8: return reinterpret_cast<const void*>(&colsum_kernel<8>);
+        case 16: return reinterpret_cast<const void*>(&colsum_kernel<16>);
+        default: return reinterpret_cast<const void*>(&colsum_kernel<32>);
+    }
+}
+
+// Thread rows of the column sum: 32 while one wave of blocks (32 columns
+// each) covers every column, halved for wider rows until it does. With 32
+// rows at N = 65536 the sum ran as about seven waves of blocks that each
+// read one or two values a thread.
+int colsum_phases(int N, int sm_count) {
+    const int64_t resident = static_cast<int64_t>(std::max(1, sm_count)) * 2048;
+    int q = 32;
+    while (q > 1 && static_cast<int64_t>(N) * q > resident) q >>= 1;
+    return q;
 }
 // ------------------------------------------------------------ host side
 const void* main_kernel_for(int dtype, const rmsnorm_plan_t& p, bool res) {
@@ -402,8 +427,14 @@ cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t
 }
 
 cudaError_t colsum_launch(const float* partial, float* dw, int P, int N, cudaStream_t s) {
-    colsum_kernel<<<static_cast<unsigned>(cdiv(N, 32)), dim3(32, 32), 0, s>>>(partial, dw, P, N);
-    return cudaGetLastError();
+    int device = 0;
+    cudaError_t err = cudaGetDevice(&device);
+    if (err != cudaSuccess) return err;
+    const DeviceInfo* dev = device_info(device);
+    const int q = colsum_phases(N, dev ? dev->sm_count : 1);
+    const void* fn = colsum_kernel_for(q);
+    void* args[4] = {&partial, &dw, &P, &N};
+    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(cdiv(N, 32))), dim3(32, q), args, 0, s);
 }
 
 cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cudaStream_t s) {
@@ -437,8 +468,9 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     // the column sum may launch early and waits on the grid above
     // (programmatic dependent launch) instead of a full stream boundary
     cudaLaunchConfig_t cs = {};
+    const int q = colsum_phases(a.N, a.sm_count);
     cs.gridDim = dim3(static_cast<unsigned>(cdiv(a.N, 32)));
-    cs.blockDim = dim3(32, 32);
+    cs.blockDim = dim3(32, static_cast<unsigned>(q));
     cs.stream = s;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -446,7 +478,10 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cs.attrs = pdl;
     cs.numAttrs = 1;
     const float* part = a.partial;
-    return cudaLaunchKernelEx(&cs, colsum_kernel, part, a.dw, p.partial_rows, a.N);
+    float* dw = a.dw;
+    int P = p.partial_rows, N = a.N;
+    void* cargs[4] = {&part, &dw, &P, &N};
+    return cudaLaunchKernelExC(&cs, colsum_kernel_for(q), cargs);
 }
 
 }  // namespace rmsn

@@ -48,6 +48,7 @@ struct BwdArgs {
     uint64_t wait_limit_ns;
     int64_t drop_unit;  // failure-injection hook, -1 = off
     const void* dres;   // gradient added to dx (residual path), nullptr = none
+    int sm_count;       // the device's SMs (sizes the column sum)
 };
 
 constexpr int kMaxCluster = 8;

@@ -101,6 +101,7 @@ extern "C" int rmsnorm_bwd_noalloc(const void* x, const void* w, const void* dy,
     a.M = M;
     a.N = static_cast<int>(N);
     a.status = dev->status_word;
+    a.sm_count = dev->sm_count;
     a.wait_limit_ns = 1000000000ull;  // one second, as for the other entry points by default
     a.drop_unit = -1;
     if (bwd_launch(plan, dtype, a, stream) != cudaSuccess) {
