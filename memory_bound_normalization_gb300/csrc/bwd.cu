@@ -90,6 +90,55 @@ __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict_
     }
 }
 
+// Narrow rows (N < 2048): C columns by R = 1024/C thread rows a block, C
+// chosen so that at least 64 blocks share the sum. Thread row q adds
+// p = q, q+R, q+2R, ... in ascending order, then the R sums of a column are
+// added by a fixed pairwise tree (halving strides), the same bits on every
+// run for a given P, N and C. With 32 columns a block, QK-norm's 608 partial
+// rows of 128 columns went to 4 blocks whose threads read 19 values each, one
+// after another.
+template <int C>
+__global__ void __launch_bounds__(1024) colsum_narrow_kernel(const float* __restrict__ partial,
+                                                             float* __restrict__ dw, int P,
+                                                             int N) {
+    constexpr int R = 1024 / C;
+    __shared__ float part[R][C + 1];
+    wait_for_prerequisite_grid();  // partial rows complete and visible
+    allow_dependent_launch();
+    const int cx = threadIdx.x, q = threadIdx.y;
+    const int64_t col = static_cast<int64_t>(blockIdx.x) * C + cx;
+    float s = 0.f;
+    if (col < N) {
+#pragma unroll 2
+        for (int p = q; p < P; p += R) s += partial[static_cast<int64_t>(p) * N + col];
+    }
+    part[q][cx] = s;
+    __syncthreads();
+#pragma unroll
+    for (int h = R / 2; h > 0; h >>= 1) {
+        if (q < h) part[q][cx] += part[q + h][cx];
+        __syncthreads();
+    }
+    if (q == 0 && col < N) dw[col] = part[0][cx];
+}
+
+// Columns a block of the narrow column sum takes: at least 64 blocks.
+int colsum_narrow_cols(int N) {
+    int c = 16;
+    while (c > 1 && N < 64 * c) c >>= 1;
+    return c;
+}
+
+const void* colsum_narrow_for(int c) {
+    switch (c) {
+        case 16: return reinterpret_cast<const void*>(&colsum_narrow_kernel<16>);
+        case 8: return reinterpret_cast<const void*>(&colsum_narrow_kernel<8>);
+        case 4: return reinterpret_cast<const void*>(&colsum_narrow_kernel<4>);
+        case 2: return reinterpret_cast<const void*>(&colsum_narrow_kernel<2>);
+        default: return reinterpret_cast<const void*>(&colsum_narrow_kernel<1>);
+    }
+}
+
 // The column-sum kernel with q thread rows (a power of two up to 32).
 const void* colsum_kernel_for(int q) {
     switch (q) {
@@ -101,6 +150,9 @@ const void* colsum_kernel_for(int q) {
         default: return reinterpret_cast<const void*>(&colsum_kernel<32>);
     }
 }
+
+// Rows narrower than this take the narrow column sum.
+constexpr int kColsumNarrowBelow = 2048;
 
 // Thread rows of the column sum: 32 while one wave of blocks (32 columns
 // each) covers every column, halved for wider rows until it does. With 32
@@ -431,9 +483,14 @@ cudaError_t colsum_launch(const float* partial, float* dw, int P, int N, cudaStr
     cudaError_t err = cudaGetDevice(&device);
     if (err != cudaSuccess) return err;
     const DeviceInfo* dev = device_info(device);
+    void* args[4] = {&partial, &dw, &P, &N};
+    if (N < kColsumNarrowBelow) {
+        const int c = colsum_narrow_cols(N);
+        return cudaLaunchKernel(colsum_narrow_for(c), dim3(static_cast<unsigned>(cdiv(N, c))),
+                                dim3(c, 1024 / c), args, 0, s);
+    }
     const int q = colsum_phases(N, dev ? dev->sm_count : 1);
     const void* fn = colsum_kernel_for(q);
-    void* args[4] = {&partial, &dw, &P, &N};
     return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(cdiv(N, 32))), dim3(32, q), args, 0, s);
 }
 
@@ -468,9 +525,12 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     // the column sum may launch early and waits on the grid above
     // (programmatic dependent launch) instead of a full stream boundary
     cudaLaunchConfig_t cs = {};
+    const bool narrow = a.N < kColsumNarrowBelow;
     const int q = colsum_phases(a.N, a.sm_count);
-    cs.gridDim = dim3(static_cast<unsigned>(cdiv(a.N, 32)));
-    cs.blockDim = dim3(32, static_cast<unsigned>(q));
+    const int c = colsum_narrow_cols(a.N);
+    cs.gridDim = dim3(static_cast<unsigned>(narrow ? cdiv(a.N, c) : cdiv(a.N, 32)));
+    cs.blockDim = narrow ? dim3(static_cast<unsigned>(c), static_cast<unsigned>(1024 / c))
+                         : dim3(32, static_cast<unsigned>(q));
     cs.stream = s;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -481,7 +541,7 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     float* dw = a.dw;
     int P = p.partial_rows, N = a.N;
     void* cargs[4] = {&part, &dw, &P, &N};
-    return cudaLaunchKernelExC(&cs, colsum_kernel_for(q), cargs);
+    return cudaLaunchKernelExC(&cs, narrow ? colsum_narrow_for(c) : colsum_kernel_for(q), cargs);
 }
 
 }  // namespace rmsn

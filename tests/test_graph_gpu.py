@@ -118,3 +118,32 @@ def test_graph_replay_residual_in_place(M, N, dtype):
         for got, want in zip((res, y, rstd, dres, dw), ref):
             assert torch.equal(got, want)
     assert pkg.rmsnorm_get_last_device_error() == pkg.OK
+
+
+@pytest.mark.parametrize("M,N,dtype", [(48, 45056, torch.bfloat16), (8, 28672, F32),
+                                       (40, 1000, torch.bfloat16)])
+def test_first_call_inside_capture(M, N, dtype):
+    """A width's first call may come inside stream capture: its plan (the
+    device's cluster-shape choice included) is made there, and the replay
+    matches eager calls bit for bit. The widths are used by no other test."""
+    wl = synth.Workload(f"cap{M}x{N}", M, N, dtype, 1e-6, 71, 72, 73)
+    inp = synth.make_inputs(wl, device=DEV)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    code = pkg.dtype_code(dtype)
+    y = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=DEV)
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=torch.float32, device=DEV)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        s = torch.cuda.current_stream()
+        pkg.check(pkg.rmsnorm_fwd(x, w, y, rstd, M, N, wl.eps, code, s))
+        pkg.check(pkg.rmsnorm_bwd(x, w, dy, rstd, dx, dw, M, N, code, s))
+    graph.replay()
+    torch.cuda.synchronize()
+    y2, r2 = pkg.forward(x, w, wl.eps)
+    dx2, dw2 = pkg.backward(x, w, dy, r2)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2) and torch.equal(rstd, r2)
+    assert torch.equal(dx, dx2) and torch.equal(dw, dw2)
+    assert pkg.rmsnorm_get_last_device_error() == pkg.OK
