@@ -76,7 +76,7 @@ TYPE_IDS = ["bf16", "f32", "f16", "bf16_wf32", "f16_wf32"]
 SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (37, 256),
           (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (5, 6144), (4, 8192),
           (3, 16384), (3, 20480), (5, 24576), (2, 32768), (3, 40960), (4, 49152), (3, 57344),
-          (2, 65536), (1, 65536), (2, 98304),
+          (2, 65536), (1, 65536), (2, 98304), (3, 131072),
           (1000, 40), (777, 96)]
 
 
@@ -133,10 +133,13 @@ def test_device_chosen_wide_shapes(N, dtype, w_dtype):
             assert 2 <= p.stages <= 6  # the forward's one-shot cluster kernel has no ring
 
 
-@pytest.mark.parametrize("dtype,w_dtype", [(torch.bfloat16, None), (torch.float32, None)],
-                         ids=["bf16", "f32"])
-@pytest.mark.parametrize("N", [24576, 40960, 49152, 65536, 98304])
-def test_wide_rows_around_cluster_grid(N, dtype, w_dtype):
+WIDE_GRID = [(N, dt) for N in (24576, 40960, 49152, 65536, 98304)
+             for dt in (torch.bfloat16, torch.float32)] + [(131072, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("N,dtype", WIDE_GRID,
+                         ids=[f"{n}-{str(d)[6:]}" for n, d in WIDE_GRID])
+def test_wide_rows_around_cluster_grid(N, dtype, w_dtype=None):
     """Rows split over a cluster of the shape chosen on the device: M just
     below, at and above the number of co-resident clusters, and a ragged
     multiple of it."""
