@@ -644,7 +644,9 @@ def run_ours(args):
         "clocks": clock_info,
         "e2e": e2e,
         "small_m": small_m,
-        "gpu_launches": (4 if naive else 3) * K,  # ours only: fwd, main bwd, column sum(s)
+        # ours only: fwd, main bwd and its column sum (none with one partial row);
+        # the naive chain is three kernels behind the forward
+        "gpu_launches": (4 if naive else 2 + (plan_b["partial_rows"] > 1)) * K,
         "validation": errs,
         "library": {"path": pkg.library_path(), "source_hash": libbuild.source_hash(),
                     "bwd_kernel_hash": libbuild.kernel_source_hash(),
