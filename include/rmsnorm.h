@@ -285,7 +285,7 @@ typedef struct {
     int threads_per_row;    /* lanes sharing one row (ROWGROUP), else threads */
     int rows_per_unit;      /* rows per block pass (row-group tile, or row
                                groups); TWO_PASS: blocks per SM */
-    int cluster;            /* blocks per row (1 unless CLUSTER_ROW) */
+    int cluster;            /* blocks per row (1 unless CLUSTER_ROW or RING) */
     int row_groups;         /* independent row groups per block (backward
                                CTA_ROW: each group of threads/row_groups
                                threads owns its own rows; else 1) */
@@ -293,15 +293,19 @@ typedef struct {
     int smem_bytes;         /* dynamic shared memory per block */
     int grid;               /* blocks launched; 0 when device < 0 */
     int partial_rows;       /* dw partial rows written (backward), else 0 */
-    int64_t workspace_bytes;/* backward workspace, 0 for the forward */
+    int64_t workspace_bytes;/* backward workspace: 0 for the forward, and 0
+                               when one partial row (written to dw) suffices */
 } rmsnorm_plan_t;
 
 /*
  * Describe, without launching anything, what the pass named by `pass`
  * (rmsnorm_pass_t) would run for this shape with 16-byte aligned
  * pointers. With device >= 0 the grid and workspace are filled in from
- * that device's properties (needs a GPU); with device < 0 only the
- * width-dependent choices are made (host only). Returns a status code.
+ * that device's properties (needs a GPU), and a row split over a cluster
+ * gets the cluster shape the calls use on that device (chosen with the
+ * occupancy API, once per dtype and N); with device < 0 only the
+ * width-dependent choices of the static ladder are made (host only), which
+ * for such rows may differ from what runs. Returns a status code.
  */
 int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device,
                  rmsnorm_plan_t *out);
