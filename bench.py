@@ -67,6 +67,9 @@ def parse_args(argv=None):
                         "naive: rmsnorm_fwd + the naive three-kernel rmsnorm_bwd_naive "
                         "(ablation)")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--ref-seconds", type=float, default=120.0,
+                   help="host time the reference arm (the fp64 oracle) spends over all its "
+                        "warm-up and timed steps")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle budget for the cpu_baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -845,7 +848,7 @@ def run_reference(args):
 
     t = one(4)
     per_row = t / 4
-    total_budget = 120.0
+    total_budget = args.ref_seconds
     rows = int(max(1, min(rows_avail, total_budget / max(1, args.steps + args.warmup) / per_row)))
     for _ in range(args.warmup):
         one(rows)

@@ -70,3 +70,18 @@ def test_cpu_baseline_reports_one_thread_and_all_cores():
     if cores > 1:
         allc = got["all_cores"]
         assert allc["cores"] == cores and allc["value"] > 0 and allc["unit"] == got["unit"]
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """bench.py --impl reference: the fp64 oracle on the host cores, one JSON
+    line with the keys the contract names (small budget here)."""
+    import json
+
+    bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1", "--ref-seconds", "0.3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["steps"] == 2 and line["warmup"] == 1 and line["n_gpus"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["metric"] and line["config"]["workload"]
