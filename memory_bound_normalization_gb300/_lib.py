@@ -148,10 +148,19 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
 
 
 def _ptr(t) -> int | None:
+    """Device address of a tensor argument (None and raw integer addresses
+    pass through). Host or non-contiguous tensors are refused here, before
+    anything reaches the library: its kernels read every tensor as dense
+    row-major device memory."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"tensor argument on {t.device}: the library takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensor argument is not contiguous: the library takes dense row-major "
+                         "tensors (call .contiguous() first)")
     return t.data_ptr()
 
 

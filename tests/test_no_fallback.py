@@ -54,3 +54,15 @@ def test_package_never_imports_the_oracle():
     for f in os.listdir(csrc):
         text = open(os.path.join(csrc, f)).read()
         assert "rmsnorm_oracle" not in text and "oracle_rmsnorm" not in text, f
+
+
+def test_host_tensors_are_refused_before_the_library():
+    """Tensor arguments must be CUDA tensors: a host tensor raises in the
+    binding, so no host address ever reaches a kernel."""
+    import pytest
+    import torch
+
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    w = torch.ones(64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        pkg.rmsnorm_fwd(x, w, x, torch.zeros(4), 4, 64, 1e-6, pkg.BF16, 0)

@@ -237,6 +237,21 @@ def test_empty_and_degenerate():
     assert pkg.rmsnorm_fwd(0, w, y, rstd, 4, 64, 1e-6, pkg.BF16) == pkg.ERR_INVALID_ARG
 
 
+def test_strided_and_host_tensors_are_refused():
+    """The kernels read dense row-major device memory: a transposed view or a
+    host tensor raises in the binding and nothing is launched."""
+    x = torch.randn(64, 128, device=DEV, dtype=torch.bfloat16)
+    w = torch.ones(64, device=DEV, dtype=torch.bfloat16)
+    y = torch.full((128, 64), 7.0, device=DEV, dtype=torch.bfloat16)
+    rstd = torch.zeros(128, device=DEV)
+    with pytest.raises(ValueError, match="contiguous"):
+        pkg.rmsnorm_fwd(x.t(), w, y, rstd, 128, 64, 1e-6, pkg.BF16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        pkg.rmsnorm_fwd(x.t().contiguous().cpu(), w, y, rstd, 128, 64, 1e-6, pkg.BF16)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
 def test_workspace_entry_point():
     M, N = 300, 4096
     inp, eps = inputs(M, N, torch.bfloat16)
