@@ -85,3 +85,15 @@ def test_reference_arm_prints_the_contract_line(capsys):
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["metric"] and line["config"]["workload"]
+
+
+def test_profiled_traffic_only_for_the_current_sources():
+    """roofline.traffic comes from the committed ncu summary of the backward
+    only while that summary's source hash is the current one."""
+    from memory_bound_normalization_gb300 import build
+
+    h = build.kernel_source_hash()
+    got = bench.read_profiled_traffic("rmsnorm_bwd", "hidden4096_16384x4096", h)
+    assert got is not None and 300_000_000 < got < 410_000_000  # about the call's logical bytes
+    assert bench.read_profiled_traffic("rmsnorm_bwd", "hidden4096_16384x4096", "0" * 16) is None
+    assert bench.read_profiled_traffic("rmsnorm_bwd", "no_such_workload", h) is None
