@@ -87,13 +87,14 @@ def test_reference_arm_prints_the_contract_line(capsys):
     assert line["metric"] and line["config"]["workload"]
 
 
-def test_profiled_traffic_only_for_the_current_sources():
-    """roofline.traffic comes from the committed ncu summary of the backward
-    only while that summary's source hash is the current one."""
-    from memory_bound_normalization_gb300 import build
-
-    h = build.kernel_source_hash()
-    got = bench.read_profiled_traffic("rmsnorm_bwd", "hidden4096_16384x4096", h)
-    assert got is not None and 300_000_000 < got < 410_000_000  # about the call's logical bytes
-    assert bench.read_profiled_traffic("rmsnorm_bwd", "hidden4096_16384x4096", "0" * 16) is None
-    assert bench.read_profiled_traffic("rmsnorm_bwd", "no_such_workload", h) is None
+def test_profiled_traffic_only_for_the_current_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary of the backward
+    only while that summary's source hash is the one given (the current
+    sources'); a missing summary or another hash gives None."""
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "rmsnorm_bwd_wl.md").write_text(
+        "# summary\n\nsource_hash: 0123456789abcdef\n\ntraffic_bytes_per_launch: 354168064\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.read_profiled_traffic("rmsnorm_bwd", "wl", "0123456789abcdef") == 354168064
+    assert bench.read_profiled_traffic("rmsnorm_bwd", "wl", "fedcba9876543210") is None
+    assert bench.read_profiled_traffic("rmsnorm_bwd", "other", "0123456789abcdef") is None
