@@ -321,6 +321,33 @@ def pin_row_selection(o):
     assert np.array_equal(y_last[0], y_all[5])
 
 
+def pin_nan_and_inf_rows(o):
+    """IEEE 754 semantics of the definition on non-finite input: a NaN in a
+    row makes that row's sum of squares NaN, so its r, y and dx are NaN in
+    every column and every column of dw is NaN; an infinity makes the sum
+    infinite, so r = 1/sqrt(inf) = 0, y is 0 except NaN (inf * 0) where the
+    infinity sits, and dx is NaN across the row (its dot with g is NaN).
+    Rows without such values are computed as if the others were absent."""
+    x = _rows(4, 7, 50)
+    w = _rng(51).standard_normal(7)
+    dy = _rows(4, 7, 52)
+    x[1, 3] = math.nan
+    x[2, 5] = math.inf
+    y, r = o.fwd(x, w, 1e-5)
+    dx = o.bwd_dx(x, w, dy, 1e-5)
+    dw = o.bwd_dw(x, dy, 1e-5)
+    assert np.isnan(r[1]) and np.isnan(y[1]).all() and np.isnan(dx[1]).all()
+    assert r[2] == 0.0
+    assert np.isnan(y[2, 5]) and np.all(y[2, np.arange(7) != 5] == 0.0)
+    assert np.isnan(dx[2]).all()
+    assert np.isnan(dw).all()
+    clean = [0, 3]
+    y_c, r_c = o.fwd(x[clean], w, 1e-5)
+    dx_c = o.bwd_dx(x[clean], w, dy[clean], 1e-5)
+    assert np.array_equal(y[clean], y_c) and np.array_equal(r[clean], r_c)
+    assert np.array_equal(dx[clean], dx_c)
+
+
 # ------------------------------------------------- rounding and residual add
 
 def _f16_ties(rng, n):
@@ -470,6 +497,7 @@ ALL_PINS = [
     pin_f16_decoding,
     pin_mixed_weight_dtype,
     pin_row_selection,
+    pin_nan_and_inf_rows,
     pin_rounding_matches_numpy,
     pin_bf16_rounding,
     pin_add_printed_example,
