@@ -12,11 +12,22 @@ Timing rules:
     events), so no call is served from L2;
   * each call is bracketed by CUDA events on the stream it is launched on;
   * the HBM roofline is measured in the same run (best of copy, pure write
-    and 2-read-1-write probes) before and after the timed region, to catch
-    drift; the measured copy bandwidth (MEASURED_PEAKS.json) is the
-    reported `roofline.peak`;
+    and 2-read-1-write probes over 4 GiB, 20 samples each) at the start and
+    again after every timed cell, and a closing / opening ratio below 0.98
+    is flagged as drift; the measured copy bandwidth
+    (MEASURED_PEAKS.json) is the reported `roofline.peak`, and a copy timed
+    under the cells' own flush-then-events protocol is reported beside it;
+  * `steady` times the same calls back to back with no flush, as in a
+    training step, where each call also pays for writing back what the call
+    before left dirty in L2;
   * SM clocks and throttle reasons are sampled with nvidia-smi during the
-    timed region.
+    timed region; before the first launch a read-only nvidia-smi query
+    checks that no other process is using the GPU (flagged in `idle_gate`,
+    or refused with --require-idle).
+
+The default run also times the width sweep and the other named workloads
+(256 x 1024, 32768 x 8192 with outliers, QK-norm 1048576 x 128) under the
+same rules, and records the run environment in `env`.
 
 `--impl reference` times the fp64 CPU oracle (the slow, obviously correct
 restatement of the method) on the host cores, on a bounded sample of rows of
@@ -34,6 +45,7 @@ import dataclasses
 import io
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -47,6 +59,8 @@ if ROOT not in sys.path:
 METRIC = "RMSNorm fwd+bwd GB/s and % of measured HBM roofline, bf16 M×N sweep"
 DEFAULT_WORKLOAD = "hidden4096_16384x4096"
 FALLBACK_HBM_GBS = 6800.0
+# closing / opening probe ratio below which the run is flagged as drifting
+DRIFT_LIMIT = 0.98
 
 
 # --------------------------------------------------------------------- setup
@@ -79,6 +93,20 @@ def parse_args(argv=None):
     p.add_argument("--sweep-steps", type=int, default=30)
     p.add_argument("--no-small-m", action="store_true",
                    help="skip the small-M eager vs CUDA-graph latency table")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other named workloads (256 x 1024, 32768 x 8192 with "
+                        "outliers, QK-norm 1048576 x 128), each validated and timed like the "
+                        "main workload with --config-steps steps")
+    p.add_argument("--config-steps", type=int, default=100)
+    p.add_argument("--steady-steps", type=int, default=500,
+                   help="back-to-back forward + backward steps of the steady-state block "
+                        "(no flush between calls); 0 skips it")
+    p.add_argument("--probe-gib", type=float, default=4.0,
+                   help="buffer size of each in-run roofline probe, GiB")
+    p.add_argument("--probe-samples", type=int, default=20)
+    p.add_argument("--require-idle", action="store_true",
+                   help="exit with an error instead of flagging the line when the GPU is "
+                        "busy (memory in use or utilisation) before the first launch")
     p.add_argument("--profile", action="store_true",
                    help="lean run for profilers: no probes, validation, e2e or CPU baseline")
     p.add_argument("--json-out", default=None, help="also write the JSON line to this file")
@@ -115,6 +143,95 @@ def read_profiled_traffic(kernel_tag: str, workload: str, source_hash: str):
     if not h or not t or h.group(1) != source_hash:
         return None
     return int(t.group(1))
+
+
+# ------------------------------------------------------- run environment
+
+def smi_index(local: int) -> str:
+    """nvidia-smi's index of this process's GPU `local`: the entry of
+    CUDA_VISIBLE_DEVICES when that lists indices, else `local` itself."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    if local < len(vis) and vis[local].strip().isdigit():
+        return vis[local].strip()
+    return str(local)
+
+
+def smi_query(fields: str, index: str) -> list[str] | None:
+    """One read-only nvidia-smi query of this GPU; None if it cannot run."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+                              "-i", index], capture_output=True, text=True, timeout=20)
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    if out.returncode != 0 or not out.stdout.strip():
+        return None
+    return [f.strip() for f in out.stdout.strip().splitlines()[0].split(",")]
+
+
+# A GPU counts as busy when another process holds more memory than a
+# driver's idle reservation, or the GPU is computing, before our first launch.
+IDLE_MAX_MIB = 1024
+IDLE_MAX_UTIL = 5
+
+
+def judge_idle(samples: list[tuple[float, float]]) -> dict:
+    """Idle verdict over (memory used MiB, utilisation %) samples."""
+    if not samples:
+        return {"checked": False, "busy": None}
+    mem = max(s[0] for s in samples)
+    util = max(s[1] for s in samples)
+    return {"checked": True, "busy": mem > IDLE_MAX_MIB or util > IDLE_MAX_UTIL,
+            "memory_used_mib_max": mem, "utilization_pct_max": util, "samples": len(samples),
+            "limits": {"memory_used_mib": IDLE_MAX_MIB, "utilization_pct": IDLE_MAX_UTIL}}
+
+
+def idle_gate(local: int) -> dict:
+    """Reads memory used and utilisation of this GPU three times, 0.2 s
+    apart, before this process creates its CUDA context ("What a tuned
+    RMSNorm kernel actually costs on Hopper", section 02: the sweep starts
+    only on an idle GPU). Read-only: nothing is changed on the device."""
+    samples = []
+    for k in range(3):
+        rec = smi_query("memory.used,utilization.gpu", smi_index(local))
+        if rec is not None:
+            try:
+                samples.append((float(rec[0]), float(rec[1])))
+            except (ValueError, IndexError):
+                pass
+        if k < 2:
+            time.sleep(0.2)
+    return judge_idle(samples)
+
+
+def env_record(torch, local: int, l2: int) -> dict:
+    """What the numbers were measured on: GPU, driver, toolkit, PyTorch,
+    host and the library's sources."""
+    from memory_bound_normalization_gb300 import build as libbuild
+
+    props = torch.cuda.get_device_properties(local)
+    drv = smi_query("driver_version", smi_index(local))
+    nvcc = None
+    try:
+        out = subprocess.run([libbuild._nvcc(), "--version"], capture_output=True, text=True,
+                             timeout=20)
+        m = re.search(r"release ([0-9.]+), V([0-9.]+)", out.stdout)
+        nvcc = m.group(2) if m else None
+    except (OSError, RuntimeError, subprocess.TimeoutExpired):
+        pass
+    git = None
+    try:
+        out = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True,
+                             text=True, timeout=10)
+        git = out.stdout.strip() or None if out.returncode == 0 else None
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    return {"gpu": props.name, "sm_count": props.multi_processor_count,
+            "compute_capability": f"{props.major}.{props.minor}", "l2_bytes": l2,
+            "hbm_bytes": int(props.total_memory), "driver": drv[0] if drv else None,
+            "nvcc": nvcc, "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
+            "python": platform.python_version(), "host_arch": platform.machine(),
+            "host_cores": os.cpu_count(), "git_head": git,
+            "library_source_hash": libbuild.source_hash()}
 
 
 # ------------------------------------------------------------ multi-rank
@@ -156,7 +273,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.gpu_index)],
+                 "-lms", "100", "-i", smi_index(self.gpu_index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -216,8 +333,57 @@ def event_ms(a, b) -> float:
     return a.elapsed_time(b)
 
 
+def make_flush(torch, l2: int, device):
+    """The clean-cold-L2 step run before every timed call: write a 2x L2
+    buffer, then read another 2x L2 buffer, so the written dirty lines are
+    written back here (outside the events) and the timed call starts from a
+    clean, cold L2."""
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+    flush_sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_sink)
+
+    return flush
+
+
+def run_cold_copy(pkg, torch, nbytes: int, l2: int, samples: int = 20):
+    """The copy probe under the cells' protocol: the clean-cold-L2 flush
+    before each sample, CUDA events around the copy alone. Copying nbytes
+    moves what a forward over an nbytes activation moves (read x, write y),
+    and the copy's dirty output lines left in L2 at its end escape its
+    events exactly as the cells' outputs do, so this is the like-for-like
+    denominator of the cold-cell fractions."""
+    dev = torch.cuda.current_device()
+    a = torch.ones(nbytes // 4, dtype=torch.float32, device=dev)
+    c = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flush = make_flush(torch, l2, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        flush()
+        pkg.check(pkg.rmsnorm_probe(pkg.PROBE_COPY, c, a, None, nbytes, 4, stream), "probe")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(samples)]
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        pkg.check(pkg.rmsnorm_probe(pkg.PROBE_COPY, c, a, None, nbytes, 4, stream), "probe")
+        e1.record(stream)
+    torch.cuda.synchronize()
+    gbs = [2 * nbytes / (event_ms(e0, e1) * 1e-3) / 1e9 for e0, e1 in ev]
+    del a, c
+    torch.cuda.empty_cache()
+    return {"bytes": nbytes, "moved_bytes": 2 * nbytes, "samples": samples,
+            "median_gbs": round(statistics.median(gbs), 1), "best_gbs": round(max(gbs), 1),
+            "protocol": "clean cold L2 before each sample, events around the copy only"}
+
+
 def run_probes(pkg, torch, nbytes: int, samples: int = 10):
-    """Best-of GB/s for copy, pure write and 2R1W over nbytes-sized buffers."""
+    """Best-of GB/s for copy, pure write and 2R1W over nbytes-sized buffers,
+    timed back to back (steady state: each sample pays the write-back of the
+    one before)."""
     dev = torch.cuda.current_device()
     a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -243,6 +409,8 @@ def run_probes(pkg, torch, nbytes: int, samples: int = 10):
     del a, b, c
     torch.cuda.empty_cache()
     res["best"] = max(res.values())
+    res["bytes"] = nbytes
+    res["samples"] = samples
     return res
 
 
@@ -382,7 +550,7 @@ def pick_workload(synth, args):
 # ------------------------------------------------------------------ our arm
 
 def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_first=True,
-              sample_clocks=False, dist=None):
+              sample_clocks=False, dist=None, steady_steps=0):
     """Validates (unless check_first is False) and times `steps` forward +
     backward calls of one workload: inputs rotated over clone sets covering
     >= 3x L2, a clean cold L2 before every call, CUDA events on the calling
@@ -408,16 +576,8 @@ def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_f
                      "h": torch.empty_like(base["x"]) if residual else None,
                      "rstd": torch.empty(M, dtype=torch.float32, device=base["x"].device),
                      "dw": torch.empty(N, dtype=torch.float32, device=base["x"].device)})
-    # L2 flush between timed calls: write a 2x L2 buffer, then read another
-    # 2x L2 buffer so the dirty lines of the write are written back here,
-    # outside the events, and the timed call starts from a clean, cold L2
-    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=base["x"].device)
-    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=base["x"].device)
-    flush_sink = torch.empty((), dtype=torch.float32, device=base["x"].device)
-
-    def flush():
-        flush_w.zero_()
-        torch.sum(flush_r, dim=0, out=flush_sink)
+    # L2 flush between timed calls (outside the events)
+    flush = make_flush(torch, l2, base["x"].device)
 
     stream = torch.cuda.current_stream()
 
@@ -518,9 +678,47 @@ def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_f
     bwd_mean = sum(bwd_ms) / K
     step_ms = fwd_mean + bwd_mean
     region_ms = event_ms(region0, region1)
+    steady = None
+    if steady_steps > 0:
+        steady = time_steady(torch, fwd, bwd, nsets, steady_steps, stream)
+        if not torch.equal(outs[0]["dw"], dw0):
+            raise SystemExit("dw changed between the cold and the steady-state calls")
     return {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_mean": fwd_mean, "bwd_mean": bwd_mean,
             "step_ms": step_ms, "region_ms": region_ms, "nsets": nsets, "set_bytes": set_bytes,
-            "errs": errs, "base": base, "clock_info": clock_info, "dw0": outs[0]["dw"]}
+            "errs": errs, "base": base, "clock_info": clock_info, "dw0": outs[0]["dw"],
+            "steady": steady}
+
+
+def time_steady(torch, fwd, bwd, nsets: int, steps: int, stream):
+    """Steady state, as inside a training step: forward and backward calls
+    back to back over the rotating clone sets (>= 3x L2 of inputs, so no
+    call finds its inputs in L2), with no flush, so every call also pays for
+    writing back the outputs the call before left dirty in L2. One event pair
+    brackets all `steps` steps; a second pass records events between the
+    calls for the forward / backward split."""
+    for k in range(2 * nsets):
+        fwd(k % nsets)
+        bwd(k % nsets)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        fwd(k % nsets)
+        bwd(k % nsets)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    step_ms = event_ms(e0, e1) / steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
+    ev[0].record(stream)
+    for k in range(steps):
+        fwd(k % nsets)
+        ev[2 * k + 1].record(stream)
+        bwd(k % nsets)
+        ev[2 * k + 2].record(stream)
+    torch.cuda.synchronize()
+    f = [event_ms(ev[2 * k], ev[2 * k + 1]) for k in range(steps)]
+    b = [event_ms(ev[2 * k + 1], ev[2 * k + 2]) for k in range(steps)]
+    return {"steps": steps, "step_ms": step_ms, "fwd_ms": sum(f) / steps, "bwd_ms": sum(b) / steps}
 
 
 def run_ours(args):
@@ -531,6 +729,10 @@ def run_ours(args):
     from memory_bound_normalization_gb300 import synth
 
     rank, world, local = dist_env()
+    # before this process touches the GPU: is anyone else using it?
+    idle = idle_gate(local)
+    if idle.get("busy") and args.require_idle:
+        raise SystemExit(f"GPU {smi_index(local)} is busy before the first launch: {json.dumps(idle)}")
     torch.cuda.set_device(local)
     dist = None
     if world > 1:
@@ -555,10 +757,13 @@ def run_ours(args):
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
 
     peak, peak_src = read_peaks()
-    probes_open = None if args.profile else run_probes(pkg, torch, 1 << 30)
+    probe_bytes = int(args.probe_gib * (1 << 30)) // 16 * 16
+    probes_open = None if args.profile else run_probes(pkg, torch, probe_bytes,
+                                                       args.probe_samples)
 
     cell = time_cell(pkg, torch, synth, wl, args.op, code, args.steps, args.warmup, local, l2,
-                     check_first=not args.profile, sample_clocks=True, dist=dist)
+                     check_first=not args.profile, sample_clocks=True, dist=dist,
+                     steady_steps=0 if args.profile else args.steady_steps)
     fwd_ms, bwd_ms = cell["fwd_ms"], cell["bwd_ms"]
     fwd_mean, bwd_mean, step_ms = cell["fwd_mean"], cell["bwd_mean"], cell["step_ms"]
     region_ms, nsets, set_bytes = cell["region_ms"], cell["nsets"], cell["set_bytes"]
@@ -574,8 +779,6 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         return line if rank == 0 else None
-    probes_close = run_probes(pkg, torch, 1 << 30)
-
     # end to end through pinned host buffers
     e2e = run_e2e(pkg, torch, wl, base, code, stream, args.e2e_steps, fwd_bytes + bwd_bytes,
                   args.op, ref_dw=cell["dw0"])
@@ -591,6 +794,29 @@ def run_ours(args):
     value = replica_throughput(world, fwd_bytes + bwd_bytes, step_ms)
     bwd_gbs = bwd_bytes / (bwd_mean * 1e-3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_mean * 1e-3) / 1e9
+    # the copy probe under the cells' own protocol, sized to move what the
+    # forward and the backward call move
+    cold = {"fwd_sized": run_cold_copy(pkg, torch, fwd_bytes // 32 * 16, l2),
+            "bwd_sized": run_cold_copy(pkg, torch, bwd_bytes // 32 * 16, l2)}
+    steady = None
+    if cell["steady"] is not None:
+        sd = cell["steady"]
+        sd_ms = slowest_rank(dist, [sd["step_ms"]], base["x"].device)[0]
+        sd_gbs = replica_throughput(world, fwd_bytes + bwd_bytes, sd_ms)
+        sf = fwd_bytes / (sd["fwd_ms"] * 1e-3) / 1e9
+        sb = bwd_bytes / (sd["bwd_ms"] * 1e-3) / 1e9
+        steady = {
+            "steps": sd["steps"], "ms_per_step": round(sd_ms, 5), "gbs": round(sd_gbs, 1),
+            "frac": round(sd_gbs / world / peak, 4),
+            "frac_of_probe": round(sd_gbs / world / probes_open["best"], 4),
+            "fwd_gbs": round(sf, 1), "fwd_frac": round(sf / peak, 4),
+            "bwd_gbs": round(sb, 1), "bwd_frac": round(sb / peak, 4),
+            "protocol": "forward + backward calls back to back over the rotating clone sets, "
+                        "no flush: each call pays the write-back of the outputs the call "
+                        "before left dirty in L2; one event pair around all steps (the "
+                        "fwd/bwd split from a second pass with events between the calls); "
+                        "frac of MEASURED_PEAKS, frac_of_probe of the in-run probes, which "
+                        "run back to back as well"}
     traffic = read_profiled_traffic("rmsnorm_add_bwd" if residual else "rmsnorm_bwd", wl.name,
                                     libbuild.kernel_source_hash())
     line = {
@@ -621,12 +847,18 @@ def run_ours(args):
         "fwd": {"ms": round(fwd_mean, 5), "median_ms": round(statistics.median(fwd_ms), 5),
                 "gbs": round(fwd_gbs, 1),
                 "frac_of_peak": round(fwd_gbs / peak, 4),
-                "frac_of_probe": round(fwd_gbs / probes_open["best"], 4), "plan": plan_f},
+                "frac_of_probe": round(fwd_gbs / probes_open["best"], 4),
+                "frac_of_cold_copy": round(fwd_gbs / cold["fwd_sized"]["median_gbs"], 4),
+                "plan": plan_f},
         "bwd": {"ms": round(bwd_mean, 5), "median_ms": round(statistics.median(bwd_ms), 5),
                 "gbs": round(bwd_gbs, 1),
                 "frac_of_peak": round(bwd_gbs / peak, 4),
-                "frac_of_probe": round(bwd_gbs / probes_open["best"], 4), "plan": plan_b,
+                "frac_of_probe": round(bwd_gbs / probes_open["best"], 4),
+                "frac_of_cold_copy": round(bwd_gbs / cold["bwd_sized"]["median_gbs"], 4),
+                "plan": plan_b,
                 "workspace_bytes_overhead": 2 * plan_b["workspace_bytes"]},
+        "steady": steady,
+        "cold_copy": cold,
         "frac_of_peak": round(value / world / peak, 4),
         "roofline": {
             "bound": "hbm",
@@ -641,8 +873,6 @@ def run_ours(args):
             "frac": round(bwd_gbs / peak, 4),
             "traffic": traffic,
         },
-        "probes": {"open": probes_open, "close": probes_close,
-                   "close_over_open": round(probes_close["best"] / probes_open["best"], 4)},
         "timed_region_ms": round(region_ms, 3),
         "clocks": clock_info,
         "e2e": e2e,
@@ -654,9 +884,24 @@ def run_ours(args):
         "library": {"path": pkg.library_path(), "source_hash": libbuild.source_hash(),
                     "bwd_kernel_hash": libbuild.kernel_source_hash(),
                     "version": pkg.rmsnorm_version()},
+        "idle_gate": idle,
+        "env": env_record(torch, local, l2),
     }
     if world == 1 and args.op == "norm" and not args.no_sweep:
         line["sweep"] = run_sweep(pkg, torch, synth, args, local, l2, peak)
+    if world == 1 and args.op == "norm" and not args.no_configs:
+        line["configs"] = run_configs(pkg, torch, synth, args, local, l2, peak,
+                                      skip=wl.name)
+    # the closing probe comes after every timed cell, so a drift across the
+    # whole run shows ("What a tuned RMSNorm kernel actually costs on Hopper",
+    # sections 02 and 08: opening and closing probes)
+    probes_close = run_probes(pkg, torch, probe_bytes, args.probe_samples)
+    ratio = probes_close["best"] / probes_open["best"]
+    line["probes"] = {"open": probes_open, "close": probes_close,
+                      "close_over_open": round(ratio, 4), "drift_flag": ratio < DRIFT_LIMIT,
+                      "drift_limit": DRIFT_LIMIT,
+                      "note": "closing probe taken after the main cell, the sweep and the "
+                              "other workloads"}
     if rank == 0 and not args.no_cpu_baseline and args.op == "norm":
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     if dist is not None:
@@ -683,6 +928,38 @@ def run_sweep(pkg, torch, synth, args, local, l2, peak):
                           "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1)})
             del c
     return {"steps": args.sweep_steps, "peak_gbs": peak, "cells": cells}
+
+
+CONFIG_WORKLOADS = ("small_256x1024", "hidden8192_32768x8192_outliers", "qknorm_1048576x128")
+
+
+def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None):
+    """The other named workloads (256 x 1024, which fits in L2 and is bound
+    by latency; 32768 x 8192 with 0.1% outliers; QK-norm 1048576 x 128),
+    each validated against PyTorch and timed like the main workload: clone
+    sets >= 3x L2, a clean cold L2 before every call, events per call."""
+    cells = []
+    for name in CONFIG_WORKLOADS:
+        if name == skip:
+            continue
+        wl = synth.WORKLOADS[name]
+        code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
+        elem = torch.empty(0, dtype=wl.dtype).element_size()
+        fb, bb = synth.logical_bytes(wl.M, wl.N, elem)
+        c = time_cell(pkg, torch, synth, wl, "norm", code, args.config_steps, 5, local, l2)
+        fg = fb / (c["fwd_mean"] * 1e-3) / 1e9
+        bg = bb / (c["bwd_mean"] * 1e-3) / 1e9
+        plan_b = pkg.rmsnorm_plan(wl.M, wl.N, code, pkg.PASS_BWD, local).as_dict()
+        cells.append({"workload": wl.name, "dtype": wl.dtype_name, "M": wl.M, "N": wl.N,
+                      "fwd_us": round(c["fwd_mean"] * 1e3, 2),
+                      "bwd_us": round(c["bwd_mean"] * 1e3, 2),
+                      "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
+                      "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
+                      "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1),
+                      "bwd_variant": plan_b["variant_name"],
+                      "validation": c["errs"]})
+        del c
+    return {"steps": args.config_steps, "peak_gbs": peak, "cells": cells}
 
 
 def run_small_m(pkg, torch, steps: int = 200):

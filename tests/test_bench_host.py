@@ -1,0 +1,34 @@
+"""bench.py's host-side rules without a GPU: the idle-GPU verdict, the index
+nvidia-smi is asked about, and the drift flag's threshold."""
+from __future__ import annotations
+
+import bench
+
+
+def test_idle_verdict():
+    assert bench.judge_idle([]) == {"checked": False, "busy": None}
+    idle = bench.judge_idle([(0.0, 0.0), (3.0, 0.0), (0.0, 1.0)])
+    assert idle["checked"] and idle["busy"] is False
+    assert idle["memory_used_mib_max"] == 3.0 and idle["utilization_pct_max"] == 1.0
+    # another process's memory, or work on the GPU, in any sample makes it busy
+    assert bench.judge_idle([(0.0, 0.0), (bench.IDLE_MAX_MIB + 1.0, 0.0)])["busy"] is True
+    assert bench.judge_idle([(0.0, bench.IDLE_MAX_UTIL + 1.0)])["busy"] is True
+    assert bench.judge_idle([(bench.IDLE_MAX_MIB, bench.IDLE_MAX_UTIL)])["busy"] is False
+
+
+def test_smi_index_follows_visible_devices(monkeypatch):
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    assert bench.smi_index(0) == "0" and bench.smi_index(3) == "3"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "5,2")
+    assert bench.smi_index(0) == "5" and bench.smi_index(1) == "2"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-1234abcd")
+    assert bench.smi_index(0) == "0"
+
+
+def test_drift_limit_and_new_options():
+    assert bench.DRIFT_LIMIT == 0.98
+    a = bench.parse_args([])
+    assert a.probe_gib >= 4 and a.probe_samples >= 20
+    assert a.steady_steps > 0 and not a.no_configs and not a.require_idle
+    assert set(bench.CONFIG_WORKLOADS) == {"small_256x1024", "hidden8192_32768x8192_outliers",
+                                           "qknorm_1048576x128"}
