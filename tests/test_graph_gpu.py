@@ -1,13 +1,18 @@
 """Forward and backward captured into a CUDA graph replay bit for bit like the
-eager calls. Small-M shapes are launch-bound (a 256 x 1024 step moves 2.6 MB),
-so a caller replays the pair as one graph; the backward's workspace comes
-from the stream-ordered allocator, which capture turns into graph memory
-nodes. Every kernel family is covered: short rows, one block per row, row
-groups, clusters (fp32 wide rows), two-pass forward, scalar (ragged N)."""
+eager calls, and the replayed outputs match the fp64 oracle within the
+parity tolerances. Small-M shapes are launch-bound (a 256 x 1024 step moves
+2.6 MB), so a caller replays the pair as one graph; the backward's workspace
+comes from the stream-ordered allocator, which capture turns into graph
+memory nodes. Every kernel family is covered: short rows, one block per row,
+row groups, clusters (fp32 wide rows), two-pass forward, scalar (ragged N)."""
 from __future__ import annotations
 
+import numpy as np
 import pytest
 import torch
+
+import oracle
+from parity_util import check_dw, check_rows, check_rstd
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +28,19 @@ def _lib():
         pytest.skip("needs a CUDA device")
     torch.cuda.set_device(0)
     pkg.load_library(build_if_missing=True)
+    oracle.build()
     yield
+
+
+def check_against_oracle(x, w, dy, eps, y, rstd, dx, dw):
+    """Replayed outputs against the fp64 oracle (the definition), element by
+    element."""
+    xc, wc, dyc = x.cpu(), w.cpu(), dy.cpu()
+    y_ref, r_ref = oracle.fwd(xc, wc, eps)
+    check_rows(y, y_ref, x.dtype, "replayed y")
+    check_rstd(rstd, r_ref, "replayed rstd")
+    check_rows(dx, oracle.bwd_dx(xc, wc, dyc, eps), x.dtype, "replayed dx")
+    check_dw(dw, oracle.bwd_dw(xc, dyc, eps), "replayed dw")
 
 
 F32 = torch.float32
@@ -72,6 +89,7 @@ def test_graph_replay_matches_eager(M, N, dtype, w_dtype):
         for got, want in zip((y, rstd, dx, dw), ref):
             assert torch.equal(got, want)
     assert pkg.rmsnorm_get_last_device_error() == pkg.OK
+    check_against_oracle(x, w, dy, wl.eps, y, rstd, dx, dw)
 
 
 RES_CASES = [(1, 4096, torch.bfloat16), (256, 1024, torch.bfloat16), (300, 128, torch.float16),
@@ -118,6 +136,15 @@ def test_graph_replay_residual_in_place(M, N, dtype):
         for got, want in zip((res, y, rstd, dres, dw), ref):
             assert torch.equal(got, want)
     assert pkg.rmsnorm_get_last_device_error() == pkg.OK
+    # the replayed outputs against the oracle: the stored sum bit for bit,
+    # the rest within the parity tolerances
+    h_ref, y_ref, r_ref = oracle.add_fwd(x.cpu(), res0.cpu(), w.cpu(), wl.eps)
+    assert np.array_equal(res.float().cpu().numpy().astype(np.float64), h_ref), "replayed h"
+    check_rows(y, y_ref, dtype, "replayed y")
+    check_rstd(rstd, r_ref, "replayed rstd")
+    hc, wc, dyc = res.cpu(), w.cpu(), dy.cpu()
+    check_rows(dres, oracle.add_bwd_dx(hc, wc, dyc, dres0.cpu(), wl.eps), dtype, "replayed dx")
+    check_dw(dw, oracle.bwd_dw(hc, dyc, wl.eps), "replayed dw")
 
 
 @pytest.mark.parametrize("M,N,dtype", [(48, 45056, torch.bfloat16), (8, 28672, F32),
@@ -147,3 +174,4 @@ def test_first_call_inside_capture(M, N, dtype):
     assert torch.equal(y, y2) and torch.equal(rstd, r2)
     assert torch.equal(dx, dx2) and torch.equal(dw, dw2)
     assert pkg.rmsnorm_get_last_device_error() == pkg.OK
+    check_against_oracle(x, w, dy, wl.eps, y, rstd, dx, dw)
