@@ -43,6 +43,11 @@
  *   - Results are deterministic: the same inputs, shapes, dtype, device
  *     model and pointer-alignment class give bitwise-identical outputs,
  *     dw included (fixed reduction trees, no floating-point atomics).
+ *   - The library looks up per-device state once (properties, the device
+ *     status word, rmsnorm_bwd_noalloc's scratch address) and keeps it for
+ *     the life of the process, in the device's primary context. Calls are
+ *     not supported after cudaDeviceReset or from a non-primary context on
+ *     a device the library has already used.
  */
 #ifndef RMSNORM_H_
 #define RMSNORM_H_
@@ -71,7 +76,10 @@ typedef enum {
     RMSNORM_ERR_MISALIGNED = 3,
     RMSNORM_ERR_CUDA = 4,
     RMSNORM_ERR_NOMEM = 5,
-    RMSNORM_ERR_DEVICE_TIMEOUT = 6
+    RMSNORM_ERR_DEVICE_TIMEOUT = 6,
+    RMSNORM_ERR_OUT_OF_BOUNDS = 7 /* checked debug build only: a kernel access
+                                     fell outside its tensor or ring and was
+                                     skipped */
 } rmsnorm_status_t;
 
 /*
@@ -161,6 +169,12 @@ int rmsnorm_add_bwd(const void *h, const void *w, const void *dy,
 #define RMSNORM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /*
+ * RMSNORM_NOALLOC_SCRATCH_BYTES as the loaded library was built with it, for
+ * bindings that cannot read this header's macros. Host only; no CUDA call.
+ */
+size_t rmsnorm_noalloc_scratch_bytes(void);
+
+/*
  * rmsnorm_bwd for callers that cannot allocate device memory: code running
  * where cudaMalloc and the stream-ordered allocator are off limits, such as
  * under a custom allocator that owns all device memory, in a real-time loop
@@ -213,9 +227,12 @@ int rmsnorm_bwd_naive(const void *x, const void *w, const void *dy,
  * Device-side status. Every wait inside the kernels (on a bulk copy landing
  * in shared memory) is bounded in time; a wait that runs out records
  * RMSNORM_ERR_DEVICE_TIMEOUT in a status word on the device and the kernel
- * returns early instead of hanging. This call synchronises `stream`, returns
- * the status recorded on the current device since the last call (RMSNORM_OK
- * if none), and clears it. RMSNORM_ERR_CUDA if the synchronisation fails.
+ * returns early instead of hanging. In the checked debug build (compiled
+ * with RMSNORM_CHECKS) a kernel access outside its tensor, workspace or
+ * shared-memory ring is skipped and recorded as RMSNORM_ERR_OUT_OF_BOUNDS.
+ * This call synchronises `stream`, returns the first status recorded on the
+ * current device since the last call (RMSNORM_OK if none), and clears it.
+ * RMSNORM_ERR_CUDA if the synchronisation fails.
  */
 int rmsnorm_get_last_device_error(cudaStream_t stream);
 
@@ -310,7 +327,8 @@ typedef struct {
 int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device,
                  rmsnorm_plan_t *out);
 
-/* Library version as "major.minor.patch" (static storage). */
+/* Library version as "major.minor.patch" (static storage), followed by
+   "+checks" in the checked debug build. */
 const char *rmsnorm_version(void);
 
 #ifdef __cplusplus

@@ -18,6 +18,7 @@ from ._lib import (  # noqa: F401
     ERR_INVALID_ARG,
     ERR_MISALIGNED,
     ERR_NOMEM,
+    ERR_OUT_OF_BOUNDS,
     ERR_UNSUPPORTED,
     EXPORTS,
     F16,
@@ -35,9 +36,9 @@ from ._lib import (  # noqa: F401
     Plan,
     RMSNormError,
     check,
+    checked_variant,
     library_path,
     load_library,
-    NOALLOC_SCRATCH_BYTES,
     rmsnorm_add_bwd,
     rmsnorm_add_fwd,
     rmsnorm_bwd,
@@ -47,6 +48,7 @@ from ._lib import (  # noqa: F401
     rmsnorm_bwd_ws,
     rmsnorm_fwd,
     rmsnorm_get_last_device_error,
+    rmsnorm_noalloc_scratch_bytes,
     rmsnorm_plan,
     rmsnorm_probe,
     rmsnorm_set_wait_limit_ns,
@@ -55,7 +57,7 @@ from ._lib import (  # noqa: F401
     rmsnorm_version,
 )
 
-__version__ = "0.1.0"
+__version__ = "0.2.0"
 
 
 def dtype_code(torch_dtype, w_dtype=None) -> int:

@@ -8,6 +8,11 @@ None (the current torch stream of the current device).
 
 There is no fallback: if the library is missing or fails to load, importing
 the first function raises.
+
+With RMSNORM_LIBRARY_VARIANT=checked in the environment the binding loads the
+checked debug build of the same sources instead (every kernel access tested
+against its extent; see build.py), for tests that look for out-of-range
+accesses.
 """
 from __future__ import annotations
 
@@ -30,6 +35,7 @@ ERR_MISALIGNED = 3
 ERR_CUDA = 4
 ERR_NOMEM = 5
 ERR_DEVICE_TIMEOUT = 6
+ERR_OUT_OF_BOUNDS = 7  # reported by the checked debug build only
 
 PASS_FWD = 0
 PASS_BWD = 1
@@ -52,6 +58,7 @@ EXPORTS = (
     "rmsnorm_bwd_ws",
     "rmsnorm_add_fwd",
     "rmsnorm_add_bwd",
+    "rmsnorm_noalloc_scratch_bytes",
     "rmsnorm_bwd_noalloc",
     "rmsnorm_bwd_naive",
     "rmsnorm_get_last_device_error",
@@ -97,8 +104,13 @@ _lock = threading.Lock()
 _lib: ctypes.CDLL | None = None
 
 
+def checked_variant() -> bool:
+    """True when this process is to load the checked debug build."""
+    return os.environ.get("RMSNORM_LIBRARY_VARIANT", "") == "checked"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.lib_path(checked_variant())
 
 
 def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
@@ -108,9 +120,10 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
-        if build_if_missing and (not os.path.exists(path) or _build.is_stale()):
-            _build.build()
+        checked = checked_variant()
+        path = _build.lib_path(checked)
+        if build_if_missing and (not os.path.exists(path) or _build.is_stale(checked)):
+            _build.build(checked=checked)
         if not os.path.exists(path):
             raise OSError(
                 f"{path} is missing: build the CUDA library first "
@@ -126,6 +139,8 @@ def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.rmsnorm_add_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f, i, vp]
         lib.rmsnorm_add_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i, vp]
         lib.rmsnorm_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i, vp]
+        lib.rmsnorm_noalloc_scratch_bytes.argtypes = []
+        lib.rmsnorm_noalloc_scratch_bytes.restype = sz
         lib.rmsnorm_bwd_naive.argtypes = [vp, vp, vp, vp, vp, i64, i64, f, i, vp]
         lib.rmsnorm_get_last_device_error.argtypes = [vp]
         lib.rmsnorm_status_string.argtypes = [i]
@@ -213,7 +228,10 @@ def rmsnorm_bwd_noalloc(x, w, dy, rstd, dx, dw, M: int, N: int, dtype: int, stre
                                               _ptr(dw), M, N, dtype, _stream(stream))
 
 
-NOALLOC_SCRATCH_BYTES = 16 << 20
+def rmsnorm_noalloc_scratch_bytes() -> int:
+    """Size of rmsnorm_bwd_noalloc's fixed scratch array, as the library was
+    built with it."""
+    return int(load_library().rmsnorm_noalloc_scratch_bytes())
 
 
 def rmsnorm_bwd_naive(x, w, dy, dx, dw, M: int, N: int, eps: float, dtype: int,

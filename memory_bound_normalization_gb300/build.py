@@ -4,6 +4,13 @@ Each translation unit is compiled by its own nvcc process (in parallel), then
 linked into ``_build/librmsnorm.so`` against the shared CUDA runtime, so the
 library and PyTorch share one runtime state. A rebuild happens only when a
 source or header is newer than the library.
+
+A second, checked variant of the same sources (``-DRMSNORM_CHECKS``, in
+``_build_checked/``) tests every global store, bulk copy and shared-memory
+ring access of the kernels against the extent it belongs to and reports a
+failed check as RMSNORM_ERR_OUT_OF_BOUNDS instead of making the access. It is
+a debug build for the tests; the binding loads it only when
+RMSNORM_LIBRARY_VARIANT=checked is set.
 """
 from __future__ import annotations
 
@@ -19,8 +26,10 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
+CHECKED_BUILD_DIR = os.path.join(PKG_DIR, "_build_checked")
 LIB_NAME = "librmsnorm.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+CHECKED_LIB_PATH = os.path.join(CHECKED_BUILD_DIR, LIB_NAME)
 
 SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_f32.cu", "bwd_bf16.cu", "bwd_f16.cu",
            "bwd_res_f32.cu", "bwd_res_bf16.cu", "bwd_res_f16.cu", "naive.cu", "probe.cu",
@@ -73,10 +82,15 @@ def kernel_source_hash(names=BWD_KERNEL_FILES) -> str:
     return h.hexdigest()[:16]
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def lib_path(checked: bool = False) -> str:
+    return CHECKED_LIB_PATH if checked else LIB_PATH
+
+
+def is_stale(checked: bool = False) -> bool:
+    path = lib_path(checked)
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
@@ -90,32 +104,55 @@ def _run(cmd: list[str], log: str | None) -> None:
         raise RuntimeError(f"command failed ({res.returncode}): {' '.join(cmd)}\n{out}")
 
 
-def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None) -> str:
-    """Compile and link the library if needed; returns its path."""
-    if not force and not is_stale():
-        return LIB_PATH
+def _variant_jobs(checked: bool, extra: list[str]):
+    """(compile commands, objects, link step) of one variant."""
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
-    objs = []
-    cmds = []
+    out_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    os.makedirs(out_dir, exist_ok=True)
+    defs = ["-DRMSNORM_CHECKS"] if checked else []
+    objs, cmds = [], []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(obj)
-        log = os.path.join(BUILD_DIR, src.replace(".cu", ".log"))
-        cmds.append(([nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj], log))
+        log = os.path.join(out_dir, src.replace(".cu", ".log"))
+        cmds.append(([nvcc, *ARCH, *FLAGS, *defs, *extra, "-c", os.path.join(CSRC, src), "-o",
+                      obj], log))
+    return cmds, objs, out_dir
+
+
+def _link(objs: list[str], checked: bool) -> None:
+    path = lib_path(checked)
+    tmp = path + f".tmp{os.getpid()}"
+    _run([_nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], None)
+    os.replace(tmp, path)
+    with open(os.path.join(os.path.dirname(path), "BUILD_INFO"), "w") as fh:
+        fh.write(f"source_hash={source_hash()}\nnvcc={_nvcc()}\narch=sm_103a\n"
+                 f"checked={int(checked)}\n")
+
+
+def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None,
+          checked: bool = False, both: bool = False) -> str:
+    """Compile and link the library if needed; returns its path. `checked`
+    builds the checked debug variant instead; `both` builds the library and
+    the checked variant together (one pool of compile jobs) and returns the
+    library's path."""
+    variants = [False, True] if both else [checked]
+    todo = [v for v in variants if force or is_stale(v)]
+    if not todo:
+        return lib_path(checked and not both)
+    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    plans = {v: _variant_jobs(v, extra) for v in todo}
+    cmds = [c for v in todo for c in plans[v][0]]
     workers = jobs or min(len(cmds), max(1, os.cpu_count() or 1))
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         for fut in [ex.submit(_run, c, log) for c, log in cmds]:
             fut.result()
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], None)
-    os.replace(tmp, LIB_PATH)
-    with open(os.path.join(BUILD_DIR, "BUILD_INFO"), "w") as fh:
-        fh.write(f"source_hash={source_hash()}\nnvcc={nvcc}\narch=sm_103a\n")
-    return LIB_PATH
+    for v in todo:
+        _link(plans[v][1], v)
+    return lib_path(checked and not both)
 
 
 if __name__ == "__main__":
-    path = build(force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv)
+    path = build(force="--force" in sys.argv, ptxas_verbose="-v" in sys.argv,
+                 checked="--checked" in sys.argv, both="--both" in sys.argv)
     print(path)

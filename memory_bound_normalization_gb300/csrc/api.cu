@@ -297,6 +297,7 @@ const char* rmsnorm_status_string(int status) {
         case RMSNORM_ERR_CUDA: return "RMSNORM_ERR_CUDA";
         case RMSNORM_ERR_NOMEM: return "RMSNORM_ERR_NOMEM";
         case RMSNORM_ERR_DEVICE_TIMEOUT: return "RMSNORM_ERR_DEVICE_TIMEOUT";
+        case RMSNORM_ERR_OUT_OF_BOUNDS: return "RMSNORM_ERR_OUT_OF_BOUNDS";
         default: return "RMSNORM_STATUS_UNKNOWN";
     }
 }
@@ -348,6 +349,10 @@ int rmsnorm_plan(int64_t M, int64_t N, int dtype, int pass, int device, rmsnorm_
     return cuda_status(e);
 }
 
-const char* rmsnorm_version(void) { return "0.1.0"; }
+#ifdef RMSNORM_CHECKS
+const char* rmsnorm_version(void) { return "0.2.0+checks"; }
+#else
+const char* rmsnorm_version(void) { return "0.2.0"; }
+#endif
 
 }  // extern "C"

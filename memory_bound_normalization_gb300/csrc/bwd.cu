@@ -13,6 +13,11 @@
 #include "bwd_kernels.cuh"
 
 namespace rmsn {
+
+static_assert(kStatusTimeout == RMSNORM_ERR_DEVICE_TIMEOUT, "device status codes follow the C ABI");
+static_assert(kStatusOutOfBounds == RMSNORM_ERR_OUT_OF_BOUNDS,
+              "device status codes follow the C ABI");
+
 namespace {
 
 constexpr int kStageBudget = 48 * 1024;   // ring bytes aimed at per short-row block
@@ -69,7 +74,8 @@ const BwdTuning& tuning() {
 // run for a given P and Q.
 template <int Q>
 __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict__ partial,
-                                                        float* __restrict__ dw, int P, int N) {
+                                                        float* __restrict__ dw, int P, int N,
+                                                        int* status) {
     __shared__ float part[Q][33];
     wait_for_prerequisite_grid();  // partial rows complete and visible
     allow_dependent_launch();
@@ -78,7 +84,10 @@ __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict_
     float s = 0.f;
     if (col < N) {
 #pragma unroll 4
-        for (int p = q; p < P; p += Q) s += partial[static_cast<int64_t>(p) * N + col];
+        for (int p = q; p < P; p += Q) {
+            const float* src = partial + static_cast<int64_t>(p) * N + col;
+            if (RMSN_OK(span_in(src, 4, partial, static_cast<int64_t>(P) * N * 4), status)) s += *src;
+        }
     }
     part[q][cx] = s;
     __syncthreads();
@@ -86,7 +95,7 @@ __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict_
         float t = 0.f;
 #pragma unroll
         for (int i = 0; i < Q; ++i) t += part[i][cx];
-        dw[col] = t;
+        if (RMSN_OK(span_in(dw + col, 4, dw, static_cast<int64_t>(N) * 4), status)) dw[col] = t;
     }
 }
 
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict_
 template <int C>
 __global__ void __launch_bounds__(1024) colsum_narrow_kernel(const float* __restrict__ partial,
                                                              float* __restrict__ dw, int P,
-                                                             int N) {
+                                                             int N, int* status) {
     constexpr int R = 1024 / C;
     __shared__ float part[R][C + 1];
     wait_for_prerequisite_grid();  // partial rows complete and visible
@@ -110,7 +119,10 @@ __global__ void __launch_bounds__(1024) colsum_narrow_kernel(const float* __rest
     float s = 0.f;
     if (col < N) {
 #pragma unroll 2
-        for (int p = q; p < P; p += R) s += partial[static_cast<int64_t>(p) * N + col];
+        for (int p = q; p < P; p += R) {
+            const float* src = partial + static_cast<int64_t>(p) * N + col;
+            if (RMSN_OK(span_in(src, 4, partial, static_cast<int64_t>(P) * N * 4), status)) s += *src;
+        }
     }
     part[q][cx] = s;
     __syncthreads();
@@ -119,7 +131,8 @@ __global__ void __launch_bounds__(1024) colsum_narrow_kernel(const float* __rest
         if (q < h) part[q][cx] += part[q + h][cx];
         __syncthreads();
     }
-    if (q == 0 && col < N) dw[col] = part[0][cx];
+    if (q == 0 && col < N && RMSN_OK(span_in(dw + col, 4, dw, static_cast<int64_t>(N) * 4), status))
+        dw[col] = part[0][cx];
 }
 
 // Columns a block of the narrow column sum takes: at least 64 blocks.
@@ -483,7 +496,8 @@ cudaError_t colsum_launch(const float* partial, float* dw, int P, int N, cudaStr
     cudaError_t err = cudaGetDevice(&device);
     if (err != cudaSuccess) return err;
     const DeviceInfo* dev = device_info(device);
-    void* args[4] = {&partial, &dw, &P, &N};
+    int* status = dev ? dev->status_word : nullptr;
+    void* args[5] = {&partial, &dw, &P, &N, &status};
     if (N < kColsumNarrowBelow) {
         const int c = colsum_narrow_cols(N);
         return cudaLaunchKernel(colsum_narrow_for(c), dim3(static_cast<unsigned>(cdiv(N, c))),
@@ -540,7 +554,8 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     const float* part = a.partial;
     float* dw = a.dw;
     int P = p.partial_rows, N = a.N;
-    void* cargs[4] = {&part, &dw, &P, &N};
+    int* status = a.status;
+    void* cargs[5] = {&part, &dw, &P, &N, &status};
     return cudaLaunchKernelExC(&cs, narrow ? colsum_narrow_for(c) : colsum_kernel_for(q), cargs);
 }
 

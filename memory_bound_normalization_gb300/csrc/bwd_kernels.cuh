@@ -151,6 +151,10 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
     const T* DRES = static_cast<const T*>(a.dres);
+    // extents for the checked build: x, dy, dx, dres; the partial rows
+    [[maybe_unused]] const int64_t tbytes =
+        a.M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t pbytes = ncl * static_cast<int64_t>(N) * 4;
     const int bar_id = 1 + g;  // named barrier of this group (0 is __syncthreads)
 
     // rows of this group: vid, vid + nvirt, ...
@@ -180,6 +184,12 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         if (row == a.drop_unit) return;  // failure injection: this wait runs out
         const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
+        if (!RMSN_OK(span_in(X + off, bytes, X, tbytes) && span_in(DY + off, bytes, DY, tbytes) &&
+                         smem_span_in(sx + s * unit, bytes) && smem_span_in(sdy + s * unit, bytes) &&
+                         (!RES || (span_in(DRES + off, bytes, DRES, tbytes) &&
+                                   smem_span_in(sdr + s * unit, bytes))),
+                     a.status))
+            return;  // checked build: the wait for this stage runs out instead
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
         if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
@@ -251,8 +261,8 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
             float2 fx[PR], fd[PR], fw[PR];
-            P::unpack2(ld_shared_16(xs + k * 16), fx);
-            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            P::unpack2(ld_ring_16(xs + k * 16, a.status), fx);
+            P::unpack2(ld_ring_16(ds + k * 16, a.status), fd);
             weights(j, k, fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) dot2 = __ffma2_rn(__fmul2_rn(fd[e], fw[e]), fx[e], dot2);
@@ -280,9 +290,9 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             const int k = j * TG + gt;
             if (k >= vcnt) continue;
             float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
-            if constexpr (RES) P::unpack2(ld_shared_16(sdr + s * unit + k * 16), fr);
-            P::unpack2(ld_shared_16(xs + k * 16), fx);
-            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            if constexpr (RES) P::unpack2(ld_ring_16(sdr + s * unit + k * 16, a.status), fr);
+            P::unpack2(ld_ring_16(xs + k * 16, a.status), fx);
+            P::unpack2(ld_ring_16(ds + k * 16, a.status), fd);
             weights(j, k, fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) {
@@ -294,7 +304,8 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
                     o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
                 acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
             }
-            st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(o));
+            T* dst = dxr + static_cast<int64_t>(vbeg + k) * VEC;
+            if (RMSN_OK(span_in(dst, 16, DX, tbytes), a.status)) st_global_16(dst, P::pack2(o));
         }
     }
     allow_dependent_launch();
@@ -315,7 +326,9 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             if (k >= vcnt) continue;
 #pragma unroll
             for (int q = 0; q < PR / 2; ++q)
-                *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
+                if (float* pd = prow + static_cast<int64_t>(k) * VEC + 4 * q;
+                    RMSN_OK(span_in(pd, 16, a.partial, pbytes), a.status))
+                *reinterpret_cast<float4*>(pd) =
                     make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
                                 acc[j][2 * q + 1].y);
         }
@@ -332,15 +345,19 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             if (k >= vcnt) continue;
 #pragma unroll
             for (int q = 0; q < PR / 2; ++q)
-                *reinterpret_cast<float4*>(comb + g * W + k * VEC + 4 * q) =
+                if (float* cd = comb + g * W + k * VEC + 4 * q;
+                    RMSN_OK(smem_span_in(cd, 16), a.status))
+                *reinterpret_cast<float4*>(cd) =
                     make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
                                 acc[j][2 * q + 1].y);
         }
         __syncthreads();
         for (int col = tid; col < W; col += blockDim.x) {
             float sum = 0.f;
-            for (int gi = 0; gi < groups; ++gi) sum += comb[gi * W + col];
-            prow[col] = sum;
+            for (int gi = 0; gi < groups; ++gi)
+                sum += RMSN_OK(smem_span_in(comb + gi * W + col, 4), a.status) ? comb[gi * W + col]
+                                                                               : 0.f;
+            if (RMSN_OK(span_in(prow + col, 4, a.partial, pbytes), a.status)) prow[col] = sum;
         }
     }
 }
@@ -403,6 +420,10 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
     const T* DRES = static_cast<const T*>(a.dres);
+    // extents for the checked build: x, dy, dx, dres; the partial rows
+    [[maybe_unused]] const int64_t tbytes =
+        a.M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t pbytes = ncl * static_cast<int64_t>(N) * 4;
 
     // rows of this cluster: cid, cid+ncl, ...
     const int64_t nrows = cid < a.M ? (a.M - 1 - cid) / ncl + 1 : 0;
@@ -432,6 +453,12 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         if (row == a.drop_unit) return;  // failure injection: this wait runs out
         const int64_t off = row * N + static_cast<int64_t>(vbeg) * VEC;
+        if (!RMSN_OK(span_in(X + off, bytes, X, tbytes) && span_in(DY + off, bytes, DY, tbytes) &&
+                         smem_span_in(sx + s * unit, bytes) && smem_span_in(sdy + s * unit, bytes) &&
+                         (!RES || (span_in(DRES + off, bytes, DRES, tbytes) &&
+                                   smem_span_in(sdr + s * unit, bytes))),
+                     a.status))
+            return;  // checked build: the wait for this stage runs out instead
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
         if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
@@ -498,8 +525,8 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
             const int k = j * nthr + tid;
             if (k >= vcnt) continue;
             float2 fx[PR], fd[PR], fw[PR];
-            P::unpack2(ld_shared_16(xs + k * 16), fx);
-            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            P::unpack2(ld_ring_16(xs + k * 16, a.status), fx);
+            P::unpack2(ld_ring_16(ds + k * 16, a.status), fd);
             weights(j, k, fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) dot2 = __ffma2_rn(__fmul2_rn(fd[e], fw[e]), fx[e], dot2);
@@ -552,9 +579,9 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
             const int k = j * nthr + tid;
             if (k >= vcnt) continue;
             float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
-            if constexpr (RES) P::unpack2(ld_shared_16(sdr + s * unit + k * 16), fr);
-            P::unpack2(ld_shared_16(xs + k * 16), fx);
-            P::unpack2(ld_shared_16(ds + k * 16), fd);
+            if constexpr (RES) P::unpack2(ld_ring_16(sdr + s * unit + k * 16, a.status), fr);
+            P::unpack2(ld_ring_16(xs + k * 16, a.status), fx);
+            P::unpack2(ld_ring_16(ds + k * 16, a.status), fd);
             weights(j, k, fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) {
@@ -566,7 +593,8 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
                     o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, gg));
                 acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
             }
-            st_global_16(dxr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(o));
+            T* dst = dxr + static_cast<int64_t>(vbeg + k) * VEC;
+            if (RMSN_OK(span_in(dst, 16, DX, tbytes), a.status)) st_global_16(dst, P::pack2(o));
         }
     };
 
@@ -630,7 +658,9 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         if (k >= vcnt) continue;
 #pragma unroll
         for (int q = 0; q < PR / 2; ++q)
-            *reinterpret_cast<float4*>(prow + static_cast<int64_t>(k) * VEC + 4 * q) =
+            if (float* pd = prow + static_cast<int64_t>(k) * VEC + 4 * q;
+                    RMSN_OK(span_in(pd, 16, a.partial, pbytes), a.status))
+                *reinterpret_cast<float4*>(pd) =
                 make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x, acc[j][2 * q + 1].y);
     }
     // no block may leave while a peer can still reach its shared memory
@@ -670,6 +700,10 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
     const T* DRES = static_cast<const T*>(a.dres);
+    // extents for the checked build: x, dy, dx, dres; the partial rows
+    [[maybe_unused]] const int64_t tbytes =
+        a.M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t pbytes = nb * static_cast<int64_t>(N) * 4;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
@@ -691,6 +725,12 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         if (tile == a.drop_unit) return;  // failure injection
         const int64_t off = tile * RT * N;
+        if (!RMSN_OK(span_in(X + off, bytes, X, tbytes) && span_in(DY + off, bytes, DY, tbytes) &&
+                         smem_span_in(sx + s * unit, bytes) && smem_span_in(sdy + s * unit, bytes) &&
+                         (!RES || (span_in(DRES + off, bytes, DRES, tbytes) &&
+                                   smem_span_in(sdr + s * unit, bytes))),
+                     a.status))
+            return;  // checked build: the wait for this tile runs out instead
         bulk_copy_g2s(sx + s * unit, X + off, bytes, &bar[s]);
         bulk_copy_g2s(sdy + s * unit, DY + off, bytes, &bar[s]);
         if constexpr (RES) bulk_copy_g2s(sdr + s * unit, DRES + off, bytes, &bar[s]);
@@ -759,8 +799,8 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                 if (!row_ok || k >= nvec) continue;
                 const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
                 float2 fx[PR], fd[PR], fw[PR];
-                P::unpack2(ld_shared_16(sx + s * unit + off), fx);
-                P::unpack2(ld_shared_16(sdy + s * unit + off), fd);
+                P::unpack2(ld_ring_16(sx + s * unit + off, a.status), fx);
+                P::unpack2(ld_ring_16(sdy + s * unit + off, a.status), fd);
                 WP::unpack2(wv[j], fw);
 #pragma unroll
                 for (int e = 0; e < PR; ++e) dot2 = __ffma2_rn(__fmul2_rn(fd[e], fw[e]), fx[e], dot2);
@@ -793,9 +833,9 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                 if (k >= nvec) continue;
                 const int off = (lr * N + k * VEC) * static_cast<int>(sizeof(T));
                 float2 fx[PR], fd[PR], fw[PR], o[PR], fr[PR];
-                if constexpr (RES) P::unpack2(ld_shared_16(sdr + s * unit + off), fr);
-                P::unpack2(ld_shared_16(sx + s * unit + off), fx);
-                P::unpack2(ld_shared_16(sdy + s * unit + off), fd);
+                if constexpr (RES) P::unpack2(ld_ring_16(sdr + s * unit + off, a.status), fr);
+                P::unpack2(ld_ring_16(sx + s * unit + off, a.status), fx);
+                P::unpack2(ld_ring_16(sdy + s * unit + off, a.status), fd);
                 WP::unpack2(wv[j], fw);
 #pragma unroll
                 for (int e = 0; e < PR; ++e) {
@@ -807,7 +847,8 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                         o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, g));
                     acc[j][e] = __ffma2_rn(fd[e], xh, acc[j][e]);
                 }
-                st_global_16(DX + row * N + static_cast<int64_t>(k) * VEC, P::pack2(o));
+                T* dst = DX + row * N + static_cast<int64_t>(k) * VEC;
+                if (RMSN_OK(span_in(dst, 16, DX, tbytes), a.status)) st_global_16(dst, P::pack2(o));
             }
         }
     }
@@ -826,7 +867,9 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
         if (k >= nvec) continue;
 #pragma unroll
         for (int q = 0; q < PR / 2; ++q)
-            *reinterpret_cast<float4*>(comb + group * N + k * VEC + 4 * q) =
+            if (float* cd = comb + group * N + k * VEC + 4 * q;
+                    RMSN_OK(smem_span_in(cd, 16), a.status))
+                *reinterpret_cast<float4*>(cd) =
                 make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
                             acc[j][2 * q + 1].y);
     }
@@ -834,8 +877,10 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
     float* prow = a.partial + b * N;
     for (int col = tid; col < N; col += blockDim.x) {
         float sum = 0.f;
-        for (int gi = 0; gi < groups; ++gi) sum += comb[gi * N + col];
-        prow[col] = sum;
+        for (int gi = 0; gi < groups; ++gi)
+            sum += RMSN_OK(smem_span_in(comb + gi * N + col, 4), a.status) ? comb[gi * N + col]
+                                                                           : 0.f;
+        if (RMSN_OK(span_in(prow + col, 4, a.partial, pbytes), a.status)) prow[col] = sum;
     }
 }
 
@@ -854,9 +899,15 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
     const TW* W = static_cast<const TW*>(a.w);
     T* DX = static_cast<T*>(a.dx);
     const T* DRES = static_cast<const T*>(a.dres);
+    // extents for the checked build: x, dy, dx, dres; the partial rows
+    [[maybe_unused]] const int64_t tbytes =
+        a.M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t pbytes =
+        static_cast<int64_t>(gridDim.x) * static_cast<int64_t>(N) * 4;
     float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
     wait_for_prerequisite_grid();  // no global access before this
-    for (int col = threadIdx.x; col < N; col += blockDim.x) prow[col] = 0.f;
+    for (int col = threadIdx.x; col < N; col += blockDim.x)
+        if (RMSN_OK(span_in(prow + col, 4, a.partial, pbytes), a.status)) prow[col] = 0.f;
     int it = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, ++it) {
         const T* xr = X + row * N;
@@ -876,11 +927,14 @@ __global__ void __launch_bounds__(256) bwd_scalar_kernel(BwdArgs a, int /*stages
             const float d = to_f32(dyr[col]);
             const float xh = to_f32(xr[col]) * r;
             const float g = d * to_f32(W[col]);
-            if constexpr (RES)
-                dxr[col] = P::from_float(fmaf(r, g - xh * c, to_f32(DRES[row * N + col])));
-            else
-                dxr[col] = P::from_float(r * (g - xh * c));
-            prow[col] = fmaf(d, xh, prow[col]);
+            if (RMSN_OK(span_in(dxr + col, sizeof(T), DX, tbytes), a.status)) {
+                if constexpr (RES)
+                    dxr[col] = P::from_float(fmaf(r, g - xh * c, to_f32(DRES[row * N + col])));
+                else
+                    dxr[col] = P::from_float(r * (g - xh * c));
+            }
+            if (RMSN_OK(span_in(prow + col, 4, a.partial, pbytes), a.status))
+                prow[col] = fmaf(d, xh, prow[col]);
         }
     }
 }

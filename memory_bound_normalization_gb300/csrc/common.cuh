@@ -446,4 +446,55 @@ __device__ __forceinline__ void report_status(int* status, int code) {
     if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------------------------ checked build
+// A debug build of the library (compiled with -DRMSNORM_CHECKS) checks every
+// global access of the kernels against the extent of the tensor it belongs
+// to (M*N elements for the activations, N for w and dw, M for rstd, the
+// partial rows for the workspace) and every ring access against the block's
+// dynamic shared memory, before it happens. A failed check records
+// kStatusOutOfBounds on the device status word and skips the access: it
+// never traps. In the normal build RMSN_OK(...) is the constant true and the
+// checks are not compiled at all, so the kernels are unchanged.
+constexpr int kStatusOutOfBounds = 7;
+
+// [p, p + n) lies inside [base, base + extent); n and extent in bytes.
+__host__ __device__ __forceinline__ bool span_in(const void* p, int64_t n, const void* base,
+                                                 int64_t extent) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(base);
+    return n >= 0 && extent >= 0 && a >= b && a - b <= static_cast<uintptr_t>(extent) &&
+           static_cast<uintptr_t>(n) <= static_cast<uintptr_t>(extent) - (a - b);
+}
+
+// Every extern dynamic shared-memory array of a kernel starts at this address.
+extern __shared__ __align__(128) unsigned char rmsn_dynamic_smem[];
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
+// [p, p + n) lies inside the block's dynamic shared memory.
+__device__ __forceinline__ bool smem_span_in(const void* p, uint32_t n) {
+    const uint32_t a = smem_u32(p), b = smem_u32(rmsn_dynamic_smem);
+    return a >= b && a - b <= dynamic_smem_bytes() && n <= dynamic_smem_bytes() - (a - b);
+}
+
+__device__ __forceinline__ bool record_if_out(bool ok, int* status) {
+    if (!ok) report_status(status, kStatusOutOfBounds);
+    return ok;
+}
+
+#ifdef RMSNORM_CHECKS
+#define RMSN_OK(cond, status) ::rmsn::record_if_out((cond), (status))
+#else
+#define RMSN_OK(cond, status) true
+#endif
+
+// A 16-byte ring read: checked against the dynamic shared memory in the
+// checked build (an out-of-range read gives zeros), a plain load otherwise.
+__device__ __forceinline__ uint4 ld_ring_16(const void* p, int* status) {
+    if (!RMSN_OK(smem_span_in(p, 16), status)) return make_uint4(0, 0, 0, 0);
+    return ld_shared_16(p);
+}
+
 }  // namespace rmsn

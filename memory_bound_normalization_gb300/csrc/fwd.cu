@@ -47,8 +47,12 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
                                                            T* __restrict__ y,
                                                            float* __restrict__ rstd, int64_t M,
                                                            int N, float eps, const T* res,
-                                                           T* hout) {
+                                                           T* hout, int* status) {
     using P = Pack<T>;
+    // extents for the checked build: x, res, h, y; rstd
+    [[maybe_unused]] const int64_t tbytes =
+        M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t rbytes = M * 4;
     constexpr int VEC = P::VEC;
     const int nvec = N / VEC;
     const int lane = threadIdx.x % G;
@@ -92,7 +96,8 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
                 const int k = j * G + lane;
                 if (row < M && k < nvec) {
                     xv[r][j] = add_vec<T>(xv[r][j], rv[r][j]);
-                    st_global_16(hout + row * N + static_cast<int64_t>(k) * VEC, xv[r][j]);
+                    T* hd = hout + row * N + static_cast<int64_t>(k) * VEC;
+                    if (RMSN_OK(span_in(hd, 16, hout, tbytes), status)) st_global_16(hd, xv[r][j]);
                 }
             }
         }
@@ -140,9 +145,10 @@ __global__ void __launch_bounds__(256) fwd_rowgroup_kernel(const T* x, const TW*
             WP::unpack2(wv[j], fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
-            st_global_16(y + row * N + static_cast<int64_t>(k) * VEC, P::pack2(fy));
+            T* yd = y + row * N + static_cast<int64_t>(k) * VEC;
+            if (RMSN_OK(span_in(yd, 16, y, tbytes), status)) st_global_16(yd, P::pack2(fy));
         }
-        if (lane == 0) rstd[row] = rs;
+        if (lane == 0 && RMSN_OK(span_in(rstd + row, 4, rstd, rbytes), status)) rstd[row] = rs;
     }
     allow_dependent_launch();
 }
@@ -166,6 +172,10 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
                    float* __restrict__ rstd, int64_t M, int N, float eps, int* status,
                    uint64_t wait_limit_ns, const T* res, T* hout) {
     using P = Pack<T>;
+    // extents for the checked build: x, res, h, y; rstd
+    [[maybe_unused]] const int64_t tbytes =
+        M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t rbytes = M * 4;
     constexpr int VEC = P::VEC;
     __shared__ float red[32];
     __shared__ float xslot[kMaxCluster];
@@ -178,6 +188,7 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
     const int nvec = N / VEC;
     const int base = static_cast<int>(crank) * V * nthr;
     const T* xr = x + row * N;
+    bool xok = true;  // the cluster exchange completed in time
 
     if (csize > 1) {
         if (threadIdx.x == 0) {
@@ -211,7 +222,8 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
             const int k = base + j * nthr + threadIdx.x;
             if (k < nvec) {
                 xv[j] = add_vec<T>(xv[j], rv[j]);
-                st_global_16(hout + row * N + static_cast<int64_t>(k) * VEC, xv[j]);
+                T* hd = hout + row * N + static_cast<int64_t>(k) * VEC;
+                if (RMSN_OK(span_in(hd, 16, hout, tbytes), status)) st_global_16(hd, xv[j]);
             }
         }
     }
@@ -237,11 +249,13 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
         if (threadIdx.x < csize)
             st_async_cluster_f32(cluster_map(&xslot[crank], threadIdx.x), total,
                                  cluster_map(&xbar, threadIdx.x));
-        if (!mbar_wait_cluster_bounded(&xbar, 0u, wait_limit_ns)) report_status(status, kStatusTimeout);
+        xok = mbar_wait_cluster_bounded(&xbar, 0u, wait_limit_ns);
+        if (!xok) report_status(status, kStatusTimeout);
         total = 0.f;
         for (uint32_t q = 0; q < csize; ++q) total += xslot[q];
-        // all C stores into this block have landed, so it may exit; the
-        // stores it sent are complete on their receivers' side the same way
+        // this block is done with its slots and its barrier; it leaves only
+        // after every block of the cluster has arrived here too (below)
+        cluster_arrive_relaxed();
     }
     const float rs = rsqrtf(total / static_cast<float>(N) + eps);
     const float2 rs2 = f2_splat(rs);
@@ -255,10 +269,20 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
         WP::unpack2(wv[j], fw);
 #pragma unroll
         for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
-        st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
+        T* yd = yr + static_cast<int64_t>(k) * VEC;
+        if (RMSN_OK(span_in(yd, 16, y, tbytes), status)) st_global_16(yd, P::pack2(fy));
     }
-    if (crank == 0 && threadIdx.x == 0) rstd[row] = rs;
+    if (crank == 0 && threadIdx.x == 0 && RMSN_OK(span_in(rstd + row, 4, rstd, rbytes), status))
+        rstd[row] = rs;
     allow_dependent_launch();
+    if (csize > 1) {
+        // No block may leave while a peer can still store into its shared
+        // memory: every block has sent its sum before it arrives. After a
+        // wait that ran out, a late sum may still be in flight to this
+        // block: let it land (bounded) before leaving.
+        cluster_wait();
+        if (!xok) mbar_wait_cluster_bounded(&xbar, 0u, wait_limit_ns);
+    }
 }
 
 // ---------------------------------------------------------------- wide rows
@@ -272,8 +296,12 @@ template <typename T, typename TW, int U, bool ADD>
 __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __restrict__ w,
                                                        T* __restrict__ y, float* __restrict__ rstd,
                                                        int64_t M, int N, float eps, const T* res,
-                                                       T* hout) {
+                                                       T* hout, int* status) {
     using P = Pack<T>;
+    // extents for the checked build: x, res, h, y; rstd
+    [[maybe_unused]] const int64_t tbytes =
+        M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t rbytes = M * 4;
     using WP = WPack<T, TW>;
     constexpr int VEC = P::VEC;
     constexpr int PR = P::PAIRS;
@@ -311,7 +339,9 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
                     const int k = base + u * nthr + tid;
                     if (k < nvec) {
                         v[u] = add_vec<T>(v[u], rv[u]);
-                        st_global_16_hint(hout + row * N + static_cast<int64_t>(k) * VEC, v[u], keep);
+                        T* hd = hout + row * N + static_cast<int64_t>(k) * VEC;
+                        if (RMSN_OK(span_in(hd, 16, hout, tbytes), status))
+                            st_global_16_hint(hd, v[u], keep);
                     }
                 }
             }
@@ -355,10 +385,11 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
                 WP::unpack2(wv[u], fw);
 #pragma unroll
                 for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
-                st_global_16(yr + static_cast<int64_t>(k) * VEC, P::pack2(fy));
+                T* yd = yr + static_cast<int64_t>(k) * VEC;
+                if (RMSN_OK(span_in(yd, 16, y, tbytes), status)) st_global_16(yd, P::pack2(fy));
             }
         }
-        if (tid == 0) rstd[row] = rs;
+        if (tid == 0 && RMSN_OK(span_in(rstd + row, 4, rstd, rbytes), status)) rstd[row] = rs;
     }
     allow_dependent_launch();
 }
@@ -390,6 +421,10 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
                                                       int* status, uint64_t wait_limit_ns,
                                                       const T* res, T* hout) {
     using P = Pack<T>;
+    // extents for the checked build: x, res, h, y; rstd
+    [[maybe_unused]] const int64_t tbytes =
+        M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t rbytes = M * 4;
     using WP = WPack<T, TW>;
     constexpr int VEC = P::VEC;
     constexpr int PR = P::PAIRS;
@@ -448,6 +483,11 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
         }
         mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
         const int64_t off = (cid + t * ncl) * N + static_cast<int64_t>(vbeg) * VEC;
+        if (!RMSN_OK(span_in(x + off, bytes, x, tbytes) && smem_span_in(sx + s * unit, bytes) &&
+                         (!ADD || (span_in(res + off, bytes, res, tbytes) &&
+                                   smem_span_in(sr + s * unit, bytes))),
+                     status))
+            return;  // checked build: the wait for this stage runs out instead
         bulk_copy_g2s(sx + s * unit, x + off, bytes, &bar[s]);
         if constexpr (ADD) bulk_copy_g2s(sr + s * unit, res + off, bytes, &bar[s]);
         pending |= 1u << s;
@@ -489,11 +529,13 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = j * nthr + tid;
-            xv[j] = k < vcnt ? ld_shared_16(sx + s * unit + k * 16) : make_uint4(0, 0, 0, 0);
+            xv[j] = k < vcnt ? ld_ring_16(sx + s * unit + k * 16, status)
+                             : make_uint4(0, 0, 0, 0);
             if constexpr (ADD) {
                 if (k < vcnt) {
-                    xv[j] = add_vec<T>(xv[j], ld_shared_16(sr + s * unit + k * 16));
-                    st_global_16(hout + row * N + static_cast<int64_t>(vbeg + k) * VEC, xv[j]);
+                    xv[j] = add_vec<T>(xv[j], ld_ring_16(sr + s * unit + k * 16, status));
+                    T* hd = hout + row * N + static_cast<int64_t>(vbeg + k) * VEC;
+                    if (RMSN_OK(span_in(hd, 16, hout, tbytes), status)) st_global_16(hd, xv[j]);
                 }
             }
             float2 f[PR];
@@ -541,9 +583,11 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
             WP::unpack2(wv[j], fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
-            st_global_16(yr + static_cast<int64_t>(vbeg + k) * VEC, P::pack2(fy));
+            T* yd = yr + static_cast<int64_t>(vbeg + k) * VEC;
+            if (RMSN_OK(span_in(yd, 16, y, tbytes), status)) st_global_16(yd, P::pack2(fy));
         }
-        if (crank == 0 && tid == 0) rstd[row] = rs;
+        if (crank == 0 && tid == 0 && RMSN_OK(span_in(rstd + row, 4, rstd, rbytes), status))
+            rstd[row] = rs;
     }
     allow_dependent_launch();
     // after a failure, let copies already in flight land before going on
@@ -562,8 +606,12 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* x, const TW* _
                                                          T* __restrict__ y,
                                                          float* __restrict__ rstd, int64_t M,
                                                          int N, float eps, const T* res,
-                                                         T* hout) {
+                                                         T* hout, int* status) {
     using P = Pack<T>;
+    // extents for the checked build: x, res, h, y; rstd
+    [[maybe_unused]] const int64_t tbytes =
+        M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    [[maybe_unused]] const int64_t rbytes = M * 4;
     __shared__ float red[2][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     wait_for_prerequisite_grid();  // no global access before this
@@ -575,7 +623,8 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* x, const TW* _
             float v = to_f32(xr[j]);
             if constexpr (ADD) {
                 const T hv = P::from_float(v + to_f32(res[row * N + j]));
-                hout[row * N + j] = hv;
+                if (RMSN_OK(span_in(hout + row * N + j, sizeof(T), hout, tbytes), status))
+                    hout[row * N + j] = hv;
                 v = to_f32(hv);
             }
             ss = fmaf(v, v, ss);
@@ -590,8 +639,10 @@ __global__ void __launch_bounds__(256) fwd_scalar_kernel(const T* x, const TW* _
         // with ADD, h is read back from the elements this thread stored
         const T* src = ADD ? hout + row * N : xr;
         for (int j = threadIdx.x; j < N; j += blockDim.x)
-            yr[j] = P::from_float(to_f32(src[j]) * rs * to_f32(w[j]));
-        if (threadIdx.x == 0) rstd[row] = rs;
+            if (RMSN_OK(span_in(yr + j, sizeof(T), y, tbytes), status))
+                yr[j] = P::from_float(to_f32(src[j]) * rs * to_f32(w[j]));
+        if (threadIdx.x == 0 && RMSN_OK(span_in(rstd + row, 4, rstd, rbytes), status))
+            rstd[row] = rs;
     }
 }
 
@@ -601,7 +652,7 @@ cudaError_t launch_rowgroup(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStrea
                                : fwd_rowgroup_kernel<T, TW, G, V, R, false>;
     return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
                       static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
-                      static_cast<const T*>(a.res), static_cast<T*>(a.h));
+                      static_cast<const T*>(a.res), static_cast<T*>(a.h), a.status);
 }
 
 template <typename T, typename TW>
@@ -678,7 +729,7 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
         auto fn = a.res != nullptr ? fwd_wide_kernel<T, TW, 4, true> : fwd_wide_kernel<T, TW, 4, false>;
         return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
                           static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
-                          a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h));
+                          a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h), a.status);
     }
     switch (p.variant) {
         case RMSNORM_VARIANT_ROWGROUP: return dispatch_rowgroup<T, TW>(p, a, s);
@@ -689,7 +740,8 @@ cudaError_t dispatch(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) 
             auto fn = a.res != nullptr ? fwd_scalar_kernel<T, TW, true> : fwd_scalar_kernel<T, TW, false>;
             return launch_pdl(fn, p.grid, p.threads, 0, 1, s, static_cast<const T*>(a.x),
                               static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N,
-                              a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h));
+                              a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h),
+                              a.status);
         }
         default: return cudaErrorInvalidValue;
     }

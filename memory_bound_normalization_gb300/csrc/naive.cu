@@ -32,8 +32,8 @@ __global__ void __launch_bounds__(1024) naive_row_kernel(const T* __restrict__ x
                                                          const TW* __restrict__ w,
                                                          const T* __restrict__ dy,
                                                          T* __restrict__ dx,
-                                                         T* __restrict__ contrib, int N,
-                                                         float eps) {
+                                                         T* __restrict__ contrib, int64_t M,
+                                                         int N, float eps, int* status) {
     using P = Pack<T>;
     using WP = WPack<T, TW>;
     constexpr int VEC = P::VEC, PR = P::PAIRS;
@@ -80,7 +80,12 @@ __global__ void __launch_bounds__(1024) naive_row_kernel(const T* __restrict__ x
         o[e] = __fmul2_rn(r2, __ffma2_rn(xh, nc2, __fmul2_rn(fd[e], fw[e])));
         q[e] = __fmul2_rn(fd[e], xh);
     }
-    if (ok) {
+    // extent of dx and of the intermediate, for the checked build
+    [[maybe_unused]] const int64_t tbytes =
+        M * static_cast<int64_t>(N) * static_cast<int64_t>(sizeof(T));
+    if (ok && RMSN_OK(span_in(dx + off, 16, dx, tbytes) &&
+                          span_in(contrib + off, 16, contrib, tbytes),
+                      status)) {
         st_global_16(dx + off, P::pack2(o));
         st_global_16(contrib + off, P::pack2(q));
     }
@@ -92,7 +97,7 @@ template <typename T>
 __global__ void __launch_bounds__(kColsumThreads) naive_colsum_kernel(const T* __restrict__ contrib,
                                                                       float* __restrict__ partial,
                                                                       int64_t M, int N,
-                                                                      int64_t chunk) {
+                                                                      int64_t chunk, int* status) {
     using P = Pack<T>;
     constexpr int VEC = P::VEC, PR = P::PAIRS;
     const int nvec = N / VEC;
@@ -110,10 +115,12 @@ __global__ void __launch_bounds__(kColsumThreads) naive_colsum_kernel(const T* _
         for (int e = 0; e < PR; ++e) acc[e] = __fadd2_rn(acc[e], f[e]);
     }
     float* prow = partial + static_cast<int64_t>(blockIdx.y) * N + static_cast<int64_t>(k) * VEC;
+    [[maybe_unused]] const int64_t pbytes = static_cast<int64_t>(gridDim.y) * N * 4;
 #pragma unroll
     for (int e = 0; e < PR; e += 2)
-        *reinterpret_cast<float4*>(prow + 2 * e) =
-            make_float4(acc[e].x, acc[e].y, acc[e + 1].x, acc[e + 1].y);
+        if (RMSN_OK(span_in(prow + 2 * e, 16, partial, pbytes), status))
+            *reinterpret_cast<float4*>(prow + 2 * e) =
+                make_float4(acc[e].x, acc[e].y, acc[e + 1].x, acc[e + 1].y);
 }
 
 template <typename T, typename TW>
@@ -124,16 +131,21 @@ cudaError_t launch_chain(const void* x, const void* w, const void* dy, void* dx,
     T* contrib = static_cast<T*>(workspace);
     float* partial = reinterpret_cast<float*>(
         static_cast<unsigned char*>(workspace) + naive_contrib_bytes(M, N, sizeof(T)));
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
+    const DeviceInfo* dev = device_info(device);
+    int* status = dev ? dev->status_word : nullptr;
     naive_row_kernel<T, TW><<<static_cast<unsigned>(M), round_up(nvec, 32), 0, s>>>(
         static_cast<const T*>(x), static_cast<const TW*>(w), static_cast<const T*>(dy),
-        static_cast<T*>(dx), contrib, N, eps);
-    cudaError_t e = cudaGetLastError();
+        static_cast<T*>(dx), contrib, M, N, eps, status);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t chunk = (M + kSplit - 1) / kSplit;
     const int parts = static_cast<int>((M + chunk - 1) / chunk);
     naive_colsum_kernel<T><<<dim3(static_cast<unsigned>((nvec + kColsumThreads - 1) / kColsumThreads),
                                   static_cast<unsigned>(parts)),
-                             kColsumThreads, 0, s>>>(contrib, partial, M, N, chunk);
+                             kColsumThreads, 0, s>>>(contrib, partial, M, N, chunk, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return colsum_launch(partial, dw, parts, N, s);

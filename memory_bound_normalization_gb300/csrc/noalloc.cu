@@ -110,3 +110,5 @@ extern "C" int rmsnorm_bwd_noalloc(const void* x, const void* w, const void* dy,
     }
     return RMSNORM_OK;
 }
+
+extern "C" size_t rmsnorm_noalloc_scratch_bytes(void) { return kScratchBytes; }

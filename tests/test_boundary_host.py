@@ -43,7 +43,7 @@ def test_exports_are_c_symbols(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = pkg.rmsnorm_status_string(code)
         assert s.startswith("RMSNORM_") and "UNKNOWN" not in s
     assert "UNKNOWN" in pkg.rmsnorm_status_string(99)
