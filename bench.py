@@ -909,6 +909,16 @@ def run_ours(args):
     return line if rank == 0 else None
 
 
+def steady_fields(cell, step_bytes: int, peak: float) -> dict:
+    """The steady-state step of a cell (back to back, no flush) as GB/s and
+    a fraction of the measured copy bandwidth; empty when not timed."""
+    sd = cell.get("steady")
+    if not sd:
+        return {}
+    gbs = step_bytes / (sd["step_ms"] * 1e-3) / 1e9
+    return {"steady_gbs": round(gbs, 1), "steady_frac": round(gbs / peak, 4)}
+
+
 def run_sweep(pkg, torch, synth, args, local, l2, peak):
     """The width sweep (fixed M*N = 2^27, bf16 and fp32): each cell validated
     against PyTorch, then forward and backward timed after a clean cold L2,
@@ -919,13 +929,15 @@ def run_sweep(pkg, torch, synth, args, local, l2, peak):
             code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
             elem = torch.empty(0, dtype=wl.dtype).element_size()
             fb, bb = synth.logical_bytes(wl.M, wl.N, elem)
-            c = time_cell(pkg, torch, synth, wl, "norm", code, args.sweep_steps, 3, local, l2)
+            c = time_cell(pkg, torch, synth, wl, "norm", code, args.sweep_steps, 3, local, l2,
+                          steady_steps=min(args.steady_steps, 100))
             fg = fb / (c["fwd_mean"] * 1e-3) / 1e9
             bg = bb / (c["bwd_mean"] * 1e-3) / 1e9
             cells.append({"workload": wl.name, "dtype": wl.dtype_name, "M": wl.M, "N": wl.N,
                           "fwd_gbs": round(fg, 1), "bwd_gbs": round(bg, 1),
                           "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
-                          "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1)})
+                          "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1),
+                          **steady_fields(c, fb + bb, peak)})
             del c
     return {"steps": args.sweep_steps, "peak_gbs": peak, "cells": cells}
 
@@ -946,7 +958,8 @@ def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None):
         code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
         elem = torch.empty(0, dtype=wl.dtype).element_size()
         fb, bb = synth.logical_bytes(wl.M, wl.N, elem)
-        c = time_cell(pkg, torch, synth, wl, "norm", code, args.config_steps, 5, local, l2)
+        c = time_cell(pkg, torch, synth, wl, "norm", code, args.config_steps, 5, local, l2,
+                      steady_steps=min(args.steady_steps, 100))
         fg = fb / (c["fwd_mean"] * 1e-3) / 1e9
         bg = bb / (c["bwd_mean"] * 1e-3) / 1e9
         plan_b = pkg.rmsnorm_plan(wl.M, wl.N, code, pkg.PASS_BWD, local).as_dict()
@@ -957,6 +970,7 @@ def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None):
                       "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
                       "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1),
                       "bwd_variant": plan_b["variant_name"],
+                      **steady_fields(c, fb + bb, peak),
                       "validation": c["errs"]})
         del c
     return {"steps": args.config_steps, "peak_gbs": peak, "cells": cells}

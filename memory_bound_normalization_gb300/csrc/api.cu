@@ -2,6 +2,7 @@
 // per-device properties, the device status word, workspace handling and
 // dispatch to the kernel translation units.
 #include <atomic>
+#include <cstdlib>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -156,6 +157,14 @@ int bwd_alloc_run(const void* x, const void* w, const void* dy, const float* rst
 }
 
 }  // namespace
+
+int pdl_mode() {
+    static const int mode = [] {
+        const char* v = getenv("RMSNORM_PDL");
+        return (v == nullptr || *v == 0) ? 1 : (atoi(v) != 0 ? 1 : 0);
+    }();
+    return mode;
+}
 
 const DeviceInfo* device_info(int device) {
     if (device < 0 || device >= kMaxDevices) return nullptr;

@@ -70,8 +70,11 @@ const BwdTuning& tuning() {
 // ---------------------------------------------------------- column sum
 // dw[j] = sum over p of partial[p][j] in a fixed tree: thread row q of the
 // block (Q rows of 32 threads, 32 columns) sums p = q, q+Q, q+2Q, ... in
-// ascending order, then the Q sums are added in q order. Same bits on every
-// run for a given P and Q.
+// ascending order; then warp c adds the Q sums of column c (and of c+Q,
+// c+2Q, ... when Q < 32) by a fixed xor-butterfly of shuffles. Same bits on
+// every run for a given P and Q. (Adding the Q sums one after another in a
+// single thread made a chain of 32 dependent shared-memory reads and adds
+// at the end of every backward call.)
 template <int Q>
 __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict__ partial,
                                                         float* __restrict__ dw, int P, int N,
@@ -80,22 +83,26 @@ __global__ void __launch_bounds__(32 * Q) colsum_kernel(const float* __restrict_
     wait_for_prerequisite_grid();  // partial rows complete and visible
     allow_dependent_launch();
     const int cx = threadIdx.x, q = threadIdx.y;
-    const int64_t col = static_cast<int64_t>(blockIdx.x) * 32 + cx;
+    const int64_t col0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int64_t col = col0 + cx;
+    [[maybe_unused]] const int64_t pbytes = static_cast<int64_t>(P) * N * 4;
     float s = 0.f;
     if (col < N) {
 #pragma unroll 4
         for (int p = q; p < P; p += Q) {
             const float* src = partial + static_cast<int64_t>(p) * N + col;
-            if (RMSN_OK(span_in(src, 4, partial, static_cast<int64_t>(P) * N * 4), status)) s += *src;
+            if (RMSN_OK(span_in(src, 4, partial, pbytes), status)) s += *src;
         }
     }
     part[q][cx] = s;
     __syncthreads();
-    if (q == 0 && col < N) {
-        float t = 0.f;
-#pragma unroll
-        for (int i = 0; i < Q; ++i) t += part[i][cx];
-        if (RMSN_OK(span_in(dw + col, 4, dw, static_cast<int64_t>(N) * 4), status)) dw[col] = t;
+    for (int c = q; c < 32; c += Q) {
+        // lane l holds thread row l's sum of column c (zero past Q rows)
+        float v = cx < Q ? part[cx][c] : 0.f;
+        v = group_allreduce<32>(v);
+        if (cx == 0 && col0 + c < N &&
+            RMSN_OK(span_in(dw + col0 + c, 4, dw, static_cast<int64_t>(N) * 4), status))
+            dw[col0 + c] = v;
     }
 }
 
@@ -519,7 +526,7 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_allowed();
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.cluster > 1) {
@@ -548,7 +555,7 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cs.stream = s;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    pdl[0].val.programmaticStreamSerializationAllowed = pdl_allowed();
     cs.attrs = pdl;
     cs.numAttrs = 1;
     const float* part = a.partial;

@@ -703,13 +703,20 @@ const void* ring_kernel_for(int dtype, int V, bool add) {
     }
 }
 
+// A ring grid of clusters is launched in plain stream order. Launched early
+// (programmatic serialization) while the previous kernel still held SMs, its
+// persistent clusters ran the steady forward + backward step of 2048 x 65536
+// rows at 74% (bf16) and 82% (fp32) of the copy roofline against 92% in
+// stream order; single-block ring grids and every other kernel gain from the
+// early launch.
 template <typename T, typename TW, int V, bool ADD>
 cudaError_t launch_ring(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t s) {
-    return launch_pdl(fwd_ring_kernel<T, TW, V, ADD>, p.grid, p.threads,
-                      static_cast<size_t>(p.smem_bytes), p.cluster, s, static_cast<const T*>(a.x),
-                      static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
-                      p.stages, a.status, a.wait_limit_ns, static_cast<const T*>(a.res),
-                      static_cast<T*>(a.h));
+    return launch_ex(fwd_ring_kernel<T, TW, V, ADD>, p.grid, p.threads,
+                     static_cast<size_t>(p.smem_bytes), p.cluster, s, p.cluster <= 1,
+                     static_cast<const T*>(a.x),
+                     static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
+                     p.stages, a.status, a.wait_limit_ns, static_cast<const T*>(a.res),
+                     static_cast<T*>(a.h));
 }
 
 template <typename T, typename TW>

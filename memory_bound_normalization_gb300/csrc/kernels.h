@@ -53,12 +53,19 @@ struct BwdArgs {
 
 constexpr int kMaxCluster = 8;
 
+// Programmatic stream serialization of library launches: on, except where
+// a launch asks for plain stream order; RMSNORM_PDL=0 turns it off for every
+// launch (read once; a sweep knob).
+int pdl_mode();
+inline int pdl_allowed(bool want = true) { return want && pdl_mode() != 0 ? 1 : 0; }
+
 // Launches a library kernel with programmatic stream serialization (it may
 // start while the previous kernel of the stream finishes; the kernel waits
-// for it before touching memory) and, for cluster > 1, a cluster shape.
+// for it before touching memory) unless `pdl` is false, and, for
+// cluster > 1, a cluster shape.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*fn)(KArgs...), int grid, int threads, size_t smem, int cluster,
-                       cudaStream_t s, Args... args) {
+cudaError_t launch_ex(void (*fn)(KArgs...), int grid, int threads, size_t smem, int cluster,
+                      cudaStream_t s, bool pdl, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
@@ -66,7 +73,7 @@ cudaError_t launch_pdl(void (*fn)(KArgs...), int grid, int threads, size_t smem,
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_allowed(pdl);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cluster > 1) {
@@ -77,6 +84,12 @@ cudaError_t launch_pdl(void (*fn)(KArgs...), int grid, int threads, size_t smem,
         cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, fn, static_cast<KArgs>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*fn)(KArgs...), int grid, int threads, size_t smem, int cluster,
+                       cudaStream_t s, Args... args) {
+    return launch_ex(fn, grid, threads, smem, cluster, s, true, args...);
 }
 
 // Width-dependent choices (host only, no device queries). `vector_ok` says
