@@ -41,6 +41,8 @@ struct BwdTuning {
                                    // dres, 2 always
     int rowgroup_max_vec = -1;     // widest row (16-byte vectors) for the short-row kernel
                                    // (-1 = by type: 256 for fp32 rows, 128 for 16-bit rows)
+    int early_refill = -1;         // refill a ring stage after pass 2 of its row (1) or
+                                   // after pass 1 of the next row (0); -1 = by plan
 };
 
 int env_int(const char* name, int dflt) {
@@ -62,6 +64,7 @@ const BwdTuning& tuning() {
         u.cluster = std::max(0, std::min(kMaxCluster, env_int("RMSNORM_BWD_CLUSTER", 0)));
         u.wide_select = std::max(0, std::min(2, env_int("RMSNORM_WIDE_SELECT", 2)));
         u.rowgroup_max_vec = std::max(-1, std::min(256, env_int("RMSNORM_BWD_ROWGROUP_MAX_VEC", -1)));
+        u.early_refill = std::max(-1, std::min(1, env_int("RMSNORM_BWD_EARLY_REFILL", -1)));
         return u;
     }();
     return t;
@@ -537,6 +540,15 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
         cfg.numAttrs = 2;
     }
     BwdArgs args = a;
+    // A stage is refilled once pass 2 of its row is done (one more block
+    // barrier a row) where a thread holds 8 vectors of a wide row: its row
+    // takes twice as long, and refilling only after the next row's pass 1
+    // left the two-deep ring of the fp32 2048 x 65536 backward at 90% of the
+    // copy roofline (99% with the early refill). Everywhere else the extra
+    // barrier cost 1-4 points and the later refill stays.
+    args.early_refill = tuning().early_refill >= 0
+                            ? tuning().early_refill
+                            : (p.cluster > 1 && p.vectors_per_thread >= 8 ? 1 : 0);
     if (p.partial_rows == 1) args.partial = a.dw;  // the one partial row is dw
     int stages = p.stages, groups = p.row_groups;
     void* kargs[3] = {&args, &stages, &groups};

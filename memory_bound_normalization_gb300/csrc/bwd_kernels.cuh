@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
     float r2 = nrows > 1 ? __ldg(a.rstd + vid + nvirt) : 0.f;
     bool failed = false;  // a copy wait ran out in this group
 
+    const bool early = a.early_refill != 0;  // refill a stage after pass 2 of its row
     RingPos cons;  // ring position of row t
     for (int64_t t = 0; t < nrows; ++t) {
         const int64_t row = vid + t * nvirt;
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
         float tot = lane < gnw ? rslot[lane] : 0.f;
         tot = group_allreduce<32>(tot);
         // the stage of row t-1 is free now: refill it with row t-1+S
-        if (gt == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+        if (!early && gt == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
             fence_proxy_async_shared();
             issue(t - 1 + S);
         }
@@ -306,6 +307,14 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
             }
             T* dst = dxr + static_cast<int64_t>(vbeg + k) * VEC;
             if (RMSN_OK(span_in(dst, 16, DX, tbytes), a.status)) st_global_16(dst, P::pack2(o));
+        }
+        if (early) {
+            // refill row t's stage as soon as the group is done with it
+            group_barrier(bar_id, TG);
+            if (gt == 0 && !failed && t + S < nrows) {
+                fence_proxy_async_shared();
+                issue(t + S);
+            }
         }
     }
     allow_dependent_launch();
@@ -628,17 +637,26 @@ __global__ void __launch_bounds__(512) bwd_wide_kernel(BwdArgs a, int stages, in
         }
     } else {
         // one row at a time: S-1 rows in flight, the exchange waited for in place
+        const bool early = a.early_refill != 0;
         for (int64_t t = 0; t < nrows; ++t) {
             const float r_after = t + 2 < nrows ? __ldg(a.rstd + cid + (t + 2) * ncl) : 0.f;
             pass1(t);
             __syncthreads();  // sums of row t published; every thread is done with row t-1
             failed = *fail != 0;
             const float own = reduce_send(t);
-            if (tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
+            if (!early && tid == 0 && !failed && t >= 1 && t - 1 + S < nrows) {
                 fence_proxy_async_shared();
                 issue(t - 1 + S);
             }
             pass2(t, r_cur, receive(t, own));
+            if (early) {
+                // refill row t's stage as soon as every thread is done with it
+                __syncthreads();
+                if (tid == 0 && !failed && t + S < nrows) {
+                    fence_proxy_async_shared();
+                    issue(t + S);
+                }
+            }
             r_cur = r_next;
             r_next = r_after;
         }

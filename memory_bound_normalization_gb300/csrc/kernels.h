@@ -49,6 +49,7 @@ struct BwdArgs {
     int64_t drop_unit;  // failure-injection hook, -1 = off
     const void* dres;   // gradient added to dx (residual path), nullptr = none
     int sm_count;       // the device's SMs (sizes the column sum)
+    int early_refill;   // refill a ring stage right after pass 2 of its row
 };
 
 constexpr int kMaxCluster = 8;
