@@ -333,6 +333,17 @@ def event_ms(a, b) -> float:
     return a.elapsed_time(b)
 
 
+def by_set(xs, nsets: int) -> list:
+    """Median time of the calls on each clone set (step k uses set k % nsets)."""
+    return [round(statistics.median(xs[i::nsets]), 5) for i in range(nsets) if xs[i::nsets]]
+
+
+def p90(xs) -> float:
+    """90th percentile (nearest rank)."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, -(-9 * len(ys) // 10) - 1))]
+
+
 def make_flush(torch, l2: int, device):
     """The clean-cold-L2 step run before every timed call: write a 2x L2
     buffer, then read another 2x L2 buffer, so the written dirty lines are
@@ -674,6 +685,8 @@ def time_cell(pkg, torch, synth, wl, op, code, steps, warmup, local, l2, check_f
 
     fwd_ms = [event_ms(e[0], e[1]) for e in ev]
     bwd_ms = [event_ms(e[2], e[3]) for e in ev]
+    # throughput is total bytes over total time: the means; the median, the
+    # minimum and the 90th percentile are reported beside them
     fwd_mean = sum(fwd_ms) / K
     bwd_mean = sum(bwd_ms) / K
     step_ms = fwd_mean + bwd_mean
@@ -845,12 +858,16 @@ def run_ours(args):
             "logical_bytes": {"fwd": fwd_bytes, "bwd": bwd_bytes},
         },
         "fwd": {"ms": round(fwd_mean, 5), "median_ms": round(statistics.median(fwd_ms), 5),
+                "min_ms": round(min(fwd_ms), 5), "p90_ms": round(p90(fwd_ms), 5),
+                "median_ms_by_clone_set": by_set(fwd_ms, nsets),
                 "gbs": round(fwd_gbs, 1),
                 "frac_of_peak": round(fwd_gbs / peak, 4),
                 "frac_of_probe": round(fwd_gbs / probes_open["best"], 4),
                 "frac_of_cold_copy": round(fwd_gbs / cold["fwd_sized"]["median_gbs"], 4),
                 "plan": plan_f},
         "bwd": {"ms": round(bwd_mean, 5), "median_ms": round(statistics.median(bwd_ms), 5),
+                "min_ms": round(min(bwd_ms), 5), "p90_ms": round(p90(bwd_ms), 5),
+                "median_ms_by_clone_set": by_set(bwd_ms, nsets),
                 "gbs": round(bwd_gbs, 1),
                 "frac_of_peak": round(bwd_gbs / peak, 4),
                 "frac_of_probe": round(bwd_gbs / probes_open["best"], 4),

@@ -834,6 +834,11 @@ struct FwdTuning {
                                // residual, 2 always
     int rowgroup_max_vec = -1; // widest row (16-byte vectors) for the short-row kernel
                                // (-1: 256, or 128 with the residual)
+    // largest stage budget the device choice tries: with 200 KB rings as
+    // well, the deeper ring won the ties and bf16 rows of 32768 and 98304 ran
+    // their forward at 94.6% and 84.8% of the copy roofline, against 96.2%
+    // and 85.9% with 100 KB (other widths unchanged)
+    int ring_max_budget = 100 * 1024;
 };
 
 const FwdTuning& fwd_tuning() {
@@ -855,6 +860,8 @@ const FwdTuning& fwd_tuning() {
         if (rs && *rs) u.ring_smem = std::max(16 * 1024, std::min(227 * 1024, atoi(rs)));
         const char* ws = getenv("RMSNORM_WIDE_SELECT");
         if (ws && *ws) u.wide_select = std::max(0, std::min(2, atoi(ws)));
+        const char* rb = getenv("RMSNORM_FWD_RING_MAX_BUDGET");
+        if (rb && *rb) u.ring_max_budget = std::max(16 * 1024, std::min(227 * 1024, atoi(rb)));
         const char* gm = getenv("RMSNORM_FWD_ROWGROUP_MAX_VEC");
         if (gm && *gm) u.rowgroup_max_vec = std::max(0, std::min(256, atoi(gm)));
         return u;
@@ -1016,6 +1023,7 @@ cudaError_t ring_select(const DeviceInfo& dev, int dtype, int64_t N, bool add, r
         for (int max_v : {4, 8}) {
             if (max_v == 8 && elem != 4) continue;
             for (int budget : {100 * 1024, 200 * 1024}) {
+                if (budget > fwd_tuning().ring_max_budget) continue;
                 rmsnorm_plan_t q = *p;
                 if (!ring_plan_c(nvec, add ? 2 : 1, elem, c, max_v, budget, &q)) continue;
                 if (q.smem_bytes > dev.max_smem_optin) continue;
@@ -1045,12 +1053,86 @@ cudaError_t ring_select(const DeviceInfo& dev, int dtype, int64_t N, bool add, r
 
 }  // namespace
 
+namespace {
+
+template <typename T, typename TW>
+const void* row_kernel_ptr() {
+    return reinterpret_cast<const void*>(&fwd_row_kernel<T, TW, 4, false>);
+}
+
+const void* row_kernel_for(int dtype) {
+    switch (dtype) {
+        case RMSNORM_BF16: return row_kernel_ptr<__nv_bfloat16, __nv_bfloat16>();
+        case RMSNORM_F16: return row_kernel_ptr<__half, __half>();
+        case RMSNORM_BF16_W_F32: return row_kernel_ptr<__nv_bfloat16, float>();
+        case RMSNORM_F16_W_F32: return row_kernel_ptr<__half, float>();
+        case RMSNORM_F32: return row_kernel_ptr<float, float>();
+        default: return nullptr;
+    }
+}
+
+std::mutex g_pair_mu;
+std::map<std::tuple<int, int, int64_t>, bool> g_pair_single;
+
+// A row the static ladder splits over a cluster of two blocks may fit one
+// block of up to 1024 threads instead. Whichever keeps more threads resident
+// on an SM runs (ties: the single block, which needs no exchange). With 62
+// registers a thread, fp32 rows of 5120 and 8192 ran at 100% and 95% of the
+// copy roofline in one block against 95% and 93% as pairs, while one block
+// of 384 threads (6144) fits only twice on an SM (768 threads against 960 as
+// pairs) and ran at 87% against 94%.
+cudaError_t pair_or_single(const DeviceInfo& dev, int dtype, int64_t N, rmsnorm_plan_t* p) {
+    // one block holding the whole row, 4 vectors a thread
+    const int t1 = round_up(static_cast<int>(cdiv(N / dtype_vec(dtype), 4)), 32);
+    const int t2 = p->threads;  // each block of the pair
+    const auto key = std::make_tuple(dev.device, dtype, N);
+    {
+        std::lock_guard<std::mutex> lk(g_pair_mu);
+        auto it = g_pair_single.find(key);
+        if (it != g_pair_single.end()) {
+            if (it->second) {
+                p->variant = RMSNORM_VARIANT_CTA_ROW;
+                p->cluster = 1;
+                p->threads = p->threads_per_row = t1;
+            }
+            return cudaSuccess;
+        }
+    }
+    const void* fn = row_kernel_for(dtype);
+    if (fn == nullptr) return cudaErrorInvalidValue;
+    const int cap = dtype_size(dtype) == weight_size(dtype) ? 1024 : 512;  // launch bound
+    bool single = false;
+    if (t1 <= cap) {
+        int b1 = 0, b2 = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, fn, t1, 0);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, fn, t2, 0);
+        if (e != cudaSuccess) return e;
+        single = b1 * t1 >= b2 * t2;
+    }
+    std::lock_guard<std::mutex> lk(g_pair_mu);
+    g_pair_single[key] = single;
+    if (single) {
+        p->variant = RMSNORM_VARIANT_CTA_ROW;
+        p->cluster = 1;
+        p->threads = p->threads_per_row = t1;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
                             rmsnorm_plan_t* p, bool add) {
     const FwdTuning& tu = fwd_tuning();
     if (p->variant == RMSNORM_VARIANT_RING && p->cluster >= 2 && tu.ring_cluster == 0 &&
         tu.ring_smem == 200 * 1024 && tu.wide_select >= (add ? 2 : 1)) {
         cudaError_t e = ring_select(dev, dtype, N, add, p);
+        if (e != cudaSuccess) return e;
+    }
+    // a pair of blocks, or one block, per row (plain forward, default ladder)
+    if (p->variant == RMSNORM_VARIANT_CLUSTER_ROW && p->cluster == 2 && !add && tu.wide < 0 &&
+        tu.row_threads == 0 && tu.cluster_threads == 256 && p->vectors_per_thread == 4) {
+        cudaError_t e = pair_or_single(dev, dtype, N, p);
         if (e != cudaSuccess) return e;
     }
     switch (p->variant) {
