@@ -71,6 +71,9 @@ BWD_KERNEL_FILES = ("bwd.cu", "bwd_kernels.cuh", "bwd_f32.cu", "bwd_bf16.cu", "b
                     "kernels.h")
 
 
+FWD_KERNEL_FILES = ("fwd.cu", "common.cuh", "kernels.h")
+
+
 def kernel_source_hash(names=BWD_KERNEL_FILES) -> str:
     """sha256 over the csrc files that define a kernel family (by default the
     backward), so a profile can be matched to the kernel code it measured."""
