@@ -1,11 +1,15 @@
 """The autograd wrappers run the library's kernels: their outputs and
-gradients equal the direct C-ABI calls bit for bit, and agree with
-PyTorch's own rms_norm autograd (fp32) within the bf16 rule."""
+gradients equal the direct C-ABI calls bit for bit, match the fp64 oracle
+within the parity tolerances, and agree with PyTorch's own rms_norm autograd
+(fp32) within the bf16 rule."""
 from __future__ import annotations
 
 import pytest
 import torch
 import torch.nn.functional as F
+
+import oracle
+from parity_util import check_dw, check_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -21,6 +25,7 @@ def _lib():
         pytest.skip("needs a CUDA device")
     torch.cuda.set_device(0)
     pkg.load_library(build_if_missing=True)
+    oracle.build()
     yield
 
 
@@ -53,6 +58,11 @@ def test_rms_norm_autograd(shape, dtype, w_dtype):
     assert torch.equal(y.detach().view(M, N), y2)
     assert torch.equal(x.grad.view(M, N), dx2)
     assert torch.equal(w.grad.float(), dw2.to(w.dtype).float())
+    # the oracle
+    xc, wc, dyc = inp["x"].cpu(), inp["w"].cpu(), inp["dy"].cpu()
+    check_rows(y.detach().view(M, N), oracle.fwd(xc, wc, 1e-6)[0], dtype, "autograd y")
+    check_rows(x.grad.view(M, N), oracle.bwd_dx(xc, wc, dyc, 1e-6), dtype, "autograd dx")
+    check_dw(dw2, oracle.bwd_dw(xc, dyc, 1e-6), "autograd dw (fp32)")
     # PyTorch's own, in fp32
     x32 = inp["x"].float().requires_grad_(True)
     w32 = inp["w"].float().requires_grad_(True)

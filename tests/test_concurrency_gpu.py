@@ -2,13 +2,16 @@
 backward takes its workspace from the stream-ordered pool on its own stream,
 and the plan caches (the device's cluster-shape choice included) are shared.
 Every thread's results equal the same calls made one after another, bit for
-bit."""
+bit, and those results match the fp64 oracle."""
 from __future__ import annotations
 
 import threading
 
 import pytest
 import torch
+
+import oracle
+from parity_util import check_dw, check_rows, check_rstd
 
 pytestmark = pytest.mark.gpu
 
@@ -27,6 +30,7 @@ def _lib():
         pytest.skip("needs a CUDA device")
     torch.cuda.set_device(0)
     pkg.load_library(build_if_missing=True)
+    oracle.build()
     yield
 
 
@@ -49,6 +53,15 @@ def test_threads_and_streams_match_sequential_calls():
         _step(inp, ref, M, N, code, wl.eps, torch.cuda.current_stream())
         work.append((inp, ref, M, N, code, wl.eps))
     torch.cuda.synchronize()
+    # the sequential results against the oracle (so the threads below are
+    # checked against it too, through bit equality)
+    for inp, (y, rstd, dx, dw), M, N, code, eps in work:
+        xc, wc, dyc = inp["x"].cpu(), inp["w"].cpu(), inp["dy"].cpu()
+        y_ref, r_ref = oracle.fwd(xc, wc, eps)
+        check_rows(y, y_ref, inp["x"].dtype, f"{M}x{N} y")
+        check_rstd(rstd, r_ref, f"{M}x{N} rstd")
+        check_rows(dx, oracle.bwd_dx(xc, wc, dyc, eps), inp["x"].dtype, f"{M}x{N} dx")
+        check_dw(dw, oracle.bwd_dw(xc, dyc, eps), f"{M}x{N} dw")
 
     errors = []
 
