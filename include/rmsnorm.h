@@ -104,6 +104,9 @@ int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd,
  * RMSNORM_ERR_NOMEM if that fails. Use rmsnorm_bwd_ws to pass your own.
  * When the rows are few enough for one block (or one cluster) to take them
  * all, its partial row is dw itself: one kernel, no workspace, no allocation.
+ * Up to 16 blocks' worth of rows run as one thread-block cluster whose
+ * blocks add their partial rows in rank order through distributed shared
+ * memory into dw: again one kernel and no workspace.
  */
 int rmsnorm_bwd(const void *x, const void *w, const void *dy,
                 const float *rstd, void *dx, float *dw,
@@ -302,7 +305,10 @@ typedef struct {
     int threads_per_row;    /* lanes sharing one row (ROWGROUP), else threads */
     int rows_per_unit;      /* rows per block pass (row-group tile, or row
                                groups); TWO_PASS: blocks per SM */
-    int cluster;            /* blocks per row (1 unless CLUSTER_ROW or RING) */
+    int cluster;            /* blocks per row (1 unless CLUSTER_ROW or RING);
+                               backward ROWGROUP / CTA_ROW with cluster > 1:
+                               the grid is one cluster of that many blocks,
+                               which sums dw on chip (few rows) */
     int row_groups;         /* independent row groups per block (backward
                                CTA_ROW: each group of threads/row_groups
                                threads owns its own rows; else 1) */

@@ -106,6 +106,39 @@ __device__ __forceinline__ void group_barrier(int id, int threads) {
 }
 
 
+// Few rows: the grid is a single cluster, and dw is summed on chip instead of
+// through partial rows in global memory and a second kernel. Every block has
+// its dw contribution in its shared memory at `row` (W floats, W a multiple of
+// 4, 16-byte aligned); block rank r adds the C blocks' values of its share of
+// the columns in rank order and writes them to dw. The same bits on every run
+// for a given cluster size. Called by every thread of every block.
+__device__ __forceinline__ void cluster_rows_to_dw(const float* row, int W, float* dw,
+                                                   int* status) {
+    cluster_sync_all();  // every block's row is complete and visible to the cluster
+    const uint32_t C = cluster_size(), r = cluster_rank();
+    const int n4 = W / 4;
+    const int per = (n4 + static_cast<int>(C) - 1) / static_cast<int>(C);
+    const int beg = static_cast<int>(r) * per, end = min(n4, beg + per);
+    for (int k = beg + static_cast<int>(threadIdx.x); k < end; k += blockDim.x) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (uint32_t q = 0; q < C; ++q) {
+            const float4 v = ld_cluster_f32x4(row + 4 * k, q);
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+        float* d = dw + 4 * k;
+        if (RMSN_OK(span_in(d, 16, dw, static_cast<int64_t>(W) * 4), status)) {
+            d[0] = s.x;
+            d[1] = s.y;
+            d[2] = s.z;
+            d[3] = s.w;
+        }
+    }
+    cluster_sync_all();  // no block leaves while a peer still reads its row
+}
+
 // ------------------------------------------------------ row groups per block
 // A block holds `groups` independent row groups of TG = blockDim.x / groups
 // threads. Group g of block b works as a virtual block v = b*groups + g of
@@ -327,7 +360,35 @@ __global__ void __launch_bounds__(512) bwd_row_kernel(BwdArgs a, int stages, int
 
     // one partial row per cluster (or block); each block writes its column slice
     float* prow = a.partial + cid * N + static_cast<int64_t>(vbeg) * VEC;
-    if (groups == 1) {
+    if (a.cluster_dw) {
+        // the grid is one cluster: the groups' dw meet in shared memory (group
+        // order), then the blocks' rows in dw (rank order)
+        __syncthreads();
+        float* comb = reinterpret_cast<float*>(smem);
+        const int W = vcnt * VEC;
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = j * TG + gt;
+            if (k >= vcnt) continue;
+#pragma unroll
+            for (int q = 0; q < PR / 2; ++q)
+                if (float* cd = comb + g * W + k * VEC + 4 * q;
+                    RMSN_OK(smem_span_in(cd, 16), a.status))
+                *reinterpret_cast<float4*>(cd) =
+                    make_float4(acc[j][2 * q].x, acc[j][2 * q].y, acc[j][2 * q + 1].x,
+                                acc[j][2 * q + 1].y);
+        }
+        __syncthreads();
+        if (groups > 1)
+            for (int col = tid; col < W; col += blockDim.x) {
+                float sum = 0.f;
+                for (int gi = 0; gi < groups; ++gi)
+                    sum += RMSN_OK(smem_span_in(comb + gi * W + col, 4), a.status)
+                               ? comb[gi * W + col] : 0.f;
+                comb[col] = sum;  // group 0's value of this column was read above
+            }
+        cluster_rows_to_dw(comb, W, a.dw, a.status);
+    } else if (groups == 1) {
         // one partial row per cluster; each block writes its column slice
 #pragma unroll
         for (int j = 0; j < V; ++j) {
@@ -892,6 +953,19 @@ __global__ void __launch_bounds__(256) bwd_rowgroup_kernel(BwdArgs a, int stages
                             acc[j][2 * q + 1].y);
     }
     __syncthreads();
+    if (a.cluster_dw) {
+        // the grid is one cluster: the groups' dw meet in shared memory (group
+        // order), then the blocks' rows in dw (rank order)
+        for (int col = tid; col < N; col += blockDim.x) {
+            float sum = 0.f;
+            for (int gi = 0; gi < groups; ++gi)
+                sum += RMSN_OK(smem_span_in(comb + gi * N + col, 4), a.status)
+                           ? comb[gi * N + col] : 0.f;
+            comb[col] = sum;  // group 0's value of this column was read above
+        }
+        cluster_rows_to_dw(comb, N, a.dw, a.status);
+        return;
+    }
     float* prow = a.partial + b * N;
     for (int col = tid; col < N; col += blockDim.x) {
         float sum = 0.f;
@@ -994,9 +1068,9 @@ template <typename T, typename TW, bool RES>
 const void* main_kernel(const rmsnorm_plan_t& p, bool pipelined) {
     switch (p.variant) {
         case RMSNORM_VARIANT_ROWGROUP: return rowgroup_kernel<T, TW, RES>(p.threads_per_row, p.vectors_per_thread);
-        case RMSNORM_VARIANT_CTA_ROW:
-        case RMSNORM_VARIANT_CLUSTER_ROW:
-            // single blocks: the grouped kernel; clusters: the pipelined one
+        case RMSNORM_VARIANT_CTA_ROW:  // a row per group of a block (in a cluster for few rows)
+            return row_kernel<T, TW, RES>(p.vectors_per_thread);
+        case RMSNORM_VARIANT_CLUSTER_ROW:  // a row split over a cluster
             return p.cluster == 1 ? row_kernel<T, TW, RES>(p.vectors_per_thread)
                                   : wide_kernel<T, TW, RES>(p.vectors_per_thread, pipelined);
         case RMSNORM_VARIANT_SCALAR: return reinterpret_cast<const void*>(&bwd_scalar_kernel<T, TW, RES>);

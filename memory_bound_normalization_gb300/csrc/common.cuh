@@ -387,6 +387,19 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
     return v;
 }
 
+// Reads 16 bytes (16-byte aligned) from the same shared-memory location in
+// block `rank` of this cluster.
+__device__ __forceinline__ float4 ld_cluster_f32x4(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
 // Address of the same shared-memory location in block `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank) {
     uint32_t remote;

@@ -50,6 +50,7 @@ struct BwdArgs {
     const void* dres;   // gradient added to dx (residual path), nullptr = none
     int sm_count;       // the device's SMs (sizes the column sum)
     int early_refill;   // refill a ring stage right after pass 2 of its row
+    int cluster_dw;     // the grid is one cluster that sums dw on chip (no workspace)
 };
 
 constexpr int kMaxCluster = 8;
