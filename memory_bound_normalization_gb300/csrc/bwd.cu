@@ -46,6 +46,8 @@ struct BwdTuning {
                                    // after pass 1 of the next row (0); -1 = by plan
     int cluster_dw_units = 16;     // rows (or tiles, or row-group units) up to which one
                                    // cluster sums dw on chip (0 = never)
+    int pdl_wide = -1;             // programmatic launch of rows split over a cluster:
+                                   // 1 always, 0 never, -1 by plan
 };
 
 int env_int(const char* name, int dflt) {
@@ -69,6 +71,7 @@ const BwdTuning& tuning() {
         u.rowgroup_max_vec = std::max(-1, std::min(256, env_int("RMSNORM_BWD_ROWGROUP_MAX_VEC", -1)));
         u.early_refill = std::max(-1, std::min(1, env_int("RMSNORM_BWD_EARLY_REFILL", -1)));
         u.cluster_dw_units = std::max(0, env_int("RMSNORM_BWD_CLUSTER_DW_UNITS", u.cluster_dw_units));
+        u.pdl_wide = std::max(-1, std::min(1, env_int("RMSNORM_BWD_PDL_WIDE", u.pdl_wide)));
         return u;
     }();
     return t;
@@ -551,6 +554,31 @@ cudaError_t colsum_launch(const float* partial, float* dw, int P, int N, cudaStr
     return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(cdiv(N, 32))), dim3(32, q), args, 0, s);
 }
 
+// Whether a backward launch may start early behind the previous kernel of
+// the stream. Rows split over a cluster with a two-deep ring and two blocks
+// to an SM go in plain stream order: launched early, the steady forward +
+// backward step of fp32 rows of 32768 and 49152 ran at 85% and 83% of the
+// copy roofline, in stream order at 95% and 97%. Every other wide plan
+// measured (fp32 16384 and 65536, 16-bit 32768 to 98304) lost 1 point there.
+static bool wide_pdl(const rmsnorm_plan_t& p, const void* fn) {
+    if (p.variant != RMSNORM_VARIANT_CLUSTER_ROW) return true;
+    const int mode = tuning().pdl_wide;
+    if (mode >= 0) return mode == 1;
+    if (p.stages != 2) return true;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    const DeviceInfo* dev = device_info(device);
+    int units = 0;
+    if (dev == nullptr || resident_units(*dev, fn, p.threads, p.smem_bytes, 1, &units) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return units / dev->sm_count != 2;
+}
+
 cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cudaStream_t s) {
     if (p.grid <= 0) return cudaSuccess;
     const void* fn = main_kernel_for(dtype, p, a.dres != nullptr);
@@ -562,7 +590,7 @@ cudaError_t bwd_launch(const rmsnorm_plan_t& p, int dtype, const BwdArgs& a, cud
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl_allowed();
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_allowed(wide_pdl(p, fn));
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.cluster > 1) {
