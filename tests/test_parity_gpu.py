@@ -74,7 +74,8 @@ TYPE_IDS = ["bf16", "f32", "f16", "bf16_wf32", "f16_wf32"]
 
 
 SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (37, 256),
-          (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (5, 6144), (4, 8192),
+          (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (3, 5120), (5, 6144),
+          (2, 7168), (4, 8192),
           (3, 16384), (3, 20480), (5, 24576), (2, 32768), (3, 40960), (4, 49152), (3, 57344),
           (2, 65536), (1, 65536), (2, 98304), (3, 131072),
           (1000, 40), (777, 96)]
@@ -312,6 +313,39 @@ def test_single_partial_row_is_dw(M, N, dtype):
     torch.cuda.synchronize()
     assert torch.equal(dwr, dw)  # dres does not enter dw
     check_rows(dxr, oracle.add_bwd_dx(x.cpu(), w.cpu(), dy.cpu(), dres.cpu(), eps), dtype, "dx")
+
+
+FEW = [(16, 4096, torch.bfloat16), (64, 4096, torch.bfloat16), (40, 1024, torch.bfloat16),
+       (300, 128, torch.float16), (20, 2880, torch.float32), (9, 257, torch.float32)]
+
+
+@pytest.mark.parametrize("M,N,dtype", FEW, ids=[f"{m}x{n}-{str(d)[6:]}" for m, n, d in FEW])
+def test_few_rows_one_cluster(M, N, dtype):
+    """Rows for 2 to 16 blocks run as one thread-block cluster whose blocks add
+    their dw rows in rank order through distributed shared memory: no
+    workspace, no column sum, dw bit for bit the same on every call, and the
+    same results through every backward entry point."""
+    code = pkg.dtype_code(dtype)
+    plan = pkg.rmsnorm_plan(M, N, code, pkg.PASS_BWD, 0)
+    inp, eps = inputs(M, N, dtype, seed=M % 11)
+    x, w, dy = inp["x"], inp["w"], inp["dy"]
+    vector = pkg.VARIANTS[plan.variant] in ("rowgroup", "cta_row")
+    if vector and plan.cluster > 1:
+        assert plan.partial_rows == 1 and plan.workspace_bytes == 0
+        assert plan.grid == plan.cluster and 2 <= plan.cluster <= 16
+    y, rstd, dx, dw = run(x, w, dy, eps)
+    check_all(x, w, dy, eps, y, rstd, dx, dw)
+    for _ in range(3):
+        dx2, dw2 = pkg.backward(x, w, dy, rstd)
+        torch.cuda.synchronize()
+        assert torch.equal(dx2, dx) and torch.equal(dw2.view(torch.int32), dw.view(torch.int32))
+    dx3 = torch.empty_like(x)
+    dw3 = torch.full((N,), float("nan"), dtype=torch.float32, device=DEV)
+    need = pkg.rmsnorm_bwd_workspace_size(M, N, code, 0)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=DEV)
+    pkg.check(pkg.rmsnorm_bwd_ws(x, w, dy, rstd, dx3, dw3, M, N, code, ws, need))
+    torch.cuda.synchronize()
+    assert torch.equal(dx3, dx) and torch.equal(dw3, dw)
 
 
 @pytest.mark.parametrize("wl_name", ["hidden4096_16384x4096", "qknorm_1048576x128",
