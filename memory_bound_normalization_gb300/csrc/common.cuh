@@ -1,7 +1,8 @@
 // Device helpers shared by the RMSNorm kernels: 16-byte packing of
-// fp32/bf16/fp16 rows and of weights stored in their own type, warp reductions, and inline-PTX wrappers for mbarriers, 1-D bulk
-// copies (cp.async.bulk, no tensor map), thread-block clusters and the
-// global timer used by the bounded waits.
+// fp32/bf16/fp16 rows and of weights stored in their own type, warp
+// reductions, inline-PTX wrappers for mbarriers, 1-D bulk copies
+// (cp.async.bulk, no tensor map), thread-block clusters and the global timer
+// used by the bounded waits, and the range tests of the checked build.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -188,9 +189,6 @@ __device__ __forceinline__ uint4 add_vec(const uint4& a, const uint4& b) {
 }
 
 // ------------------------------------------------------------ global memory
-__device__ __forceinline__ uint4 ld_global_16(const void* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
 // Streaming read: the row is used once, do not keep it in L1.
 __device__ __forceinline__ uint4 ld_global_16_stream(const void* p) {
     uint4 v;
@@ -201,16 +199,6 @@ __device__ __forceinline__ uint4 ld_global_16_stream(const void* p) {
 }
 __device__ __forceinline__ void st_global_16(void* p, const uint4& v) {
     *reinterpret_cast<uint4*>(p) = v;
-}
-// Coherent streaming read (no read-only path) of data that may share memory
-// with one of the kernel's outputs. It is not ordered against other memory
-// accesses: the caller reads each element before any thread writes it.
-__device__ __forceinline__ uint4 ld_global_16_coherent(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
 }
 
 // L2 eviction-priority policies (createpolicy): evict_last keeps lines that
@@ -327,12 +315,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst_smem, const void* src_gm
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
-// Asks L2 to fetch [src, src+bytes) ahead of use (16-byte aligned, a
-// multiple of 16 bytes); completes on its own, nothing waits for it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src_gmem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes)
-                 : "memory");
-}
 // Orders this thread's generic-proxy shared-memory accesses before later
 // async-proxy (bulk copy) accesses to the same buffers.
 __device__ __forceinline__ void fence_proxy_async_shared() {
@@ -377,15 +359,6 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
-// Reads a float from the same shared-memory variable in block `rank` of
-// this cluster (distributed shared memory).
-__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 // Reads 16 bytes (16-byte aligned) from the same shared-memory location in
 // block `rank` of this cluster.
@@ -406,23 +379,12 @@ __device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
     return remote;
 }
-// Store a float into another block's shared memory (distributed shared memory).
-__device__ __forceinline__ void st_cluster_f32(uint32_t remote, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
-}
 // Asynchronous store of 4 bytes into another block's shared memory whose
 // completion is counted (4 transaction bytes) on that block's mbarrier.
 __device__ __forceinline__ void st_async_cluster_f32(uint32_t remote, float v, uint32_t remote_bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
                      remote),
                  "r"(__float_as_uint(v)), "r"(remote_bar)
-                 : "memory");
-}
-// Arrive on an mbarrier in another block of the cluster, releasing this
-// thread's prior writes (including distributed shared-memory stores) at
-// cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                  : "memory");
 }
 // try_wait with acquire at cluster scope: makes the writes released by
