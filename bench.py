@@ -993,10 +993,13 @@ def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None):
     return {"steps": args.config_steps, "peak_gbs": peak, "cells": cells}
 
 
-def run_small_m(pkg, torch, steps: int = 200):
+def run_small_m(pkg, torch, steps: int = 200, per_graph: int = 20):
     """Launch-bound shapes: microseconds per forward+backward step, back to
-    back, called eagerly through the C ABI versus replayed as one captured
-    CUDA graph (inputs stay in L2 here; this measures latency, not HBM)."""
+    back (inputs stay in L2 here; this measures latency, not HBM): called
+    eagerly through the C ABI, replayed as a captured CUDA graph of one step,
+    and replayed as a graph of `per_graph` steps. The first two pay the
+    host's cost of a call or a replay every step, which for these shapes is
+    about as long as the device's work; the last shows the device's time."""
     from memory_bound_normalization_gb300 import synth
 
     out = []
@@ -1036,9 +1039,24 @@ def run_small_m(pkg, torch, steps: int = 200):
             e1.record(side)
         e1.synchronize()
         graph_us = event_ms(e0, e1) * 1e3 / steps
+        many = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(many, stream=side):
+            for _ in range(per_graph):
+                step()
+        reps = max(1, steps // per_graph)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                many.replay()
+            e0.record(side)
+            for _ in range(reps):
+                many.replay()
+            e1.record(side)
+        e1.synchronize()
+        many_us = event_ms(e0, e1) * 1e3 / (reps * per_graph)
         torch.cuda.current_stream().wait_stream(side)
         out.append({"M": M, "N": N, "eager_us_per_step": round(eager_us, 2),
-                    "graph_us_per_step": round(graph_us, 2)})
+                    "graph_us_per_step": round(graph_us, 2),
+                    f"graph_of_{per_graph}_steps_us_per_step": round(many_us, 2)})
     return out
 
 
