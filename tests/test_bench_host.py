@@ -32,3 +32,18 @@ def test_drift_limit_and_new_options():
     assert a.steady_steps > 0 and not a.no_configs and not a.require_idle
     assert set(bench.CONFIG_WORKLOADS) == {"small_256x1024", "hidden8192_32768x8192_outliers",
                                            "qknorm_1048576x128"}
+
+
+def test_statistics_helpers():
+    xs = [float(v) for v in range(1, 11)]
+    assert bench.p90(xs) == 9.0
+    assert bench.p90([3.0]) == 3.0
+    # step k runs on clone set k % nsets
+    assert bench.by_set([1.0, 10.0, 3.0, 30.0, 5.0], 2) == [3.0, 20.0]
+    assert bench.by_set([2.0, 4.0], 3) == [2.0, 4.0]
+
+
+def test_steady_fields():
+    assert bench.steady_fields({"steady": None}, 10**9, 1000.0) == {}
+    got = bench.steady_fields({"steady": {"step_ms": 0.5}}, 10**9, 4000.0)
+    assert got == {"steady_gbs": 2000.0, "steady_frac": 0.5}
