@@ -174,8 +174,8 @@ IDLE_MAX_MIB = 1024
 IDLE_MAX_UTIL = 5
 
 
-def judge_idle(samples: list[tuple[float, float]]) -> dict:
-    """Idle verdict over (memory used MiB, utilisation %) samples."""
+def assess_idle(samples: list[tuple[float, float]]) -> dict:
+    """Whether the GPU was idle over (memory used MiB, utilisation %) samples."""
     if not samples:
         return {"checked": False, "busy": None}
     mem = max(s[0] for s in samples)
@@ -200,7 +200,7 @@ def idle_gate(local: int) -> dict:
                 pass
         if k < 2:
             time.sleep(0.2)
-    return judge_idle(samples)
+    return assess_idle(samples)
 
 
 def env_record(torch, local: int, l2: int) -> dict:

@@ -6,14 +6,14 @@ import bench
 
 
 def test_idle_verdict():
-    assert bench.judge_idle([]) == {"checked": False, "busy": None}
-    idle = bench.judge_idle([(0.0, 0.0), (3.0, 0.0), (0.0, 1.0)])
+    assert bench.assess_idle([]) == {"checked": False, "busy": None}
+    idle = bench.assess_idle([(0.0, 0.0), (3.0, 0.0), (0.0, 1.0)])
     assert idle["checked"] and idle["busy"] is False
     assert idle["memory_used_mib_max"] == 3.0 and idle["utilization_pct_max"] == 1.0
     # another process's memory, or work on the GPU, in any sample makes it busy
-    assert bench.judge_idle([(0.0, 0.0), (bench.IDLE_MAX_MIB + 1.0, 0.0)])["busy"] is True
-    assert bench.judge_idle([(0.0, bench.IDLE_MAX_UTIL + 1.0)])["busy"] is True
-    assert bench.judge_idle([(bench.IDLE_MAX_MIB, bench.IDLE_MAX_UTIL)])["busy"] is False
+    assert bench.assess_idle([(0.0, 0.0), (bench.IDLE_MAX_MIB + 1.0, 0.0)])["busy"] is True
+    assert bench.assess_idle([(0.0, bench.IDLE_MAX_UTIL + 1.0)])["busy"] is True
+    assert bench.assess_idle([(bench.IDLE_MAX_MIB, bench.IDLE_MAX_UTIL)])["busy"] is False
 
 
 def test_smi_index_follows_visible_devices(monkeypatch):
