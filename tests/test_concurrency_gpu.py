@@ -21,7 +21,8 @@ from memory_bound_normalization_gb300 import synth  # noqa: E402
 DEV = "cuda:0"
 
 CASES = [(512, 4096, torch.bfloat16), (64, 40960, torch.bfloat16), (96, 24576, torch.float32),
-         (2048, 128, torch.bfloat16), (33, 257, torch.float32), (40, 53248, torch.float16)]
+         (2048, 128, torch.bfloat16), (33, 257, torch.float32), (40, 53248, torch.float16),
+         (16, 4096, torch.bfloat16), (40, 1024, torch.bfloat16)]  # the last two: one cluster
 
 
 @pytest.fixture(scope="module", autouse=True)
