@@ -199,13 +199,17 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
     }
     wait_for_prerequisite_grid();  // no global access before this
     using WP = WPack<T, TW>;
+    // fp32 rows load their weights only for the scaling, after the row's sum:
+    // holding them through the reduction took the kernel to 62 registers, so
+    // that a block of 384 threads fitted only twice on an SM
+    constexpr bool kLateW = sizeof(T) == 4;
     uint4 xv[V], wv[V][WP::WORDS];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int k = base + j * nthr + threadIdx.x;
         const bool ok = k < nvec;
         xv[j] = ok ? ld_global_16_stream(xr + static_cast<int64_t>(k) * VEC) : make_uint4(0, 0, 0, 0);
-        if (ok) WP::load(w, k, wv[j]);
+        if (!kLateW && ok) WP::load(w, k, wv[j]);
         else WP::zero(wv[j]);
     }
     if constexpr (ADD) {
@@ -260,6 +264,13 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
     const float rs = rsqrtf(total / static_cast<float>(N) + eps);
     const float2 rs2 = f2_splat(rs);
     T* yr = y + row * N;
+    if constexpr (kLateW) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const int k = base + j * nthr + threadIdx.x;
+            if (k < nvec) WP::load(w, k, wv[j]);
+        }
+    }
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int k = base + j * nthr + threadIdx.x;
@@ -945,7 +956,13 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
         return;
     const bool clusters = tu.wide >= 0 ? tu.wide == 1 : !half;
     const int row_cap = dtype_size(dtype) == weight_size(dtype) ? 1024 : 512;
-    const int row_threads = std::min(row_cap, tu.row_threads > 0 ? tu.row_threads : (half ? 512 : 256));
+    // one block per row up to this many threads, clusters beyond: fp32 rows in
+    // one block of up to 384 threads ran their forward at 103% of the copy
+    // roofline (N = 4352 to 6144) against 92-97% as pairs of blocks, while at
+    // 448 and 512 threads (N = 7168, 8192) the pairs ran 1-1.5 points ahead
+    // (the row kernel holds fp32 weights only for the scaling, 46 registers)
+    const int row_threads = std::min(row_cap, tu.row_threads > 0 ? tu.row_threads
+                                              : half ? 512 : add ? 256 : 384);
     if (vector_ok && nvec <= static_cast<int64_t>(row_threads) * 4) {
         p->variant = RMSNORM_VARIANT_CTA_ROW;
         p->vectors_per_thread = 4;
@@ -1053,86 +1070,12 @@ cudaError_t ring_select(const DeviceInfo& dev, int dtype, int64_t N, bool add, r
 
 }  // namespace
 
-namespace {
-
-template <typename T, typename TW>
-const void* row_kernel_ptr() {
-    return reinterpret_cast<const void*>(&fwd_row_kernel<T, TW, 4, false>);
-}
-
-const void* row_kernel_for(int dtype) {
-    switch (dtype) {
-        case RMSNORM_BF16: return row_kernel_ptr<__nv_bfloat16, __nv_bfloat16>();
-        case RMSNORM_F16: return row_kernel_ptr<__half, __half>();
-        case RMSNORM_BF16_W_F32: return row_kernel_ptr<__nv_bfloat16, float>();
-        case RMSNORM_F16_W_F32: return row_kernel_ptr<__half, float>();
-        case RMSNORM_F32: return row_kernel_ptr<float, float>();
-        default: return nullptr;
-    }
-}
-
-std::mutex g_pair_mu;
-std::map<std::tuple<int, int, int64_t>, bool> g_pair_single;
-
-// A row the static ladder splits over a cluster of two blocks may fit one
-// block of up to 1024 threads instead. Whichever keeps more threads resident
-// on an SM runs (ties: the single block, which needs no exchange). With 62
-// registers a thread, fp32 rows of 5120 and 8192 ran at 100% and 95% of the
-// copy roofline in one block against 95% and 93% as pairs, while one block
-// of 384 threads (6144) fits only twice on an SM (768 threads against 960 as
-// pairs) and ran at 87% against 94%.
-cudaError_t pair_or_single(const DeviceInfo& dev, int dtype, int64_t N, rmsnorm_plan_t* p) {
-    // one block holding the whole row, 4 vectors a thread
-    const int t1 = round_up(static_cast<int>(cdiv(N / dtype_vec(dtype), 4)), 32);
-    const int t2 = p->threads;  // each block of the pair
-    const auto key = std::make_tuple(dev.device, dtype, N);
-    {
-        std::lock_guard<std::mutex> lk(g_pair_mu);
-        auto it = g_pair_single.find(key);
-        if (it != g_pair_single.end()) {
-            if (it->second) {
-                p->variant = RMSNORM_VARIANT_CTA_ROW;
-                p->cluster = 1;
-                p->threads = p->threads_per_row = t1;
-            }
-            return cudaSuccess;
-        }
-    }
-    const void* fn = row_kernel_for(dtype);
-    if (fn == nullptr) return cudaErrorInvalidValue;
-    const int cap = dtype_size(dtype) == weight_size(dtype) ? 1024 : 512;  // launch bound
-    bool single = false;
-    if (t1 <= cap) {
-        int b1 = 0, b2 = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, fn, t1, 0);
-        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, fn, t2, 0);
-        if (e != cudaSuccess) return e;
-        single = b1 * t1 >= b2 * t2;
-    }
-    std::lock_guard<std::mutex> lk(g_pair_mu);
-    g_pair_single[key] = single;
-    if (single) {
-        p->variant = RMSNORM_VARIANT_CTA_ROW;
-        p->cluster = 1;
-        p->threads = p->threads_per_row = t1;
-    }
-    return cudaSuccess;
-}
-
-}  // namespace
-
 cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t N,
                             rmsnorm_plan_t* p, bool add) {
     const FwdTuning& tu = fwd_tuning();
     if (p->variant == RMSNORM_VARIANT_RING && p->cluster >= 2 && tu.ring_cluster == 0 &&
         tu.ring_smem == 200 * 1024 && tu.wide_select >= (add ? 2 : 1)) {
         cudaError_t e = ring_select(dev, dtype, N, add, p);
-        if (e != cudaSuccess) return e;
-    }
-    // a pair of blocks, or one block, per row (plain forward, default ladder)
-    if (p->variant == RMSNORM_VARIANT_CLUSTER_ROW && p->cluster == 2 && !add && tu.wide < 0 &&
-        tu.row_threads == 0 && tu.cluster_threads == 256 && p->vectors_per_thread == 4) {
-        cudaError_t e = pair_or_single(dev, dtype, N, p);
         if (e != cudaSuccess) return e;
     }
     switch (p->variant) {
