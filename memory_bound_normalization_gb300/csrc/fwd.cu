@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(row_kernel_max_threads<T, TW>())
     // fp32 rows load their weights only for the scaling, after the row's sum:
     // holding them through the reduction took the kernel to 62 registers, so
     // that a block of 384 threads fitted only twice on an SM
-    constexpr bool kLateW = sizeof(T) == 4;
+    constexpr bool kLateW = sizeof(T) == 4;  // (16-bit rows stay at 64 registers either way)
     uint4 xv[V], wv[V][WP::WORDS];
 #pragma unroll
     for (int j = 0; j < V; ++j) {
