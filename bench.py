@@ -110,6 +110,12 @@ def parse_args(argv=None):
     p.add_argument("--profile", action="store_true",
                    help="lean run for profilers: no probes, validation, e2e or CPU baseline")
     p.add_argument("--json-out", default=None, help="also write the JSON line to this file")
+    p.add_argument("--results-dir", default=None,
+                   help="write env.json and one JSON line per timed cell (cells.jsonl) here")
+    p.add_argument("--resume", action="store_true",
+                   help="with --results-dir: take the sweep and workload cells already in "
+                        "cells.jsonl instead of timing them again (the main cell is always "
+                        "timed)")
     return p.parse_args(argv)
 
 
@@ -232,6 +238,55 @@ def env_record(torch, local: int, l2: int) -> dict:
             "python": platform.python_version(), "host_arch": platform.machine(),
             "host_cores": os.cpu_count(), "git_head": git,
             "library_source_hash": libbuild.source_hash()}
+
+
+# ------------------------------------------------------------ result files
+
+class ResultsLog:
+    """Per-run record: env.json and cells.jsonl (one JSON object a timed
+    cell) in a directory, so that an interrupted run can be resumed without
+    timing its finished cells again. Without a directory it records nothing."""
+
+    def __init__(self, directory: str | None, resume: bool = False):
+        self.dir = directory
+        self.cells: dict[tuple[str, str], dict] = {}
+        if directory is None:
+            return
+        os.makedirs(directory, exist_ok=True)
+        path = os.path.join(directory, "cells.jsonl")
+        if resume and os.path.exists(path):
+            with open(path) as f:
+                for line in f:
+                    line = line.strip()
+                    if not line:
+                        continue
+                    try:
+                        rec = json.loads(line)
+                    except ValueError:
+                        continue  # a line cut off by the interruption
+                    self.cells[(rec.get("kind", ""), rec.get("workload", ""))] = rec
+        elif os.path.exists(path):
+            os.remove(path)
+
+    def done(self, kind: str, workload: str) -> dict | None:
+        rec = self.cells.get((kind, workload))
+        if rec is None:
+            return None
+        return {k: v for k, v in rec.items() if k != "kind"}
+
+    def add(self, kind: str, cell: dict) -> None:
+        if self.dir is None:
+            return
+        rec = {"kind": kind, **cell}
+        self.cells[(kind, cell.get("workload", ""))] = rec
+        with open(os.path.join(self.dir, "cells.jsonl"), "a") as f:
+            f.write(json.dumps(rec) + "\n")
+
+    def env(self, env: dict) -> None:
+        if self.dir is None:
+            return
+        with open(os.path.join(self.dir, "env.json"), "w") as f:
+            json.dump(env, f, indent=1)
 
 
 # ------------------------------------------------------------ multi-rank
@@ -904,11 +959,16 @@ def run_ours(args):
         "idle_gate": idle,
         "env": env_record(torch, local, l2),
     }
+    log = ResultsLog(args.results_dir if rank == 0 else None, args.resume)
+    log.env(line["env"])
+    log.add("main", {"workload": wl.name, "op": args.op, "fwd_frac": line["fwd"]["frac_of_peak"],
+                     "bwd_frac": line["bwd"]["frac_of_peak"], "value": line["value"],
+                     "steady_frac": steady["frac"] if steady else None})
     if world == 1 and args.op == "norm" and not args.no_sweep:
-        line["sweep"] = run_sweep(pkg, torch, synth, args, local, l2, peak)
+        line["sweep"] = run_sweep(pkg, torch, synth, args, local, l2, peak, log)
     if world == 1 and args.op == "norm" and not args.no_configs:
         line["configs"] = run_configs(pkg, torch, synth, args, local, l2, peak,
-                                      skip=wl.name)
+                                      skip=wl.name, log=log)
     # the closing probe comes after every timed cell, so a drift across the
     # whole run shows ("What a tuned RMSNorm kernel actually costs on Hopper",
     # sections 02 and 08: opening and closing probes)
@@ -936,13 +996,19 @@ def steady_fields(cell, step_bytes: int, peak: float) -> dict:
     return {"steady_gbs": round(gbs, 1), "steady_frac": round(gbs / peak, 4)}
 
 
-def run_sweep(pkg, torch, synth, args, local, l2, peak):
+def run_sweep(pkg, torch, synth, args, local, l2, peak, log=None):
     """The width sweep (fixed M*N = 2^27, bf16 and fp32): each cell validated
     against PyTorch, then forward and backward timed after a clean cold L2,
-    as for the main workload. Fractions are of the measured copy bandwidth."""
+    as for the main workload. Fractions are of the measured copy bandwidth.
+    Cells `log` already holds (a resumed run) are taken from it."""
+    log = log or ResultsLog(None)
     cells = []
     for dt in (torch.bfloat16, torch.float32):
         for wl in synth.width_sweep(dt):
+            prev = log.done("sweep", wl.name)
+            if prev is not None:
+                cells.append({**prev, "resumed": True})
+                continue
             code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
             elem = torch.empty(0, dtype=wl.dtype).element_size()
             fb, bb = synth.logical_bytes(wl.M, wl.N, elem)
@@ -955,6 +1021,7 @@ def run_sweep(pkg, torch, synth, args, local, l2, peak):
                           "fwd_frac": round(fg / peak, 4), "bwd_frac": round(bg / peak, 4),
                           "fwd_bwd_gbs": round((fb + bb) / (c["step_ms"] * 1e-3) / 1e9, 1),
                           **steady_fields(c, fb + bb, peak)})
+            log.add("sweep", cells[-1])
             del c
     return {"steps": args.sweep_steps, "peak_gbs": peak, "cells": cells}
 
@@ -962,14 +1029,20 @@ def run_sweep(pkg, torch, synth, args, local, l2, peak):
 CONFIG_WORKLOADS = ("small_256x1024", "hidden8192_32768x8192_outliers", "qknorm_1048576x128")
 
 
-def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None):
+def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None, log=None):
     """The other named workloads (256 x 1024, which fits in L2 and is bound
     by latency; 32768 x 8192 with 0.1% outliers; QK-norm 1048576 x 128),
     each validated against PyTorch and timed like the main workload: clone
-    sets >= 3x L2, a clean cold L2 before every call, events per call."""
+    sets >= 3x L2, a clean cold L2 before every call, events per call.
+    Cells `log` already holds (a resumed run) are taken from it."""
+    log = log or ResultsLog(None)
     cells = []
     for name in CONFIG_WORKLOADS:
         if name == skip:
+            continue
+        prev = log.done("config", name)
+        if prev is not None:
+            cells.append({**prev, "resumed": True})
             continue
         wl = synth.WORKLOADS[name]
         code = pkg.dtype_code(wl.dtype, wl.weight_dtype)
@@ -989,6 +1062,7 @@ def run_configs(pkg, torch, synth, args, local, l2, peak, skip=None):
                       "bwd_variant": plan_b["variant_name"],
                       **steady_fields(c, fb + bb, peak),
                       "validation": c["errs"]})
+        log.add("config", cells[-1])
         del c
     return {"steps": args.config_steps, "peak_gbs": peak, "cells": cells}
 

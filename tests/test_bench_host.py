@@ -47,3 +47,22 @@ def test_steady_fields():
     assert bench.steady_fields({"steady": None}, 10**9, 1000.0) == {}
     got = bench.steady_fields({"steady": {"step_ms": 0.5}}, 10**9, 4000.0)
     assert got == {"steady_gbs": 2000.0, "steady_frac": 0.5}
+
+
+def test_results_log_resume(tmp_path):
+    d = str(tmp_path / "run")
+    log = bench.ResultsLog(d)
+    log.env({"gpu": "x"})
+    log.add("sweep", {"workload": "a", "fwd_frac": 1.0})
+    log.add("config", {"workload": "b", "bwd_frac": 0.9})
+    with open(tmp_path / "run" / "cells.jsonl", "a") as f:
+        f.write('{"kind": "sweep", "workload": "c", "fwd')  # cut off by an interruption
+    again = bench.ResultsLog(d, resume=True)
+    assert again.done("sweep", "a") == {"workload": "a", "fwd_frac": 1.0}
+    assert again.done("config", "b") == {"workload": "b", "bwd_frac": 0.9}
+    assert again.done("sweep", "c") is None and again.done("sweep", "b") is None
+    fresh = bench.ResultsLog(d)  # without --resume the old cells are dropped
+    assert fresh.done("sweep", "a") is None
+    assert not (tmp_path / "run" / "cells.jsonl").exists()
+    assert (tmp_path / "run" / "env.json").exists()
+    assert bench.ResultsLog(None).done("sweep", "a") is None
