@@ -249,11 +249,12 @@ const char *rmsnorm_status_string(int status);
 void rmsnorm_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Failure-injection hook for testing the bounded waits: the next backward
- * launch that stages rows through bulk copies will not issue the copy of
- * unit `unit` (a row, or a tile of rows for short rows), so the wait for it
- * runs out and the status word reads RMSNORM_ERR_DEVICE_TIMEOUT. Outputs of
- * that call are unspecified. One-shot; -1 cancels.
+ * Failure-injection hook for testing the bounded waits: the next launch
+ * that stages rows through bulk copies (a backward, or a forward that takes
+ * the persistent ring kernel) will not issue the copy of unit `unit` (a
+ * row, or a tile of rows for short rows), so the wait for it runs out and
+ * the status word reads RMSNORM_ERR_DEVICE_TIMEOUT. Outputs of that call are
+ * unspecified. One-shot; -1 cancels.
  */
 void rmsnorm_test_drop_copy(int64_t unit);
 

@@ -129,6 +129,7 @@ int fwd_run(const void* x, const void* res, const void* w, void* h, void* y, flo
         return RMSNORM_ERR_UNSUPPORTED;
     FwdArgs a{x, w, y, rstd, M, static_cast<int>(N), eps, dev->status_word, g_wait_limit_ns.load(),
               res, h};
+    a.drop_unit = plan.variant == RMSNORM_VARIANT_RING ? g_drop_unit.exchange(-1) : -1;
     return cuda_status(fwd_launch(plan, dtype, a, stream));
 }
 

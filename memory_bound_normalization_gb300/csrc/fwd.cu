@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
                                                       T* __restrict__ y, float* __restrict__ rstd,
                                                       int64_t M, int N, float eps, int stages,
                                                       int* status, uint64_t wait_limit_ns,
-                                                      const T* res, T* hout) {
+                                                      const T* res, T* hout, int64_t drop_unit) {
     using P = Pack<T>;
     // extents for the checked build: x, res, h, y; rstd
     [[maybe_unused]] const int64_t tbytes =
@@ -493,6 +493,7 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
             return;
         }
         mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(NT) * bytes);
+        if (cid + t * ncl == drop_unit) return;  // failure injection: this wait runs out
         const int64_t off = (cid + t * ncl) * N + static_cast<int64_t>(vbeg) * VEC;
         if (!RMSN_OK(span_in(x + off, bytes, x, tbytes) && smem_span_in(sx + s * unit, bytes) &&
                          (!ADD || (span_in(res + off, bytes, res, tbytes) &&
@@ -727,7 +728,7 @@ cudaError_t launch_ring(const rmsnorm_plan_t& p, const FwdArgs& a, cudaStream_t 
                      static_cast<const T*>(a.x),
                      static_cast<const TW*>(a.w), static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps,
                      p.stages, a.status, a.wait_limit_ns, static_cast<const T*>(a.res),
-                     static_cast<T*>(a.h));
+                     static_cast<T*>(a.h), a.drop_unit);
 }
 
 template <typename T, typename TW>

@@ -32,6 +32,7 @@ struct FwdArgs {
     uint64_t wait_limit_ns;
     const void* res;         // residual added to x first (nullptr: plain forward)
     void* h;                 // x + res as stored (written when res is set)
+    int64_t drop_unit = -1;  // failure-injection hook (ring kernel), -1 = off
 };
 
 struct BwdArgs {
