@@ -424,7 +424,10 @@ __host__ __device__ inline int fwd_ring_smem_bytes(int stages, int unit, int nt)
 // blocks of a cluster exchange their sums by st.async into a 4-slot ring of
 // exchange slots (as in the wide backward: a block sends row t + 1 only after
 // receiving every sum of row t, so a writer is at most three rows ahead of a
-// reader), and y is scaled from registers. Every wait is bounded.
+// reader), and y is scaled from registers. A 16-bit slice of 8 vectors a
+// thread does not fit in registers: it is read from its stage once for the
+// sum of squares and again for the scaling, and its stage is refilled after
+// the next row's block barrier (S - 1 rows ahead). Every wait is bounded.
 template <typename T, typename TW, int V, bool ADD>
 __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __restrict__ w,
                                                       T* __restrict__ y, float* __restrict__ rstd,
@@ -456,6 +459,10 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
     const uint32_t bytes = static_cast<uint32_t>(vcnt) * 16u;
     const int S = stages;
     const int unit = slots * 16;
+    // 16-bit slices of 8 vectors a thread are read from the stage twice (for
+    // the sum of squares, then for the scaling) instead of being held in
+    // registers, and their stage is refilled one row later
+    constexpr bool HOLD = !(V == 8 && sizeof(T) == 2);
 
     unsigned char* sx = smem;
     unsigned char* sr = smem + S * unit;  // residual (ADD only)
@@ -535,33 +542,44 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
                 report_status(status, kStatusTimeout);
             }
         }
-        // the slice into registers (h = x + res with ADD, stored to global)
-        uint4 xv[V];
+        // the slice (h = x + res with ADD, stored to global), into registers
+        // when held
+        uint4 xv[HOLD ? V : 1];
         float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
             const int k = j * nthr + tid;
-            xv[j] = k < vcnt ? ld_ring_16(sx + s * unit + k * 16, status)
-                             : make_uint4(0, 0, 0, 0);
+            uint4 v = k < vcnt ? ld_ring_16(sx + s * unit + k * 16, status) : make_uint4(0, 0, 0, 0);
             if constexpr (ADD) {
                 if (k < vcnt) {
-                    xv[j] = add_vec<T>(xv[j], ld_ring_16(sr + s * unit + k * 16, status));
+                    v = add_vec<T>(v, ld_ring_16(sr + s * unit + k * 16, status));
                     T* hd = hout + row * N + static_cast<int64_t>(vbeg + k) * VEC;
-                    if (RMSN_OK(span_in(hd, 16, hout, tbytes), status)) st_global_16(hd, xv[j]);
+                    if (RMSN_OK(span_in(hd, 16, hout, tbytes), status)) st_global_16(hd, v);
                 }
             }
+            if constexpr (HOLD) xv[j] = v;
             float2 f[PR];
-            P::unpack2(xv[j], f);
+            P::unpack2(v, f);
 #pragma unroll
             for (int e = 0; e < PR; ++e) ss2 = __ffma2_rn(f[e], f[e], ss2);
         }
         const float part = group_allreduce<32>(ss2.x + ss2.y);
         if (lane == 0) red[(t & 1) * 32 + warp] = part;
-        __syncthreads();  // the stage is read; the warp sums of row t are published
+        // a held slice's stage is read; a re-read slice's stage of row t - 1 is
+        // (its scaling came before this barrier); the warp sums of row t are
+        // published
+        __syncthreads();
         failed = *fail != 0;
-        if (tid == 0 && !failed && t + S < nrows) {
-            fence_proxy_async_shared();
-            issue(t + S);
+        if constexpr (HOLD) {
+            if (tid == 0 && !failed && t + S < nrows) {
+                fence_proxy_async_shared();
+                issue(t + S);
+            }
+        } else {
+            if (tid == 0 && !failed && t >= 1 && t + S - 1 < nrows) {
+                fence_proxy_async_shared();
+                issue(t + S - 1);
+            }
         }
         float tot = lane < nw ? red[(t & 1) * 32 + lane] : 0.f;
         tot = group_allreduce<32>(tot);
@@ -590,8 +608,15 @@ __global__ void __launch_bounds__(512) fwd_ring_kernel(const T* x, const TW* __r
         for (int j = 0; j < V; ++j) {
             const int k = j * nthr + tid;
             if (k >= vcnt) continue;
+            uint4 v;
+            if constexpr (HOLD) {
+                v = xv[j];
+            } else {
+                v = ld_ring_16(sx + s * unit + k * 16, status);
+                if constexpr (ADD) v = add_vec<T>(v, ld_ring_16(sr + s * unit + k * 16, status));
+            }
             float2 fx[PR], fw[PR], fy[PR];
-            P::unpack2(xv[j], fx);
+            P::unpack2(v, fx);
             WP::unpack2(wv[j], fw);
 #pragma unroll
             for (int e = 0; e < PR; ++e) fy[e] = __fmul2_rn(__fmul2_rn(fx[e], rs2), fw[e]);
@@ -828,13 +853,13 @@ cudaError_t ring_resident_units(const DeviceInfo& dev, const void* fn, int threa
 // Measured on GB300: bf16 rows do best in one block of up to 256 threads and,
 // wider, in the ring kernel (N = 12288: 94% against 82% for a block of 384
 // threads; N = 16384: 95% against 92%; N = 32768: 94% against 91% two-pass;
-// N = 65536: 92% against 86%); fp16 rows, the same bytes per element, follow
-// bf16. fp32
-// rows do best in blocks of at most 256 threads, then in clusters of 2, then
-// in the ring kernel (N = 16384: 96% against 90% for a cluster of 4; N =
-// 65536: 96% against 72% for a cluster of 8); with the residual, fp32 rows
-// stay in clusters, and every row the ring cannot hold takes the two-pass
-// kernel.
+// N = 65536: 92% against 86%; N = 196608 and 262144, 16-bit slices of 8
+// vectors: 94% and 91% against 74% and 70%); fp16 rows, the same bytes per
+// element, follow bf16. fp32 rows do best in blocks of at most 256 threads,
+// then in clusters of 2, then in the ring kernel (N = 16384: 96% against 90%
+// for a cluster of 4; N = 65536: 96% against 72% for a cluster of 8; wider,
+// up to 32768 vectors); with the residual, fp32 rows stay in clusters, and
+// every row the ring cannot hold takes the two-pass kernel.
 struct FwdTuning {
     int wide = -1;             // -1: per dtype; 0: two passes; 1: clusters; 2: ring
     int row_threads = 0;       // largest block holding a row (0: per dtype)
@@ -851,6 +876,9 @@ struct FwdTuning {
     // their forward at 94.6% and 84.8% of the copy roofline, against 96.2%
     // and 85.9% with 100 KB (other widths unchanged)
     int ring_max_budget = 100 * 1024;
+    // most vectors a thread of a 16-bit ring slice: 0 by width (below), 4, or
+    // 8 (the slice re-read from its stage, up to 4096 vectors a block)
+    int ring16_max_v = 0;
 };
 
 const FwdTuning& fwd_tuning() {
@@ -874,6 +902,8 @@ const FwdTuning& fwd_tuning() {
         if (ws && *ws) u.wide_select = std::max(0, std::min(2, atoi(ws)));
         const char* rb = getenv("RMSNORM_FWD_RING_MAX_BUDGET");
         if (rb && *rb) u.ring_max_budget = std::max(16 * 1024, std::min(227 * 1024, atoi(rb)));
+        const char* r16 = getenv("RMSNORM_FWD_RING16_V");
+        if (r16 && *r16) u.ring16_max_v = atoi(r16) >= 8 ? 8 : 4;
         const char* gm = getenv("RMSNORM_FWD_ROWGROUP_MAX_VEC");
         if (gm && *gm) u.rowgroup_max_vec = std::max(0, std::min(256, atoi(gm)));
         return u;
@@ -881,15 +911,32 @@ const FwdTuning& fwd_tuning() {
     return t;
 }
 
+// Most vectors a thread of a ring slice: 8 for 32-bit elements. A 16-bit
+// slice of 8 vectors is read from its stage twice (its unpacked pairs would
+// not fit in registers), which pays only where 4 vectors a thread would need
+// clusters of more than 4 blocks: rows wider than 8192 vectors. There,
+// clusters of 4 blocks of 8 vectors (up to 144 SMs busy) ran the forward at
+// 91-92% of the copy roofline for bf16 and fp16 N = 131072, against 76% for
+// 8 blocks of 4 vectors (15 clusters, 120 SMs), and bf16 N = 98304 at 94%
+// against 83%; at N = 65536 (91% against 94%) and 32768 (one block: cold
+// 95% against 92%, back to back 87% against 92%) 4 vectors stay.
+constexpr int64_t kRing16WideVec = 8192;
+
+int ring_max_v(int elem, int64_t nvec) {
+    if (elem == 4) return 8;
+    const int knob = fwd_tuning().ring16_max_v;
+    if (knob > 0) return knob;
+    return nvec > kRing16WideVec ? 8 : 4;
+}
+
 // The ring plan for rows of nvec vectors over c blocks: 4 vectors a thread,
-// or 8 for 32-bit elements where max_v allows it and 4 would need more than
-// 512 threads (with 16-bit elements the unpacked pairs of 8 vectors spill),
-// and as many stages, 3 to 6, as `budget` bytes of shared memory hold.
+// or 8 where max_v allows it and 4 would need more than 512 threads, and as
+// many stages, 3 to 6, as `budget` bytes of shared memory hold.
 bool ring_plan_c(int64_t nvec, int nt, int elem, int c, int max_v, int budget,
                  rmsnorm_plan_t* p) {
     constexpr int kSmemMax = 227 * 1024;
     const int64_t slots = cdiv(nvec, c);
-    if (slots > ((elem == 4 && max_v >= 8) ? 4096 : 2048)) return false;
+    if (slots > (max_v >= 8 ? 4096 : 2048)) return false;
     const int v = slots <= 2048 ? 4 : 8;
     const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
     const int unit = v * t * 16;
@@ -913,9 +960,10 @@ bool ring_plan_c(int64_t nvec, int nt, int elem, int c, int max_v, int budget,
 // (2 with the residual).
 bool fwd_ring_plan(int64_t nvec, int nt, int elem, rmsnorm_plan_t* p) {
     const FwdTuning& tu = fwd_tuning();
-    if (tu.ring_cluster > 0) return ring_plan_c(nvec, nt, elem, tu.ring_cluster, 8, tu.ring_smem, p);
+    const int max_v = ring_max_v(elem, nvec);
+    if (tu.ring_cluster > 0) return ring_plan_c(nvec, nt, elem, tu.ring_cluster, max_v, tu.ring_smem, p);
     for (int c = 1; c <= kMaxCluster; c *= 2)
-        if (ring_plan_c(nvec, nt, elem, c, 8, tu.ring_smem, p)) return true;
+        if (ring_plan_c(nvec, nt, elem, c, max_v, tu.ring_smem, p)) return true;
     return false;
 }
 
@@ -992,6 +1040,11 @@ void fwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool ad
             p->threads_per_row = p->threads * c;
             return;
         }
+        // fp32 rows too wide for a cluster of blocks that hold them: the
+        // ring kernel, 8 vectors a thread over up to 8 blocks (N = 98304 and
+        // 131072: 100% and 93% of the copy roofline against 60% and 57% for
+        // the two-pass kernel)
+        if (ladder && !add && fwd_ring_plan(nvec, 1, dtype_size(dtype), p)) return;
     }
     if (vector_ok) {
         p->variant = RMSNORM_VARIANT_TWO_PASS;
@@ -1039,11 +1092,15 @@ cudaError_t ring_select(const DeviceInfo& dev, int dtype, int64_t N, bool add, r
     int64_t best_score[3] = {-1, -1, -1};
     for (int c : {2, 4, 5, 6, 8}) {
         for (int max_v : {4, 8}) {
-            if (max_v == 8 && elem != 4) continue;
+            if (max_v > ring_max_v(elem, nvec)) continue;
             for (int budget : {100 * 1024, 200 * 1024}) {
-                if (budget > fwd_tuning().ring_max_budget) continue;
                 rmsnorm_plan_t q = *p;
                 if (!ring_plan_c(nvec, add ? 2 : 1, elem, c, max_v, budget, &q)) continue;
+                // past the budget cap only 16-bit slices of 8 vectors, whose
+                // three stages at 512 threads take 192 KB
+                if (budget > fwd_tuning().ring_max_budget &&
+                    !(elem == 2 && q.vectors_per_thread == 8))
+                    continue;
                 if (q.smem_bytes > dev.max_smem_optin) continue;
                 const void* fn = ring_kernel_for(dtype, q.vectors_per_thread, add);
                 if (fn == nullptr) continue;

@@ -206,6 +206,38 @@ def test_width_ladder(lib, N, dtype):
             assert p.smem_bytes >= (3 if res else 2) * p.stages * unit
 
 
+@pytest.mark.parametrize("dtype", [pkg.BF16, pkg.F16, pkg.BF16_W_F32, pkg.F16_W_F32],
+                         ids=["bf16", "f16", "bf16_wf32", "f16_wf32"])
+def test_ring_forward_16bit_slice_width(lib, dtype):
+    """16-bit ring slices hold 4 vectors a thread up to 8192 vectors a row
+    (N = 65536) and take 8, re-read from their stage, beyond it: clusters of
+    4 blocks at N = 98304 and 131072, 8 at 262144. The residual forward,
+    whose two tensors do not fit three stages of 8 vectors, keeps 4."""
+    for N, cluster, v, threads in ((32768, 2, 4, 512), (65536, 4, 4, 512), (98304, 4, 8, 384),
+                                   (131072, 4, 8, 512), (262144, 8, 8, 512)):
+        p = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD, -1)
+        assert pkg.VARIANTS[p.variant] == "ring"
+        assert (p.cluster, p.vectors_per_thread, p.threads) == (cluster, v, threads)
+        assert p.stages >= 3 and p.smem_bytes <= 227 * 1024
+    for N in (98304, 131072):
+        a = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD_ADD, -1)
+        assert pkg.VARIANTS[a.variant] == "ring" and a.vectors_per_thread == 4 and a.cluster == 8
+    assert pkg.VARIANTS[pkg.rmsnorm_plan(1000, 524288, dtype, pkg.PASS_FWD, -1).variant] == "two_pass"
+
+
+def test_ring_forward_fp32_past_clusters(lib):
+    """fp32 rows too wide for a cluster of blocks holding the row take the
+    ring at 8 vectors a thread up to 32768 vectors (N = 131072); the residual
+    forward and wider rows take the two-pass kernel."""
+    for N, threads in ((98304, 384), (131072, 512)):
+        p = pkg.rmsnorm_plan(1000, N, pkg.F32, pkg.PASS_FWD, -1)
+        assert pkg.VARIANTS[p.variant] == "ring"
+        assert (p.cluster, p.vectors_per_thread, p.threads) == (8, 8, threads)
+        a = pkg.rmsnorm_plan(1000, N, pkg.F32, pkg.PASS_FWD_ADD, -1)
+        assert pkg.VARIANTS[a.variant] == "two_pass"
+    assert pkg.VARIANTS[pkg.rmsnorm_plan(1000, 196608, pkg.F32, pkg.PASS_FWD, -1).variant] == "two_pass"
+
+
 def test_plan_rejects_bad_arguments(lib):
     with pytest.raises(pkg.RMSNormError):
         pkg.rmsnorm_plan(10, 0, pkg.BF16, pkg.PASS_FWD)
