@@ -25,6 +25,7 @@ constexpr int kSliceBudget = 64 * 1024;   // x+dy bytes of one row slice per sta
 constexpr int kSmemMax = 227 * 1024;      // dynamic shared memory a block may opt into
 constexpr int kMaxRowGroups = 8;          // named barriers 1..8 (0 is __syncthreads)
 constexpr int kClusterDwMax = 16;         // blocks of the one cluster that sums dw on chip
+constexpr int kClusterWideMax = 16;       // blocks of a cluster for rows 8 blocks cannot hold
 
 // Tuning overrides for sweeps (read once; unset = built-in ladder). They
 // change the persistent grid, hence the order of the dw sum: results stay
@@ -320,6 +321,19 @@ bool wide_plan(int64_t nvec, int nt, int c, int max_v, int st_min, int stages, i
 
 }  // namespace
 
+// Any alignment, any N: one block per row, scalar loads.
+static void scalar_plan(rmsnorm_plan_t* p) {
+    p->variant = RMSNORM_VARIANT_SCALAR;
+    p->cluster = 1;
+    p->row_groups = 1;
+    p->rows_per_unit = 1;
+    p->threads = 256;
+    p->threads_per_row = 256;
+    p->vectors_per_thread = 0;
+    p->stages = 0;
+    p->smem_bytes = 0;
+}
+
 // With res (the residual backward) the rings carry dres as a third tensor:
 // stages may drop to two before a row group or a ring is given up, and wide
 // rows may take a larger cluster. Plans without res are unchanged by it.
@@ -406,13 +420,16 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
             if (try_wide(c, min_stages)) return;
             if (!res || c >= kMaxCluster) break;
         }
+        // rows no cluster of 8 holds (past 256 KiB a row): a cluster of 16
+        // blocks, a size the device must allow (bwd_finish_plan falls back to
+        // the scalar kernel where it does not). On GB300 seven such clusters
+        // fit (112 SMs): bf16 N = 196608 and 262144 ran at 63% and 71% of the
+        // copy roofline, fp32 N = 131072 at 86%, against 6-21% for the scalar
+        // kernel (fp32 N = 98304 takes 8 blocks of 8 vectors with a two-deep
+        // ring in the device's choice: 101%)
+        if (tu.cluster == 0 && try_wide(kClusterWideMax, min_stages)) return;
     }
-    p->variant = RMSNORM_VARIANT_SCALAR;
-    p->threads = 256;
-    p->threads_per_row = 256;
-    p->vectors_per_thread = 0;
-    p->stages = 0;
-    p->smem_bytes = 0;
+    scalar_plan(p);
 }
 
 namespace {
@@ -495,6 +512,18 @@ cudaError_t bwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t
     const void* fn = main_kernel_for(dtype, *p, res);
     if (fn == nullptr) return cudaErrorInvalidValue;
     int units = 0;
+    if (p->cluster > kMaxCluster) {
+        // a non-portable cluster size: the scalar kernel where the device
+        // refuses it or cannot hold one such cluster
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess ||
+            resident_units(dev, fn, p->threads, p->smem_bytes, p->cluster, &units) != cudaSuccess) {
+            cudaGetLastError();
+            scalar_plan(p);
+            fn = main_kernel_for(dtype, *p, res);
+            if (fn == nullptr) return cudaErrorInvalidValue;
+        }
+    }
     cudaError_t err = resident_units(dev, fn, p->threads, p->smem_bytes, p->cluster, &units);
     if (err != cudaSuccess) return err;
     int64_t work = M;  // rows, tiles of rows, or rows per block's row groups

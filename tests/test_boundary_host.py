@@ -158,7 +158,9 @@ def test_width_ladder(lib, N, dtype):
         p = pkg.rmsnorm_plan(1000, N, dtype, pass_, -1)
         assert p.grid == 0  # no device queried
         assert p.threads % 32 == 0 and 32 <= p.threads <= 1024
-        assert 1 <= p.cluster <= 8
+        # clusters of 16 (a non-portable size) only for backward rows that 8
+        # blocks cannot hold
+        assert 1 <= p.cluster <= 8 or (p.cluster == 16 and pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES))
         assert p.smem_bytes <= 227 * 1024
         name = pkg.VARIANTS[p.variant]
         if not vector_ok:
@@ -189,10 +191,10 @@ def test_width_ladder(lib, N, dtype):
             nt = 2 if pass_ == pkg.PASS_FWD_ADD else 1
             assert p.smem_bytes >= nt * p.stages * p.vectors_per_thread * p.threads * 16
         else:
-            # the backward's vector kernels cover every row up to 256 KiB;
-            # wider rows outgrow shared memory
+            # the backward's vector kernels cover every row up to 512 KiB
+            # (clusters of 16 past 256 KiB); wider rows outgrow shared memory
             assert name == "scalar" and pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES)
-            assert N * (16 // vec) > 256 * 1024
+            assert N * (16 // vec) > 512 * 1024
         if pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES) and name != "scalar":
             # the residual backward's rings carry dres too and may be 2 deep, as
             # may an fp32 row over a cluster of 5 blocks of 8 vectors a thread
@@ -236,6 +238,22 @@ def test_ring_forward_fp32_past_clusters(lib):
         a = pkg.rmsnorm_plan(1000, N, pkg.F32, pkg.PASS_FWD_ADD, -1)
         assert pkg.VARIANTS[a.variant] == "two_pass"
     assert pkg.VARIANTS[pkg.rmsnorm_plan(1000, 196608, pkg.F32, pkg.PASS_FWD, -1).variant] == "two_pass"
+
+
+@pytest.mark.parametrize("dtype,N,threads,stages", [
+    (pkg.BF16, 196608, 384, 4), (pkg.BF16, 262144, 512, 3), (pkg.F16_W_F32, 262144, 512, 3),
+    (pkg.F32, 98304, 384, 4), (pkg.F32, 131072, 512, 3)])
+def test_backward_cluster_of_16(lib, dtype, N, threads, stages):
+    """Rows of 256..512 KiB, which no cluster of 8 holds with a three-deep
+    ring, split over 16 blocks of 4 vectors a thread (the residual backward
+    with a two-deep ring); wider rows stay scalar."""
+    p = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_BWD, -1)
+    assert pkg.VARIANTS[p.variant] == "cluster_row"
+    assert (p.cluster, p.vectors_per_thread, p.threads, p.stages) == (16, 4, threads, stages)
+    r = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_BWD_RES, -1)
+    assert pkg.VARIANTS[r.variant] == "cluster_row" and (r.cluster, r.stages) == (16, 2)
+    wider = pkg.rmsnorm_plan(1000, 2 * 262144, dtype, pkg.PASS_BWD, -1)
+    assert pkg.VARIANTS[wider.variant] == "scalar"
 
 
 def test_plan_rejects_bad_arguments(lib):

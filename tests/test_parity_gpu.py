@@ -123,7 +123,9 @@ def test_device_chosen_wide_shapes(N, dtype, w_dtype):
         name = pkg.VARIANTS[p.variant]
         if name not in ("ring", "cluster_row"):
             continue
-        assert p.cluster in (1, 2, 4, 5, 6, 8) and 32 <= p.threads <= 512
+        assert p.cluster in (1, 2, 4, 5, 6, 8, 16) and 32 <= p.threads <= 512
+        if p.cluster == 16:  # backward rows that 8 blocks cannot hold
+            assert pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES) and N * (16 // vec) > 256 * 1024
         assert p.threads * p.vectors_per_thread * p.cluster * vec >= N
         assert p.vectors_per_thread in (4, 8)
         if dtype != torch.float32 and (name != "ring" or N <= 65536):
@@ -174,6 +176,30 @@ def test_forward_ring_rows_around_grid(N, dtype, w_dtype):
     plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_FWD, 0)
     assert pkg.VARIANTS[plan.variant] == "ring" and plan.vectors_per_thread == 8
     units = plan.grid // plan.cluster
+    for M in sorted({max(1, units - 1), units + 1, (plan.stages + 1) * units + 3}):
+        inp, eps = inputs(M, N, dtype, seed=M % 3, w_dtype=w_dtype)
+        out = run(inp["x"], inp["w"], inp["dy"], eps)
+        check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
+
+
+WIDEST = [(196608, torch.bfloat16, None), (262144, torch.bfloat16, None),
+          (262144, torch.float16, torch.float32), (98304, torch.float32, None),
+          (131072, torch.float32, None)]
+
+
+@pytest.mark.parametrize("N,dtype,w_dtype", WIDEST,
+                         ids=[f"{n}-{str(d)[6:]}" + ("-wf32" if w else "") for n, d, w in WIDEST])
+def test_backward_cluster_of_16(N, dtype, w_dtype):
+    """Rows of 256..512 KiB in the backward: a cluster of 16 blocks (the
+    exchange of row sums over 16 peers), or for fp32 rows the 8 blocks of 8
+    vectors with a two-deep ring that the device's choice may prefer. M
+    around the number of resident clusters and several rows per cluster."""
+    code = pkg.dtype_code(dtype, w_dtype)
+    plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_BWD, 0)
+    assert pkg.VARIANTS[plan.variant] == "cluster_row"
+    assert plan.cluster == 16 or (dtype == torch.float32 and plan.cluster == 8)
+    units = plan.grid // plan.cluster
+    assert plan.partial_rows == units
     for M in sorted({max(1, units - 1), units + 1, (plan.stages + 1) * units + 3}):
         inp, eps = inputs(M, N, dtype, seed=M % 3, w_dtype=w_dtype)
         out = run(inp["x"], inp["w"], inp["dy"], eps)

@@ -145,6 +145,25 @@ def test_rows_around_residual_grid(N, dtype, w_dtype):
         check_bwd(h, w, dy, dres, eps, dx, dw, rows=rows)
 
 
+@pytest.mark.parametrize("N,dtype", [(262144, torch.bfloat16), (131072, torch.float32)],
+                         ids=["262144-bf16", "131072-f32"])
+def test_residual_backward_cluster_of_16(N, dtype):
+    """The residual backward over rows a cluster of 8 cannot hold: 16 blocks
+    with dres as a third tensor in a two-deep ring, M around the number of
+    resident clusters."""
+    code = pkg.dtype_code(dtype, None)
+    plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_BWD_RES, 0)
+    assert pkg.VARIANTS[plan.variant] == "cluster_row" and plan.cluster in (8, 16)
+    P = plan.partial_rows
+    for M in sorted({max(1, P - 1), 3 * P + 2}):
+        x, res, w, dy, dres, eps = inputs(M, N, dtype, None, seed=M % 5)
+        h, y, rstd = run_fwd(x, res, w, eps)
+        check_fwd(x, res, w, eps, h, y, rstd)
+        for g in (dres, None):
+            dx, dw = run_bwd(h, w, dy, rstd, g)
+            check_bwd(h, w, dy, g, eps, dx, dw)
+
+
 @pytest.mark.parametrize("dtype,w_dtype", TYPES, ids=TYPE_IDS)
 @pytest.mark.parametrize("N", [128, 4104])
 def test_residual_unaligned(N, dtype, w_dtype):
