@@ -284,7 +284,8 @@ typedef enum {
     RMSNORM_VARIANT_ROWGROUP = 1,  /* short rows: a sub-warp or warp per row */
     RMSNORM_VARIANT_CTA_ROW = 2,   /* one thread block per row */
     RMSNORM_VARIANT_CLUSTER_ROW = 3, /* a thread-block cluster per row */
-    RMSNORM_VARIANT_SCALAR = 4,    /* unaligned or ragged rows */
+    RMSNORM_VARIANT_SCALAR = 4,    /* unaligned or ragged rows, and backward
+                                      rows over 512 KiB */
     RMSNORM_VARIANT_TWO_PASS = 5,  /* wide rows (forward): a block per row,
                                       two passes, the second served by L2 */
     RMSNORM_VARIANT_RING = 6       /* wide rows (forward): persistent blocks
@@ -306,7 +307,10 @@ typedef struct {
     int threads_per_row;    /* lanes sharing one row (ROWGROUP), else threads */
     int rows_per_unit;      /* rows per block pass (row-group tile, or row
                                groups); TWO_PASS: blocks per SM */
-    int cluster;            /* blocks per row (1 unless CLUSTER_ROW or RING);
+    int cluster;            /* blocks per row (1 unless CLUSTER_ROW or RING),
+                               at most 8, or 16 for backward rows over 256
+                               KiB (a non-portable cluster size: on a device
+                               that refuses it they run SCALAR);
                                backward ROWGROUP / CTA_ROW with cluster > 1:
                                the grid is one cluster of that many blocks,
                                which sums dw on chip (few rows) */
