@@ -913,14 +913,18 @@ const FwdTuning& fwd_tuning() {
 
 // Most vectors a thread of a ring slice: 8 for 32-bit elements. A 16-bit
 // slice of 8 vectors is read from its stage twice (its unpacked pairs would
-// not fit in registers), which pays only where 4 vectors a thread would need
-// clusters of more than 4 blocks: rows wider than 8192 vectors. There,
+// not fit in registers), which pays where 4 vectors a thread would need
+// clusters of more than 4 blocks, rows wider than 8192 vectors (and for one
+// block of 256-384 threads, fwd_ring_plan). There,
 // clusters of 4 blocks of 8 vectors (up to 144 SMs busy) ran the forward at
 // 91-92% of the copy roofline for bf16 and fp16 N = 131072, against 76% for
 // 8 blocks of 4 vectors (15 clusters, 120 SMs), and bf16 N = 98304 at 94%
 // against 83%; at N = 65536 (91% against 94%) and 32768 (one block: cold
 // 95% against 92%, back to back 87% against 92%) 4 vectors stay.
 constexpr int64_t kRing16WideVec = 8192;
+// 16-bit rows one block takes at 8 vectors a thread (below)
+constexpr int64_t kRing16OneBlockMin = 2048;
+constexpr int64_t kRing16OneBlockMax = 3072;
 
 int ring_max_v(int elem, int64_t nvec) {
     if (elem == 4) return 8;
@@ -930,14 +934,15 @@ int ring_max_v(int elem, int64_t nvec) {
 }
 
 // The ring plan for rows of nvec vectors over c blocks: 4 vectors a thread,
-// or 8 where max_v allows it and 4 would need more than 512 threads, and as
-// many stages, 3 to 6, as `budget` bytes of shared memory hold.
+// or 8 where max_v allows it and 4 would need more than 512 threads (or
+// where want_v8 asks for it), and as many stages, 3 to 6, as `budget` bytes
+// of shared memory hold.
 bool ring_plan_c(int64_t nvec, int nt, int elem, int c, int max_v, int budget,
-                 rmsnorm_plan_t* p) {
+                 rmsnorm_plan_t* p, bool want_v8 = false) {
     constexpr int kSmemMax = 227 * 1024;
     const int64_t slots = cdiv(nvec, c);
     if (slots > (max_v >= 8 ? 4096 : 2048)) return false;
-    const int v = slots <= 2048 ? 4 : 8;
+    const int v = (slots > 2048 || (want_v8 && max_v >= 8)) ? 8 : 4;
     const int t = std::max(32, round_up(static_cast<int>(cdiv(slots, v)), 32));
     const int unit = v * t * 16;
     int stages = std::min(6, budget / (nt * unit));
@@ -961,6 +966,19 @@ bool ring_plan_c(int64_t nvec, int nt, int elem, int c, int max_v, int budget,
 bool fwd_ring_plan(int64_t nvec, int nt, int elem, rmsnorm_plan_t* p) {
     const FwdTuning& tu = fwd_tuning();
     const int max_v = ring_max_v(elem, nvec);
+    // 16-bit rows of 2048-3072 vectors (N = 16384-24576), no residual: one
+    // block of 256-384 threads at 8 vectors a thread, the slice read twice
+    // from a ring at least four stages deep. Against 512 threads at 4 vectors
+    // (N = 16384) or clusters of 2 (wider) it ran the forward at 97 / 97%
+    // (cold / back to back) against 96 / 85% for bf16 N = 16384, 97 / 99%
+    // against 94 / 91% at 18432, and 93-95 / 85-86% against 93 / 83-85% at
+    // 20480 and 24576; fp16 N = 16384 lost 2.6 points cold (94%) and gained
+    // 1.3 on the forward + backward step. Three stages (wider rows) lost back
+    // to back, and fewer than 256 threads (narrower rows) lost both ways.
+    if (tu.ring_cluster == 0 && tu.ring16_max_v != 4 && elem == 2 && nt == 1 &&
+        nvec >= kRing16OneBlockMin && nvec <= kRing16OneBlockMax &&
+        ring_plan_c(nvec, nt, elem, 1, 8, tu.ring_smem, p, true) && p->stages >= 4)
+        return true;
     if (tu.ring_cluster > 0) return ring_plan_c(nvec, nt, elem, tu.ring_cluster, max_v, tu.ring_smem, p);
     for (int c = 1; c <= kMaxCluster; c *= 2)
         if (ring_plan_c(nvec, nt, elem, c, max_v, tu.ring_smem, p)) return true;

@@ -211,11 +211,15 @@ def test_width_ladder(lib, N, dtype):
 @pytest.mark.parametrize("dtype", [pkg.BF16, pkg.F16, pkg.BF16_W_F32, pkg.F16_W_F32],
                          ids=["bf16", "f16", "bf16_wf32", "f16_wf32"])
 def test_ring_forward_16bit_slice_width(lib, dtype):
-    """16-bit ring slices hold 4 vectors a thread up to 8192 vectors a row
-    (N = 65536) and take 8, re-read from their stage, beyond it: clusters of
-    4 blocks at N = 98304 and 131072, 8 at 262144. The residual forward,
-    whose two tensors do not fit three stages of 8 vectors, keeps 4."""
-    for N, cluster, v, threads in ((32768, 2, 4, 512), (65536, 4, 4, 512), (98304, 4, 8, 384),
+    """16-bit ring slices take 8 vectors a thread, re-read from their stage,
+    in one block of 256-384 threads for rows of 2048-3072 vectors (N = 16384
+    to 24576) and past 8192 vectors (clusters of 4 blocks at N = 98304 and
+    131072, 8 at 262144); 4 vectors elsewhere (one block of up to 448 threads
+    below 2048 vectors, clusters from 24584 to 65536). The residual forward,
+    whose two tensors do not fit its stages at 8 vectors, keeps 4."""
+    for N, cluster, v, threads in ((12288, 1, 4, 384), (14336, 1, 4, 448), (16384, 1, 8, 256),
+                                   (20480, 1, 8, 320), (24576, 1, 8, 384), (24584, 2, 4, 416),
+                                   (32768, 2, 4, 512), (65536, 4, 4, 512), (98304, 4, 8, 384),
                                    (131072, 4, 8, 512), (262144, 8, 8, 512)):
         p = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD, -1)
         assert pkg.VARIANTS[p.variant] == "ring"
@@ -224,6 +228,9 @@ def test_ring_forward_16bit_slice_width(lib, dtype):
     for N in (98304, 131072):
         a = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD_ADD, -1)
         assert pkg.VARIANTS[a.variant] == "ring" and a.vectors_per_thread == 4 and a.cluster == 8
+    for N in (16384, 24576):
+        a = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD_ADD, -1)
+        assert pkg.VARIANTS[a.variant] == "ring" and a.vectors_per_thread == 4
     assert pkg.VARIANTS[pkg.rmsnorm_plan(1000, 524288, dtype, pkg.PASS_FWD, -1).variant] == "two_pass"
 
 

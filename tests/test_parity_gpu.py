@@ -128,10 +128,13 @@ def test_device_chosen_wide_shapes(N, dtype, w_dtype):
             assert pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES) and N * (16 // vec) > 256 * 1024
         assert p.threads * p.vectors_per_thread * p.cluster * vec >= N
         assert p.vectors_per_thread in (4, 8)
-        if dtype != torch.float32 and (name != "ring" or N <= 65536):
-            # 16-bit rows: 8 vectors a thread only in the forward ring past
-            # 8192 vectors (the slice re-read from its stage)
-            assert p.vectors_per_thread == 4
+        if dtype != torch.float32 and p.vectors_per_thread == 8:
+            # 16-bit rows: 8 vectors a thread (the slice re-read from its
+            # stage) only in the forward ring, in one block for 2048-3072
+            # vectors a row and past 8192 vectors
+            nvec = N // 8
+            assert name == "ring" and pass_ == pkg.PASS_FWD
+            assert (p.cluster == 1 and 2048 <= nvec <= 3072) or nvec > 8192
         assert p.smem_bytes <= 227 * 1024
         assert p.grid % p.cluster == 0 and p.grid > 0
         if name == "ring" or pass_ in (pkg.PASS_BWD, pkg.PASS_BWD_RES):
@@ -158,20 +161,21 @@ def test_wide_rows_around_cluster_grid(N, dtype, w_dtype=None):
         check_all(inp["x"], inp["w"], inp["dy"], eps, *out)
 
 
-RING_GRID = [(N, dt, wdt) for N in (98304, 131072)
+RING_GRID = [(N, dt, wdt) for N in (16384, 24576, 98304, 131072)
              for dt, wdt in ((torch.bfloat16, None), (torch.float16, None),
-                             (torch.bfloat16, torch.float32), (torch.float32, None))] + \
-            [(262144, torch.bfloat16, None)]
+                             (torch.bfloat16, torch.float32), (torch.float32, None))
+             if N > 65536 or dt != torch.float32] + [(262144, torch.bfloat16, None)]
 
 
 @pytest.mark.parametrize("N,dtype,w_dtype", RING_GRID,
                          ids=[f"{n}-{str(d)[6:]}" + ("-wf32" if w else "") for n, d, w in RING_GRID])
 def test_forward_ring_rows_around_grid(N, dtype, w_dtype):
-    """The persistent forward over rows wider than 8192 vectors at 8 vectors a
-    thread (16-bit slices are read from the ring stage twice and their stage
-    is refilled one row late; fp32 slices are held in registers): M around
-    the number of resident clusters and several rows per cluster (more than
-    the ring's stages), so that every stage is refilled and reused."""
+    """The persistent forward at 8 vectors a thread: 16-bit rows of 2048-3072
+    vectors in one block and rows wider than 8192 vectors in clusters (16-bit
+    slices are read from the ring stage twice and their stage is refilled one
+    row late; fp32 slices are held in registers). M around the number of
+    resident blocks or clusters and several rows each (more than the ring's
+    stages), so that every stage is refilled and reused."""
     code = pkg.dtype_code(dtype, w_dtype)
     plan = pkg.rmsnorm_plan(1 << 20, N, code, pkg.PASS_FWD, 0)
     assert pkg.VARIANTS[plan.variant] == "ring" and plan.vectors_per_thread == 8
