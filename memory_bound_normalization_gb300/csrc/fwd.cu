@@ -913,10 +913,10 @@ const FwdTuning& fwd_tuning() {
 
 // Most vectors a thread of a ring slice: 8 for 32-bit elements. A 16-bit
 // slice of 8 vectors is read from its stage twice (its unpacked pairs would
-// not fit in registers), which pays where 4 vectors a thread would need
-// clusters of more than 4 blocks, rows wider than 8192 vectors (and for one
-// block of 256-384 threads, fwd_ring_plan). There,
-// clusters of 4 blocks of 8 vectors (up to 144 SMs busy) ran the forward at
+// not fit in registers), which pays in one block of 256-384 threads
+// (fwd_ring_plan) and where 4 vectors a thread would need clusters of more
+// than 4 blocks, rows wider than 8192 vectors. There, clusters of 4 blocks
+// of 8 vectors (up to 144 SMs busy) ran the forward at
 // 91-92% of the copy roofline for bf16 and fp16 N = 131072, against 76% for
 // 8 blocks of 4 vectors (15 clusters, 120 SMs), and bf16 N = 98304 at 94%
 // against 83%; at N = 65536 (91% against 94%) and 32768 (one block: cold
@@ -976,9 +976,13 @@ bool fwd_ring_plan(int64_t nvec, int nt, int elem, rmsnorm_plan_t* p) {
     // 1.3 on the forward + backward step. Three stages (wider rows) lost back
     // to back, and fewer than 256 threads (narrower rows) lost both ways.
     if (tu.ring_cluster == 0 && tu.ring16_max_v != 4 && elem == 2 && nt == 1 &&
-        nvec >= kRing16OneBlockMin && nvec <= kRing16OneBlockMax &&
-        ring_plan_c(nvec, nt, elem, 1, 8, tu.ring_smem, p, true) && p->stages >= 4)
-        return true;
+        nvec >= kRing16OneBlockMin && nvec <= kRing16OneBlockMax) {
+        rmsnorm_plan_t q = *p;
+        if (ring_plan_c(nvec, nt, elem, 1, 8, tu.ring_smem, &q, true) && q.stages >= 4) {
+            *p = q;
+            return true;
+        }
+    }
     if (tu.ring_cluster > 0) return ring_plan_c(nvec, nt, elem, tu.ring_cluster, max_v, tu.ring_smem, p);
     for (int c = 1; c <= kMaxCluster; c *= 2)
         if (ring_plan_c(nvec, nt, elem, c, max_v, tu.ring_smem, p)) return true;
