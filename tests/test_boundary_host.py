@@ -4,9 +4,12 @@ makes consistent choices. No kernel is launched here."""
 from __future__ import annotations
 
 import ctypes
+import json
 import math
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -232,6 +235,33 @@ def test_ring_forward_16bit_slice_width(lib, dtype):
         a = pkg.rmsnorm_plan(1000, N, dtype, pkg.PASS_FWD_ADD, -1)
         assert pkg.VARIANTS[a.variant] == "ring" and a.vectors_per_thread == 4
     assert pkg.VARIANTS[pkg.rmsnorm_plan(1000, 524288, dtype, pkg.PASS_FWD, -1).variant] == "two_pass"
+
+
+def _child_plans(env: dict, shapes) -> list:
+    """Forward plans of (N, dtype code) pairs in a child process with extra
+    environment variables (the tuning knobs are read once per process)."""
+    code = ("import json, sys, memory_bound_normalization_gb300 as p; p.load_library(); "
+            "out = [p.rmsnorm_plan(1000, n, d, p.PASS_FWD, -1).as_dict() for n, d in "
+            "json.loads(sys.argv[1])]; print(json.dumps(out))")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "-c", code, json.dumps(shapes)], cwd=root,
+                         env={**os.environ, **env}, capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stderr[-2000:]
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def test_ring16_knob(lib):
+    """RMSNORM_FWD_RING16_V=4 restores 4-vector 16-bit ring slices everywhere
+    (one block of 512 threads at N = 16384, clusters of 2 at 20480, of 8 at
+    131072); =8 keeps the width rule's plans."""
+    shapes = [[16384, pkg.BF16], [20480, pkg.F16], [131072, pkg.BF16]]
+    four = _child_plans({"RMSNORM_FWD_RING16_V": "4"}, shapes)
+    assert [(p["cluster"], p["vectors_per_thread"], p["threads"]) for p in four] == \
+        [(1, 4, 512), (2, 4, 320), (8, 4, 512)]
+    eight = _child_plans({"RMSNORM_FWD_RING16_V": "8"}, shapes)
+    assert [(p["cluster"], p["vectors_per_thread"], p["threads"]) for p in eight] == \
+        [(1, 8, 256), (1, 8, 320), (4, 8, 512)]
+    assert all(p["variant_name"] == "ring" for p in four + eight)
 
 
 def test_ring_forward_fp32_past_clusters(lib):
