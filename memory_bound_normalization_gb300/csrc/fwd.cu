@@ -327,10 +327,15 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
     for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
         const T* xr = x + row * N;
         float2 ss2 = make_float2(0.f, 0.f);
-        for (int base = 0; base < nvec; base += nthr * U) {
-            uint4 v[U];
+        // pass 1 of a plain fp32 row keeps 16 vectors a thread in flight: with
+        // 4 (or 8) the 1024-thread block streamed too little to fill HBM
+        // (fp32 N = 196608 and 262144: 62% and 60% of the copy roofline
+        // against 52% and 49%; 16-bit rows did not move)
+        constexpr int U1 = (sizeof(T) == 4 && !ADD) ? 16 : U;
+        for (int base = 0; base < nvec; base += nthr * U1) {
+            uint4 v[U1];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < U1; ++u) {
                 const int k = base + u * nthr + tid;
                 v[u] = k < nvec ? ld_global_16_hint(xr + static_cast<int64_t>(k) * VEC, keep)
                                 : make_uint4(0, 0, 0, 0);
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(1024) fwd_wide_kernel(const T* x, const TW* __
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < U1; ++u) {
                 float2 f[PR];
                 P::unpack2(v[u], f);
 #pragma unroll
@@ -1176,7 +1181,8 @@ cudaError_t fwd_finish_plan(const DeviceInfo& dev, int dtype, int64_t M, int64_t
             p->grid = static_cast<int>(M * p->cluster);
             break;
         case RMSNORM_VARIANT_TWO_PASS:
-            // rows_per_unit blocks per SM walk all rows
+            // rows_per_unit blocks per SM walk all rows (a smaller grid, to keep
+            // fewer rows in L2, ran slower in proportion at N = 196608..1048576)
             p->grid = static_cast<int>(
                 std::min<int64_t>(M, static_cast<int64_t>(p->rows_per_unit) * dev.sm_count));
             break;

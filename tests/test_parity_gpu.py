@@ -77,7 +77,7 @@ SHAPES = [(1, 8), (3, 13), (33, 257), (5, 16), (7, 32), (100, 64), (130, 128), (
           (19, 512), (256, 1024), (11, 2048), (9, 2880), (6, 4096), (3, 5120), (5, 6144),
           (2, 7168), (4, 8192),
           (3, 16384), (3, 20480), (5, 24576), (2, 32768), (3, 40960), (4, 49152), (3, 57344),
-          (2, 65536), (1, 65536), (2, 98304), (3, 131072),
+          (2, 65536), (1, 65536), (2, 98304), (3, 131072), (2, 196608), (1, 524288),
           (1000, 40), (777, 96)]
 
 
