@@ -427,7 +427,9 @@ void bwd_choose(int64_t N, int dtype, bool vector_ok, rmsnorm_plan_t* p, bool re
         // copy roofline, fp32 N = 131072 at 86%, against 6-21% for the scalar
         // kernel (fp32 N = 98304 takes 8 blocks of 8 vectors with a two-deep
         // ring in the device's choice: 101%)
-        if (tu.cluster == 0 && try_wide(kClusterWideMax, min_stages)) return;
+        if (tu.cluster == 0 &&
+            (try_wide(kClusterWideMax, min_stages) || (sz == 4 && !res && try_wide(kClusterWideMax, 2))))
+            return;
     }
     scalar_plan(p);
 }

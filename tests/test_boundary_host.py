@@ -202,7 +202,8 @@ def test_width_ladder(lib, N, dtype):
             # the residual backward's rings carry dres too and may be 2 deep, as
             # may an fp32 row over a cluster of 5 blocks of 8 vectors a thread
             res = pass_ == pkg.PASS_BWD_RES
-            two_deep = res or (dtype == pkg.F32 and p.cluster == 5 and p.vectors_per_thread == 8)
+            two_deep = res or (dtype == pkg.F32 and p.cluster in (5, 16) and
+                               p.vectors_per_thread == 8)
             assert (2 if two_deep else 3) <= p.stages <= 6
             if name == "rowgroup":
                 unit = p.rows_per_unit * N * (16 // vec)
@@ -291,6 +292,20 @@ def test_backward_cluster_of_16(lib, dtype, N, threads, stages):
     assert pkg.VARIANTS[r.variant] == "cluster_row" and (r.cluster, r.stages) == (16, 2)
     wider = pkg.rmsnorm_plan(1000, 2 * 262144, dtype, pkg.PASS_BWD, -1)
     assert pkg.VARIANTS[wider.variant] == "scalar"
+
+
+def test_backward_fp32_cluster_of_16_two_deep(lib):
+    """fp32 rows past 131072, up to 229376, take 16 blocks of 8 vectors a thread
+    with a two-deep ring (the residual backward, a third tensor, does not fit
+    and stays scalar); wider rows stay scalar."""
+    for N, threads in ((163840, 320), (196608, 384), (229376, 448)):
+        p = pkg.rmsnorm_plan(1000, N, pkg.F32, pkg.PASS_BWD, -1)
+        assert pkg.VARIANTS[p.variant] == "cluster_row"
+        assert (p.cluster, p.vectors_per_thread, p.threads, p.stages) == (16, 8, threads, 2)
+        assert p.smem_bytes <= 227 * 1024
+        r = pkg.rmsnorm_plan(1000, N, pkg.F32, pkg.PASS_BWD_RES, -1)
+        assert pkg.VARIANTS[r.variant] == "scalar"
+    assert pkg.VARIANTS[pkg.rmsnorm_plan(1000, 262144, pkg.F32, pkg.PASS_BWD, -1).variant] == "scalar"
 
 
 def test_plan_rejects_bad_arguments(lib):

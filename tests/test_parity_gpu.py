@@ -188,7 +188,7 @@ def test_forward_ring_rows_around_grid(N, dtype, w_dtype):
 
 WIDEST = [(196608, torch.bfloat16, None), (262144, torch.bfloat16, None),
           (262144, torch.float16, torch.float32), (98304, torch.float32, None),
-          (131072, torch.float32, None)]
+          (131072, torch.float32, None), (196608, torch.float32, None)]
 
 
 @pytest.mark.parametrize("N,dtype,w_dtype", WIDEST,
