@@ -285,7 +285,8 @@ typedef enum {
     RMSNORM_VARIANT_CTA_ROW = 2,   /* one thread block per row */
     RMSNORM_VARIANT_CLUSTER_ROW = 3, /* a thread-block cluster per row */
     RMSNORM_VARIANT_SCALAR = 4,    /* unaligned or ragged rows, and backward
-                                      rows over 512 KiB */
+                                      rows wider than 262144 16-bit or
+                                      229376 fp32 elements */
     RMSNORM_VARIANT_TWO_PASS = 5,  /* wide rows (forward): a block per row,
                                       two passes, the second served by L2 */
     RMSNORM_VARIANT_RING = 6       /* wide rows (forward): persistent blocks
